@@ -1,0 +1,221 @@
+"""Pins for the planner, boundary metadata, tile maps and loss probe oracles (CPU only)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import loss as ol
+from oracle import packing as op
+from oracle import tiles as ot
+
+hyp = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+
+def test_three_sample_metadata(golden_dir):
+    fx = json.load(open(os.path.join(golden_dir, "three_samples_layout.json")))
+    cu, pos, seg, mx = op.build_metadata(fx["lengths"])
+    assert cu.tolist() == fx["cu_seqlens"]
+    assert pos.tolist() == fx["position_ids"]
+    assert seg.tolist() == [0] * 5 + [1] * 3 + [2] * 4
+    assert mx == fx["max_seqlen"]
+    # boundary compilation (blog section 3) inverts the positions, both readings
+    for at_min in (False, True):
+        cu2, mx2 = op.cu_seqlens_from_position_ids(pos, reset_at_min=at_min)
+        assert cu2.tolist() == fx["cu_seqlens"] and mx2 == fx["max_seqlen"]
+    # positions that start at 1 need the minimum-based reading
+    cu3, _ = op.cu_seqlens_from_position_ids(pos + 1, reset_at_min=True)
+    assert cu3.tolist() == fx["cu_seqlens"]
+
+
+def test_tail_pad_segment():
+    cu, pos, seg, mx = op.build_metadata([3, 2], pad_to=8)
+    assert cu.tolist() == [0, 3, 5, 8]
+    assert pos.tolist() == [0, 1, 2, 0, 1, 0, 1, 2]
+    assert seg.tolist() == [0, 0, 0, 1, 1, 2, 2, 2] and mx == 3
+    cu, _, _, _ = op.build_metadata([3, 5], pad_to=8)      # exact fill: no pad segment
+    assert cu.tolist() == [0, 3, 8]
+    with pytest.raises(ValueError):
+        op.build_metadata([5, 5], pad_to=8)
+
+
+def test_nine_target_rows(golden_dir):
+    """Course 'Fill only the current row': next-fit at capacity 6 gives rows 3+2 and 4."""
+    fx = json.load(open(os.path.join(golden_dir, "nine_target_fixture.json")))
+    lengths = [len(x) for x in fx["pair_inputs"]]
+    assert lengths == [3, 2, 4]
+    assert op.next_fit(lengths, fx["capacity"]) == [[0, 1], [2]]
+    rows = op.packed_storage_rows(fx["pair_inputs"], fx["pair_targets"], fx["capacity"])
+    assert rows["inputs"] == fx["rows_inputs"]
+    assert rows["targets"] == fx["rows_targets"]
+    assert rows["segments"] == fx["rows_segments"]
+    assert rows["positions"] == fx["rows_positions"]
+    assert rows["input_valid"] == fx["rows_valid"]
+    assert sum(map(len, rows["inputs"])) == fx["stored_cells"]
+    assert sum(map(sum, rows["target_valid"])) == fx["real_targets"]
+    # each real row is one segment list of the metadata oracle; pad cells sit outside
+    for r, pack in enumerate(op.next_fit(lengths, fx["capacity"])):
+        cu, pos, seg, _ = op.build_metadata([lengths[i] for i in pack])
+        n = int(cu[-1])
+        assert pos.tolist() == fx["rows_positions"][r][:n]
+
+
+def test_nine_target_permissions(golden_dir):
+    """B's first query (column 3) may use only column 3; its second uses columns 3 and 4."""
+    fx = json.load(open(os.path.join(golden_dir, "nine_target_fixture.json")))
+    seg, pos, val = fx["rows_segments"][0], fx["rows_positions"][0], fx["rows_valid"][0]
+
+    def allowed(i, j):
+        return val[i] and val[j] and seg[i] == seg[j] and pos[j] <= pos[i]
+    c = fx["b_first_query_column"]
+    assert [j for j in range(6) if allowed(c, j)] == fx["b_first_query_allowed_keys"]
+    assert [j for j in range(6) if allowed(c + 1, j)] == fx["b_second_query_allowed_keys"]
+
+
+def test_nine_target_loss_probe(golden_dir):
+    """Token-weighted loss = 11 ln2 / 9 = 0.847180 (sum 7.624619); the row-mean and the
+    document-mean weightings give 0.831777 and 0.924196 and must not be what we compute."""
+    fx = json.load(open(os.path.join(golden_dir, "nine_target_fixture.json")))
+    V = fx["vocab"]
+    tg = np.asarray(fx["rows_targets"]).reshape(-1)
+    seg = np.asarray(fx["rows_segments"]).reshape(-1)
+    elig = np.asarray(fx["rows_valid"]).reshape(-1)
+    qmap = {int(k): v for k, v in fx["gold_probability_by_segment"].items()}
+    qcell = [qmap.get(int(s), 0.5) for s in seg]
+    z = ol.constructed_logits(tg, elig, qcell, V)
+    s, mean, grad = ol.token_weighted_loss(z, tg, elig)
+    p = 10 ** -fx["printed_decimals"]
+    assert abs(s - fx["loss_sum_printed"]) < p and abs(s - 11 * math.log(2)) < 1e-12
+    assert abs(mean - fx["loss_mean_printed"]) < p
+    assert abs(mean - 11 * math.log(2) / 9) < 1e-12
+    assert abs(mean - fx["row_mean_printed"]) > 1e-3
+    assert abs(mean - fx["document_mean_printed"]) > 1e-3
+    # the two wrong weightings reproduce the page's other printed numbers
+    nll = -np.log(np.asarray(qcell))[elig]
+    rows = np.asarray(fx["rows_valid"])
+    row_means = [nll[:rows[0].sum()].mean(), nll[rows[0].sum():].mean()]
+    assert abs(np.mean(row_means) - fx["row_mean_printed"]) < p
+    segs = seg[elig]
+    doc_means = [nll[segs == d].mean() for d in (0, 1, 2)]
+    assert abs(np.mean(doc_means) - fx["document_mean_printed"]) < p
+    # gradient against torch autograd of the same objective
+    import torch
+    tz = torch.tensor(z, requires_grad=True)
+    idx = torch.tensor(np.nonzero(elig)[0])
+    lm = torch.nn.functional.cross_entropy(tz[idx], torch.tensor(tg)[idx], reduction="mean")
+    lm.backward()
+    assert np.allclose(grad, tz.grad.numpy(), atol=1e-15, rtol=1e-12)
+    assert np.all(grad[~elig] == 0)
+    with pytest.raises(ValueError):
+        ol.token_weighted_loss(z, tg, np.zeros_like(elig))
+
+
+def test_next_fit_rules():
+    assert op.next_fit([3, 3, 6, 1], 6) == [[0, 1], [2], [3]]   # exact fill opens no extra row
+    assert op.next_fit([], 6) == []
+    with pytest.raises(ValueError):
+        op.next_fit([7], 6)                                      # never split
+    with pytest.raises(ValueError):
+        op.next_fit([0], 6)
+
+
+def test_best_fit_decreasing_small():
+    # sorted: 5(i1) 4(i0) 3(i3) 2(i2) 2(i4) 1(i5)
+    assert op.best_fit_decreasing([4, 5, 2, 3, 2, 1], 6) == [[1, 5], [0, 2], [3, 4]]
+    assert op.best_fit_decreasing([2, 2, 2], 6) == [[0, 1, 2]]
+    # two bins with equal room: the earlier one wins
+    assert op.best_fit_decreasing([3, 3, 1], 4) == [[0, 2], [1]]
+
+
+def _bfd_brute(lengths, cap):
+    """Independent restatement: one pass per item over explicit bin contents."""
+    order = sorted(range(len(lengths)), key=lambda i: (-lengths[i], i))
+    bins = []
+    for i in order:
+        cands = [(cap - sum(lengths[j] for j in b), n) for n, b in enumerate(bins)]
+        cands = [c for c in cands if c[0] >= lengths[i]]
+        if cands:
+            bins[min(cands)[1]].append(i)
+        else:
+            bins.append([i])
+    return bins
+
+
+@settings(max_examples=150, deadline=None)
+@given(st.lists(st.integers(1, 50), max_size=60), st.integers(50, 120))
+def test_planner_properties(lengths, cap):
+    for packs in (op.next_fit(lengths, cap), op.best_fit_decreasing(lengths, cap)):
+        flat = sorted(i for p in packs for i in p)
+        assert flat == list(range(len(lengths)))                 # multiset preserved
+        assert all(sum(lengths[i] for i in p) <= cap for p in packs)
+        assert all(p for p in packs)
+    nf = op.next_fit(lengths, cap)
+    assert [i for p in nf for i in p] == list(range(len(lengths)))   # order kept
+    for a, b in zip(nf, nf[1:]):                                 # b's first did not fit a
+        assert sum(lengths[i] for i in a) + lengths[b[0]] > cap
+    assert op.best_fit_decreasing(lengths, cap) == _bfd_brute(lengths, cap)
+
+
+# ----------------------------------------------------------------- tile maps
+
+def _allowed_edges(cu):
+    e = set()
+    for b in range(len(cu) - 1):
+        for i in range(cu[b], cu[b + 1]):
+            for j in range(cu[b], i + 1):
+                e.add((i, j))
+    return e
+
+
+@pytest.mark.parametrize("BM,BN", [(2, 2), (4, 2), (2, 4), (128, 128), (256, 128)])
+@pytest.mark.parametrize("seed", range(4))
+def test_fwd_tile_map_covers_each_allowed_edge_once(BM, BN, seed):
+    """Course 'History': tile traversal visits the same permitted edges as query order."""
+    rng = np.random.default_rng(seed)
+    lengths = rng.integers(1, 3 * max(BM, BN) // 2 + 2, size=5).tolist()
+    cu, _, _, _ = op.build_metadata(lengths)
+    H = 2
+    tm = ot.fwd_tile_map(cu, H, BM, BN)
+    allowed = _allowed_edges(cu.tolist())
+    for h in range(H):
+        seen = []
+        for it in tm[tm[:, 2] == h]:
+            cover = ot.fwd_item_edges(cu, it, BM, BN)
+            hit = [e for e in cover if e in allowed]
+            assert hit, "a listed tile has no permitted edge"
+            seen.extend(hit)
+            b, m, _, nb = it
+            s, l = cu[b], cu[b + 1] - cu[b]
+            last_row = s + min(l, (m + 1) * BM) - 1
+            assert (last_row, s + (nb - 1) * BN) in allowed      # last kv tile is needed
+        assert sorted(seen) == sorted(allowed)                  # each edge exactly once
+    keys = [(-r[3], r[0], r[1], r[2]) for r in tm]
+    assert keys == sorted(keys)
+
+
+@pytest.mark.parametrize("BM,BN", [(2, 2), (2, 4), (4, 2), (128, 128), (64, 128)])
+def test_bwd_tile_map_covers_each_allowed_edge_once(BM, BN):
+    lengths = [5, 1, 9, 3, 260, 130]
+    cu, _, _, _ = op.build_metadata(lengths)
+    tm = ot.bwd_tile_map(cu, 1, BM, BN)
+    allowed = _allowed_edges(cu.tolist())
+    seen = []
+    for b, n, _h, nq in tm:
+        s, l = cu[b], cu[b + 1] - cu[b]
+        m0 = -(-l // BM) - nq
+        cols = range(s + n * BN, s + min(l, (n + 1) * BN))
+        rows = range(s + m0 * BM, s + l)
+        hit = [(i, j) for i in rows for j in cols if (i, j) in allowed]
+        assert hit
+        seen.extend(hit)
+        # rows before m0 * BM see none of these keys
+        assert all((i, j) not in allowed for i in range(s, s + m0 * BM) for j in cols)
+    assert sorted(seen) == sorted(allowed)
+
+
+def test_tile_map_noncausal_counts():
+    cu = [0, 300, 301]
+    tm = ot.fwd_tile_map(cu, 1, 128, 128, causal=False)
+    assert tm.tolist() == [[0, 0, 0, 3], [0, 1, 0, 3], [0, 2, 0, 3], [1, 0, 0, 1]]
