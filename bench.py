@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the packed-sequence varlen causal attention hot path on GB300.
+
+One step = the whole path over one batch of synthetic packs: host packing
+planner (next-fit), then per pack the metadata kernel, the forward (contract
+check, tile plan, attention) and the backward (contract check, tile plans,
+rowsum, dK/dV, dQ).  The batch is the first 16 next-fit packs of 8192 tokens
+(segment lengths uniform in [32, 2048], tail padded to 8192), Hq = Hkv = 32,
+d = 128, bf16, causal.  Every pack's q/k/v/dO (256 MB) is larger than L2, so
+no flush is needed between steps.
+
+Metric: in-segment causal FLOPs per second, fwd 4*d*Hq*E + bwd 10*d*Hq*E with
+E = sum over real documents of l(l+1)/2 (the tail pad segment is computed but
+not credited), in TFLOP/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torch.distributed.run; each rank runs its own packs
+(independent replicas, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "varlen causal attn fwd+bwd TFLOP/s (in-segment FLOPs), % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "sft8k"
+PACKS_PER_STEP = 16
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def edges(lengths):
+    return sum(l * (l + 1) // 2 for l in lengths)
+
+
+def batch_packs(rank: int, planner):
+    """Doc lengths (without pad) of this rank's packs, with the workload.
+
+    ``planner(lengths, capacity)`` returns packs as index lists: the library's
+    next-fit for our arm, the oracle's for the CPU legs.
+    """
+    w = si.WORKLOADS[WORKLOAD]
+    raw = si.raw_lengths(WORKLOAD).tolist()
+    packs = [[raw[i] for i in p] for p in planner(raw, w.capacity)]
+    idx = [(rank * PACKS_PER_STEP + i) % len(packs) for i in range(PACKS_PER_STEP)]
+    return [packs[i] for i in idx], idx, w
+
+
+def flops_of(docs, pad_to, d, Hq):
+    e_doc = edges(docs)
+    pad = pad_to - sum(docs)
+    e_all = e_doc + (edges([pad]) if pad > 0 else 0)
+    return {"fwd": 4 * d * Hq * e_doc, "bwd": 10 * d * Hq * e_doc,
+            "e_doc": e_doc, "e_all": e_all}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows]
+        pw = [num(r[3]) for r in rows]
+        busy = [s for s, p in zip(sm, pw) if p == p and p > 0.25 * max(pw)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import packed_sequence_varlen_gb300 as va
+    from packed_sequence_varlen_gb300 import _lib
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = _lib.load()
+    packs, idx, w = batch_packs(rank, va.pack_next_fit)
+    d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to
+    fl = [flops_of(p, T, d, Hq) for p in packs]
+    step_flops = sum(f["fwd"] + f["bwd"] for f in fl)
+
+    # device-resident inputs
+    ins = []
+    for pi, docs in zip(idx, packs):
+        q, k, v, do = si.tensors(T, Hq, Hkv, d, seed_offset=1000 * pi)
+        ins.append(tuple(x.to(dev) for x in (q, k, v, do)))
+    lens_dev = [torch.tensor(p, dtype=torch.int32, device=dev) for p in packs]
+    all_docs = [L for p in packs for L in p]
+    B = [len(p) + (1 if sum(p) < T else 0) for p in packs]
+    mxs = [max(p + ([T - sum(p)] if sum(p) < T else [])) for p in packs]
+    ws_f = torch.empty(va.workspace_size(T, max(B), Hq, Hkv, d, T, False), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(va.workspace_size(T, max(B), Hq, Hkv, d, T, True), dtype=torch.uint8, device=dev)
+    outs = [(torch.empty_like(i[0]), torch.empty((Hq, T), dtype=torch.float32, device=dev),
+             torch.empty_like(i[0]), torch.empty_like(i[1]), torch.empty_like(i[2])) for i in ins]
+
+    def step():
+        # host planner over the batch's documents (its packs match the resident lengths)
+        va.pack_next_fit(all_docs, w.capacity)
+        for p in range(len(packs)):
+            q, k, v, do = ins[p]
+            o, lse, dq, dk, dv = outs[p]
+            cu, _, _, _, _ = va.build_metadata(lens_dev[p], pad_to=T, T_capacity=T)
+            cu = cu[:B[p] + 1]
+            va.varlen_attn_fwd(q, k, v, cu, mxs[p], None, True, out=o, lse=lse, workspace=ws_f)
+            va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs[p], None, True, dq=dq, dk=dk, dv=dv,
+                               workspace=ws_b)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if va.read_status(ws_f) or va.read_status(ws_b):
+        raise RuntimeError("device status error during warm-up")
+
+    n_launch_cap = args.steps * PACKS_PER_STEP * 16 + 64
+    lib.varlen_profile_enable(n_launch_cap)
+    lc0 = lib.varlen_launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        start.record()
+        for _ in range(args.steps):
+            step()
+        stop.record()
+        barrier()
+    launches = lib.varlen_launch_count() - lc0
+    elapsed_ms = start.elapsed_time(stop)
+    import ctypes
+    ids = (ctypes.c_int32 * n_launch_cap)()
+    ms = (ctypes.c_float * n_launch_cap)()
+    cnt = ctypes.c_int32()
+    lib.varlen_profile_read(ids, ms, n_launch_cap, ctypes.byref(cnt))
+    lib.varlen_profile_enable(0)
+    per_kernel = {}
+    for i in range(cnt.value):
+        name = lib.varlen_kernel_name(ids[i]).decode()
+        t, c = per_kernel.get(name, (0.0, 0))
+        per_kernel[name] = (t + ms[i], c + 1)
+
+    max_ms = elapsed_ms
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+    total_flops = step_flops * args.steps * world
+    value = total_flops / (max_ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel: algorithmic flops per launch / launch time
+    peaks = load_peaks()
+    e_all = sum(f["e_all"] for f in fl) * args.steps
+    kernel_flops = {"fwd": 4 * d * Hq * e_all, "bwd_dkdv": 8 * d * Hq * e_all,
+                    "bwd_dq": 6 * d * Hq * e_all}
+    dom = max(per_kernel, key=lambda k: per_kernel[k][0])
+    roof = None
+    if dom in kernel_flops:
+        ach = kernel_flops[dom] / (per_kernel[dom][0] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 2),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16_tflops_sustained"], 4),
+                "peak_kind": f"bf16 sustained, {peaks['source']}",
+                "traffic": None,
+                "launches": per_kernel[dom][1],
+                "avg_launch_us": round(per_kernel[dom][0] / per_kernel[dom][1] * 1e3, 2)}
+    kernel_table = {k: {"launches": c, "total_ms": round(t, 3),
+                        "share": round(t / max(sum(x[0] for x in per_kernel.values()), 1e-9), 4)}
+                    for k, (t, c) in sorted(per_kernel.items(), key=lambda kv: -kv[1][0])}
+    fwd_t = per_kernel.get("fwd", (0.0, 1))[0]
+    fwd_tflops = 4 * d * Hq * sum(f["e_doc"] for f in fl) * args.steps / (fwd_t * 1e-3) / 1e12 if fwd_t else None
+
+    e2e = run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier) if not args.no_e2e else None
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(max_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: first {PACKS_PER_STEP} next-fit packs of 8192 tokens "
+                               "(lengths U[32,2048], tail padded), Hq=Hkv=32, d=128, causal, fwd+bwd",
+                   "tokens_per_step": PACKS_PER_STEP * T, "packs_per_step": PACKS_PER_STEP,
+                   "l2": "inputs larger than L2 (256 MB per pack)",
+                   "parallelism": f"replicas x{world}",
+                   "pct_of_bf16_peak_burst": round(100 * value / world / peaks["bf16_tflops"], 2),
+                   "fwd_kernel_tflops": round(fwd_tflops, 2) if fwd_tflops else None},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "kernels": kernel_table,
+        "roofline": roof,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    return result
+
+
+def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier):
+    """Same step through the public API from pinned HOST buffers: H2D of every pack's q/k/v/dO
+    and lengths, the step, D2H of dq/dk/dv, all inside the timed region."""
+    import torch
+    d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to
+    host_in = []
+    for pi in idx:
+        q, k, v, do = si.tensors(T, Hq, Hkv, d, seed_offset=1000 * pi)
+        host_in.append(tuple(x.pin_memory() for x in (q, k, v, do)))
+    host_len = [torch.tensor(p, dtype=torch.int32).pin_memory() for p in packs]
+    host_out = tuple(torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory() for H in (Hq, Hkv, Hkv))
+    dev_in = [torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv, Hq)]
+    lens_dev = torch.empty(max(len(p) for p in packs), dtype=torch.int32, device=dev)
+    o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    g = [torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv)]
+    all_docs = [L for p in packs for L in p]
+    h2d = sum(x.numel() * x.element_size() for t in host_in for x in t) + sum(x.numel() * 4 for x in host_len)
+    d2h = len(packs) * sum(x.numel() * x.element_size() for x in host_out)
+
+    def step():
+        va.pack_next_fit(all_docs, w.capacity)
+        for p in range(len(packs)):
+            for dst, src in zip(dev_in, host_in[p]):
+                dst.copy_(src, non_blocking=True)
+            n = len(packs[p])
+            lens_dev[:n].copy_(host_len[p], non_blocking=True)
+            cu, _, _, mx, _ = va.build_metadata(lens_dev[:n], pad_to=T, T_capacity=T)
+            Bp = n + (1 if sum(packs[p]) < T else 0)
+            mxs = max(packs[p] + ([T - sum(packs[p])] if sum(packs[p]) < T else []))
+            cu = cu[:Bp + 1]
+            q, k, v, do = dev_in
+            va.varlen_attn_fwd(q, k, v, cu, mxs, None, True, out=o, lse=lse)
+            va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs, None, True, dq=g[0], dk=g[1], dv=g[2])
+            for dst, src in zip(host_out, g):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    barrier()
+    dt = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([dt], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": round(step_flops * args.steps * world / dt / 1e12, 3), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def cpu_baseline(budget_s: float = 12.0, steps: int | None = None):
+    """The float64 CPU oracle as it stands, on sft8k pack 0, one kv head at a time, fwd+bwd."""
+    from oracle import attention as oa
+    from oracle import packing as op
+    packs, idx, w = batch_packs(0, op.next_fit)
+    docs = packs[0]
+    T = w.pad_to
+    segs = docs + ([T - sum(docs)] if sum(docs) < T else [])
+    cu = np.cumsum([0] + segs)
+    q, k, v, do = si.tensors(T, w.Hq, w.Hkv, w.d, seed_offset=1000 * idx[0])
+    qq, kk, vv, dd = (si.to_f64(x) for x in (q, k, v, do))
+    per_head = 14 * w.d * edges(docs)           # one q head, real documents only
+    heads, t_total, times = 0, 0.0, []
+    while (steps is None and t_total < budget_s and heads < w.Hkv) or (steps is not None and heads < steps):
+        h = heads % w.Hkv
+        t0 = time.perf_counter()
+        o, lse = oa.varlen_forward(qq, kk, vv, cu, None, True, [h])
+        oa.varlen_backward(qq, kk, vv, o, lse, dd, cu, None, True, [h])
+        dt = time.perf_counter() - t0
+        times.append(dt)
+        t_total += dt
+        heads += 1
+    value = per_head * heads / t_total / 1e12
+    return {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{WORKLOAD} pack 0 ({len(docs)} documents + pad, T={T}), {heads} of "
+                      f"{w.Hq} heads, fwd+bwd, numpy float64 (BLAS on all cores)",
+            "seconds": round(t_total, 2), "step_times_s": [round(x, 3) for x in times]}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, one kv head of pack 0 per step."""
+    if rank != 0:
+        return None
+    from oracle import attention as oa
+    from oracle import packing as op
+    packs, idx, w = batch_packs(0, op.next_fit)
+    docs = packs[0]
+    T = w.pad_to
+    segs = docs + ([T - sum(docs)] if sum(docs) < T else [])
+    cu = np.cumsum([0] + segs)
+    q, k, v, do = si.tensors(T, w.Hq, w.Hkv, w.d, seed_offset=1000 * idx[0])
+    qq, kk, vv, dd = (si.to_f64(x) for x in (q, k, v, do))
+    per_step = 14 * w.d * edges(docs)
+
+    def step(i):
+        h = i % w.Hkv
+        o, lse = oa.varlen_forward(qq, kk, vv, cu, None, True, [h])
+        oa.varlen_backward(qq, kk, vv, o, lse, dd, cu, None, True, [h])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt / 1e12
+    sample = (f"{WORKLOAD} pack 0 ({len(docs)} documents + pad, T={T}), one of {w.Hq} heads per "
+              "step, fwd+bwd, numpy float64 (BLAS on all cores)")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{WORKLOAD}: one head of pack 0 per step (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

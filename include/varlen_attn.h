@@ -1,0 +1,234 @@
+/*
+ * varlen_attn.h -- C ABI of the GB300 (sm_103a) packed-sequence attention library.
+ *
+ * The library computes block-diagonal causal attention over a padding-free
+ * packed token stream.  Q, K, V and O share one token axis of length T
+ * ([T, H, d], the last dim contiguous) and the int32 boundary array
+ * cu_seqlens[B+1] cuts that axis into B independent segments
+ * [cu_seqlens[b], cu_seqlens[b+1]); no [T, T] mask is ever built.
+ *   Source: "Packing与 FlashAttention Varlen", section 1 (mental model: physical
+ *   continuity, logical discontinuity), section 3 (the cumulative-boundary
+ *   contract) and section 5 (per-segment address domain and tile bounds);
+ *   "Pack sequences without joining their contexts", "Permission depends on
+ *   the example" (block-causal permission rule).
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns every buffer.  Apart from the host planner's
+ *     own bookkeeping, the library allocates nothing; workspaces are sized with
+ *     varlen_attn_workspace_size() and passed in.  Outputs are overwritten.
+ *   - Pointers named *_dev are device pointers; the others are host pointers.
+ *   - Asynchrony: device calls are enqueued on the caller's stream and return
+ *     at once.  The return code covers what the host can check (arguments,
+ *     sizes, alignment, launch errors).  What only the device can see (a
+ *     cu_seqlens that breaks the contract, a bounded wait that gave up) is
+ *     written as a va_status into the int32 status word at byte 0 of the
+ *     workspace; read it after synchronising (varlen_read_status()).  Kernels
+ *     that find a non-zero status do no work.
+ *   - Errors never trap, abort or throw across the ABI.  varlen_last_error()
+ *     gives a message for the last failing call on this host thread.
+ *   - dtypes: q, k, v, out, dout, dq, dk, dv are bf16; lse is fp32 [Hq, T].
+ *   - Alignment: base pointers 16-byte aligned; row and head strides (in
+ *     elements) multiples of 8; d in {64, 128}; Hq % Hkv == 0 (q head h reads
+ *     kv head h / (Hq / Hkv)).
+ */
+#ifndef VARLEN_ATTN_H
+#define VARLEN_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* va_stream_t; /* a cudaStream_t; NULL is the legacy default stream */
+
+typedef enum {
+  VA_OK = 0,
+  VA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad alignment or stride */
+  VA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, Hq % Hkv != 0, ... */
+  VA_ERR_WORKSPACE = 3,    /* workspace smaller than varlen_attn_workspace_size() */
+  VA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  VA_ERR_BAD_SEQLENS = 5,  /* cu_seqlens breaks the contract (device-detected or host) */
+  VA_ERR_TIMEOUT = 6,      /* a bounded device wait gave up (device-detected) */
+  VA_ERR_CAPACITY = 7      /* planner: a document longer than the pack capacity */
+} va_status;
+
+/* Shape and strides of one packed call.  Strides are in elements.
+ * Source: "Packing与 FlashAttention Varlen", section 5 (per-segment views with
+ * row stride and head stride over the flat token axis). */
+typedef struct {
+  int32_t T;          /* tokens in the stream (= cu_seqlens[B]) */
+  int32_t B;          /* segments, cu_seqlens has B+1 entries */
+  int32_t Hq, Hkv, d; /* query heads, key/value heads, head dim */
+  int32_t max_seqlen; /* upper bound of cu_seqlens[b+1]-cu_seqlens[b]; sizes plans */
+  int64_t q_row_stride, q_head_stride;
+  int64_t k_row_stride, k_head_stride;
+  int64_t v_row_stride, v_head_stride;
+  int64_t o_row_stride, o_head_stride; /* out, dout, dq use these; dk/dv use k's */
+} va_shape;
+
+/* Fills the strides of a contiguous [T, H, d] layout. */
+void varlen_shape_contiguous(va_shape* s, int32_t T, int32_t B, int32_t Hq, int32_t Hkv,
+                             int32_t d, int32_t max_seqlen);
+
+/* ---------------------------------------------------------------- host planner
+ * Order-preserving next-fit.  Source: "Packing与 FlashAttention Varlen",
+ * section 2 (the sequential strategy); "Pack sequences without joining their
+ * contexts", "Fill only the current row" and "Extend the existing storage and
+ * decoder" (a new pack starts when a document does not fit the space left; a
+ * document longer than the capacity is an error, never split; an exact fill
+ * opens no extra pack).
+ *   lengths[n]        host, document lengths (> 0)
+ *   order[n]          host out: document indices grouped by pack (pack order,
+ *                     then order inside the pack)
+ *   pack_offsets[n+1] host out: pack p holds order[pack_offsets[p] .. pack_offsets[p+1])
+ *   n_packs           host out
+ * Errors: VA_ERR_INVALID_ARG (null, n < 0, capacity <= 0, length <= 0),
+ *         VA_ERR_CAPACITY (a length > capacity).  Synchronous, host only. */
+va_status varlen_pack_next_fit(const int32_t* lengths, int32_t n, int32_t capacity,
+                               int32_t* order, int32_t* pack_offsets, int32_t* n_packs);
+
+/* Best-fit-decreasing.  Source: "Packing与 FlashAttention Varlen", section 2
+ * (the default binpack strategy, which maximises fill and may reorder).  The
+ * page fixes no tie rule; this library sorts by length descending then index,
+ * puts each document in the open pack with the least room that still fits it
+ * (ties: the earliest pack), else opens a pack; packs keep their opening order
+ * and documents their insertion order.  Arguments and errors as next-fit.
+ * O(n log n). */
+va_status varlen_pack_best_fit_decreasing(const int32_t* lengths, int32_t n, int32_t capacity,
+                                          int32_t* order, int32_t* pack_offsets,
+                                          int32_t* n_packs);
+
+/* ---------------------------------------------------------------- metadata kernel
+ * Builds the boundary metadata of one pack on the device.  Source:
+ * "Packing与 FlashAttention Varlen", section 2 (packing_row: positions restart
+ * at 0 per sample) and section 3 (cu_seqlens: int32, first 0, last T, strictly
+ * increasing; max_seqlen = max diff); "Pack sequences without joining their
+ * contexts", "Fill only the current row" (occurrence segment ids).
+ *   lengths_dev[n]        device, segment lengths in stream order (> 0)
+ *   pad_to                if > sum(lengths), a tail pad segment of the
+ *                         difference is appended (its positions are 0..p-1);
+ *                         0 for none.  The host knows sum(lengths) when it
+ *                         packs, so it knows B = n (+1 with a pad).
+ *   cu_seqlens_dev[n+2]   device out; entry n+1 equals entry n when there is no pad
+ *   position_ids_dev[T]   device out, T = max(sum, pad_to)
+ *   segment_ids_dev[T]    device out
+ *   max_seqlen_dev[1]     device out
+ *   status_dev[1]         device out: 0, or VA_ERR_BAD_SEQLENS for a length <= 0
+ *                         or pad_to < sum
+ *   T_capacity            elements available in position_ids_dev/segment_ids_dev
+ * Errors: VA_ERR_INVALID_ARG, VA_ERR_CUDA.  Asynchronous. */
+va_status varlen_build_metadata(const int32_t* lengths_dev, int32_t n, int32_t pad_to,
+                                int32_t T_capacity, int32_t* cu_seqlens_dev,
+                                int32_t* position_ids_dev, int32_t* segment_ids_dev,
+                                int32_t* max_seqlen_dev, int32_t* status_dev, va_stream_t stream);
+
+/* Checks the cumulative-boundary contract on the device ("Packing与
+ * FlashAttention Varlen", section 3): cu[0] == 0, cu[B] == T, strictly
+ * increasing, every length <= max_seqlen.  Writes VA_ERR_BAD_SEQLENS into
+ * *status_dev on a violation (leaves it untouched otherwise).  Asynchronous. */
+va_status varlen_validate_cu_seqlens(const int32_t* cu_seqlens_dev, int32_t B, int32_t T,
+                                     int32_t max_seqlen, int32_t* status_dev,
+                                     va_stream_t stream);
+
+/* ---------------------------------------------------------------- tile scheduler
+ * Tile sizes the attention kernels use (BM query rows x BN key rows for
+ * kind 0 = forward map; BM x BN for kind 1 = backward kv map; kind 2 = the
+ * backward dQ map).  Host only. */
+va_status varlen_attn_tile_sizes(int32_t kind, int32_t d, int32_t* BM, int32_t* BN);
+
+/* Bytes of workspace varlen_attn_fwd (for_bwd = 0) or varlen_attn_bwd
+ * (for_bwd = 1) needs for this shape.  Depends on T, B, Hq, Hkv, d, max_seqlen. */
+size_t varlen_attn_workspace_size(const va_shape* shape, int32_t for_bwd);
+
+/* Builds a tile map on the device.  Source: "Packing与 FlashAttention
+ * Varlen", section 5 (a q block exists only while m*BM < l; its key blocks
+ * stop at ceil(min(l, (m+1)*BM)/BN) when causal, ceil(l/BN) otherwise); the
+ * order -- longest first, ties by (segment, block, head) -- is this library's
+ * reading, the page fixes none.
+ *   kind 0: records {segment, q block, q head, n key blocks}
+ *   kind 1: records {segment, kv block, kv head, n q blocks} where the q blocks
+ *           of a kv block n start at floor(n*BN/BM) (causal)
+ *   kind 2: as kind 0 with the dQ kernel's tile sizes
+ *   tile_map_dev    device out, int32 [capacity][4]
+ *   n_items_dev     device out, int32
+ *   capacity        records available; VA_ERR_WORKSPACE if the bound
+ *                   (ceil(T/BM)+B)*heads exceeds it
+ * Asynchronous. */
+va_status varlen_attn_plan(const va_shape* shape, const int32_t* cu_seqlens_dev, int32_t kind,
+                           int32_t causal, int32_t* tile_map_dev, int32_t capacity,
+                           int32_t* n_items_dev, va_stream_t stream);
+
+/* ---------------------------------------------------------------- attention
+ * Forward.  Source: "Packing与 FlashAttention Varlen", section 5 (each segment
+ * b reads Q/K/V at offset cu[b]*row_stride with extent cu[b+1]-cu[b]; the
+ * output is written at Q's offsets, so O has the input's flat order) and
+ * section 1 (three independent attentions for [0,5,8,12]).  Per segment, q
+ * head h, kv head h/(Hq/Hkv):
+ *     s_ij = scale * q_i . k_j  (j <= i when causal, j in the segment),
+ *     lse_i = ln sum_j exp(s_ij),  o_i = sum_j exp(s_ij - lse_i) v_j.
+ *   q_dev [T,Hq,d], k_dev/v_dev [T,Hkv,d]  bf16 in, strides from shape
+ *   cu_seqlens_dev [B+1]                   int32 in
+ *   scale                                  usually 1/sqrt(d)
+ *   out_dev [T,Hq,d] bf16 out;  lse_dev [Hq,T] fp32 out (natural log)
+ *   ws_dev / ws_bytes                      workspace (>= workspace_size(shape, 0))
+ * Errors: VA_ERR_INVALID_ARG, VA_ERR_UNSUPPORTED, VA_ERR_WORKSPACE, VA_ERR_CUDA;
+ * device-detected VA_ERR_BAD_SEQLENS / VA_ERR_TIMEOUT in the status word. */
+va_status varlen_attn_fwd(const void* q_dev, const void* k_dev, const void* v_dev,
+                          const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
+                          int32_t causal, void* out_dev, float* lse_dev, void* ws_dev,
+                          size_t ws_bytes, va_stream_t stream);
+
+/* Backward.  The analytic gradient of the forward definition, with P
+ * recomputed from lse ("Packing与 FlashAttention Varlen", section 5 names the
+ * training branch; the gradient itself is the plain derivative):
+ *     D_i = dO_i . O_i,  dV_j = sum_i P_ij dO_i,  dP_ij = dO_i . v_j,
+ *     dS_ij = P_ij (dP_ij - D_i),  dQ_i = scale sum_j dS_ij k_j,
+ *     dK_j = scale sum_i dS_ij q_i;  dK, dV sum over a kv head's q heads.
+ *   out_dev, lse_dev   the forward's results; dout_dev [T,Hq,d] bf16
+ *   dq_dev [T,Hq,d], dk_dev/dv_dev [T,Hkv,d] bf16 out (overwritten)
+ *   ws_dev / ws_bytes  workspace (>= workspace_size(shape, 1))
+ * Errors as the forward. */
+va_status varlen_attn_bwd(const void* q_dev, const void* k_dev, const void* v_dev,
+                          const void* out_dev, const float* lse_dev, const void* dout_dev,
+                          const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
+                          int32_t causal, void* dq_dev, void* dk_dev, void* dv_dev, void* ws_dev,
+                          size_t ws_bytes, va_stream_t stream);
+
+/* Copies the workspace status word to *status_host after synchronising the
+ * stream.  VA_ERR_CUDA if the copy fails. */
+va_status varlen_read_status(const void* ws_dev, int32_t* status_host, va_stream_t stream);
+
+/* Clears the workspace status word (asynchronous). */
+va_status varlen_clear_status(void* ws_dev, va_stream_t stream);
+
+/* ---------------------------------------------------------------- tracing
+ * Per-launch timing.  With capacity > 0, the library records a CUDA event pair
+ * on the launching stream around each of the next `capacity` kernel launches
+ * it makes (any entry point); capacity 0 switches this off and frees the
+ * events.  Host-global state: not for concurrent use from several threads.
+ * Errors: VA_ERR_INVALID_ARG, VA_ERR_CUDA. */
+va_status varlen_profile_enable(int32_t capacity);
+
+/* Waits for the recorded launches, writes up to `capacity` (kernel id, ms)
+ * pairs in launch order, sets *count and restarts recording from slot 0. */
+va_status varlen_profile_read(int32_t* kernel_ids, float* ms, int32_t capacity, int32_t* count);
+
+/* Name of a kernel id reported by varlen_profile_read ("" if unknown). */
+const char* varlen_kernel_name(int32_t kernel_id);
+
+/* Kernel launches this library has made in this process (all threads). */
+int64_t varlen_launch_count(void);
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char* varlen_last_error(void);
+
+/* Library version string. */
+const char* varlen_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VARLEN_ATTN_H */

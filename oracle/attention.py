@@ -245,3 +245,44 @@ def dense_permission_attention(q, k, v, segments, positions, valid, scale):
     p = torch.exp(s - safe[..., None]).masked_fill(~allowed[None], 0.0)
     o = torch.einsum("hij,jhc->ihc", p, V)
     return o, lse, allowed
+
+
+def key_rows_backward(q, k, v, do, cu_seqlens, tokens, kv_head, scale=None, causal=True):
+    """dK, dV for single (key token, kv head) pairs, from the queries that read them.
+
+    dK_j and dV_j need P_ij for every query i that sees key j (i >= j in the
+    segment when causal), and P_ij needs that query's full-row LSE_i and D_i.
+    Cost is (queries after j) x (segment length) per key, so this is meant for
+    keys near the end of long segments.  Returns (dk [n,d], dv [n,d]).
+    """
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    cu = check_cu_seqlens(cu_seqlens, T)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    seg = np.searchsorted(cu, np.asarray(tokens), side="right") - 1
+    dk = np.zeros((len(tokens), d))
+    dv = np.zeros((len(tokens), v.shape[2]))
+    cache = {}
+    for r, (j, b) in enumerate(zip(tokens, seg)):
+        s0, e0 = cu[b], cu[b + 1]
+        first_q = j if causal else s0
+        for h in range(kv_head * g, (kv_head + 1) * g):
+            for i in range(first_q, e0):
+                key = (i, h)
+                if key not in cache:
+                    kend = i + 1 if causal else e0
+                    K = k[s0:kend, kv_head]
+                    V = v[s0:kend, kv_head]
+                    sc = scale * (K @ q[i, h])
+                    mx = sc.max()
+                    e = np.exp(sc - mx)
+                    z = e.sum()
+                    o_i = (e / z) @ V
+                    cache[key] = (mx + np.log(z), do[i, h] @ o_i)
+                lse_i, D_i = cache[key]
+                p = np.exp(scale * (q[i, h] @ k[j, kv_head]) - lse_i)
+                dp = do[i, h] @ v[j, kv_head]
+                dv[r] += p * do[i, h]
+                dk[r] += scale * p * (dp - D_i) * q[i, h]
+    return dk, dv

@@ -1,0 +1,246 @@
+"""GB300 (sm_103a) packed-sequence varlen causal attention.
+
+Python face of the C ABI in ``include/varlen_attn.h``: argument marshalling
+only.  PyTorch supplies device memory and the current stream; every step of
+the path (planner, metadata, tile scheduler, forward, backward) runs in the
+library.  There is no CPU fallback: a missing library raises.
+
+Layout: q [T, Hq, d], k/v [T, Hkv, d] bf16 with the last dim contiguous;
+``cu_seqlens`` int32 [B+1] on the device; lse fp32 [Hq, T].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import VarlenError, VaShape, check
+
+__all__ = [
+    "pack_next_fit", "pack_best_fit_decreasing", "build_metadata", "validate_cu_seqlens",
+    "tile_sizes", "workspace_size", "plan", "varlen_attn_fwd", "varlen_attn_bwd", "varlen_attn",
+    "read_status", "VarlenError", "make_shape", "library_path",
+]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _stream(dev: torch.device | None = None):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+# ----------------------------------------------------------------- host planner
+
+def _pack(fn, lengths, capacity: int):
+    lib = _lib.load()
+    n = len(lengths)
+    arr = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in lengths])
+    order = (ctypes.c_int32 * max(n, 1))()
+    offs = (ctypes.c_int32 * (n + 1))()
+    npk = ctypes.c_int32(0)
+    check(getattr(lib, fn)(arr, n, int(capacity), order, offs, ctypes.byref(npk)))
+    return [[order[j] for j in range(offs[p], offs[p + 1])] for p in range(npk.value)]
+
+
+def pack_next_fit(lengths, capacity: int):
+    """Order-preserving next-fit; packs as lists of document indices."""
+    return _pack("varlen_pack_next_fit", lengths, capacity)
+
+
+def pack_best_fit_decreasing(lengths, capacity: int):
+    """Best-fit-decreasing; packs as lists of document indices."""
+    return _pack("varlen_pack_best_fit_decreasing", lengths, capacity)
+
+
+# ----------------------------------------------------------------- metadata
+
+def build_metadata(lengths: torch.Tensor, pad_to: int = 0, T_capacity: int | None = None):
+    """Device lengths (int32) -> (cu_seqlens[n+2], position_ids[T], segment_ids[T], max_seqlen[1],
+    status[1]), all int32 device tensors.  ``cu_seqlens[n+1] == cu_seqlens[n]`` means no pad."""
+    assert lengths.is_cuda and lengths.dtype == torch.int32 and lengths.is_contiguous()
+    n = lengths.numel()
+    if T_capacity is None:
+        T_capacity = max(int(pad_to), 0)
+    dev = lengths.device
+    cu = torch.empty(n + 2, dtype=torch.int32, device=dev)
+    pos = torch.empty(max(T_capacity, 1), dtype=torch.int32, device=dev)
+    seg = torch.empty(max(T_capacity, 1), dtype=torch.int32, device=dev)
+    mx = torch.empty(1, dtype=torch.int32, device=dev)
+    st = torch.empty(1, dtype=torch.int32, device=dev)
+    check(_lib.load().varlen_build_metadata(_ptr(lengths), n, int(pad_to), int(T_capacity),
+                                            _ptr(cu), _ptr(pos), _ptr(seg), _ptr(mx), _ptr(st),
+                                            _stream(dev)))
+    return cu, pos[:T_capacity], seg[:T_capacity], mx, st
+
+
+def validate_cu_seqlens(cu_seqlens: torch.Tensor, T: int, max_seqlen: int,
+                        status: torch.Tensor):
+    """Enqueue the contract check; a violation sets ``status`` to VA_ERR_BAD_SEQLENS."""
+    check(_lib.load().varlen_validate_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(T),
+                                                 int(max_seqlen), _ptr(status),
+                                                 _stream(cu_seqlens.device)))
+
+
+# ----------------------------------------------------------------- shapes, plans
+
+def make_shape(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, B: int, max_seqlen: int,
+               out: torch.Tensor | None = None) -> VaShape:
+    T, Hq, d = q.shape
+    s = VaShape()
+    s.T, s.B, s.Hq, s.Hkv, s.d, s.max_seqlen = T, B, Hq, k.shape[1], d, int(max_seqlen)
+    s.q_row_stride, s.q_head_stride = q.stride(0), q.stride(1)
+    s.k_row_stride, s.k_head_stride = k.stride(0), k.stride(1)
+    s.v_row_stride, s.v_head_stride = v.stride(0), v.stride(1)
+    o = out if out is not None else q
+    s.o_row_stride, s.o_head_stride = o.stride(0), o.stride(1)
+    return s
+
+
+def _contig_shape(T, B, Hq, Hkv, d, max_seqlen) -> VaShape:
+    s = VaShape()
+    _lib.load().varlen_shape_contiguous(ctypes.byref(s), T, B, Hq, Hkv, d, int(max_seqlen))
+    return s
+
+
+def tile_sizes(kind: int, d: int):
+    """(BM, BN) of a tile map kind: 0 forward, 1 backward kv blocks, 2 backward dQ blocks."""
+    bm, bn = ctypes.c_int32(), ctypes.c_int32()
+    check(_lib.load().varlen_attn_tile_sizes(kind, d, ctypes.byref(bm), ctypes.byref(bn)))
+    return bm.value, bn.value
+
+
+def workspace_size(T, B, Hq, Hkv, d, max_seqlen, for_bwd: bool) -> int:
+    s = _contig_shape(T, B, Hq, Hkv, d, max_seqlen)
+    lib = _lib.load()
+    n = lib.varlen_attn_workspace_size(ctypes.byref(s), int(for_bwd))
+    if n == 0:  # the shape check failed: the plan entry point reports why
+        check(lib.varlen_attn_plan(ctypes.byref(s), None, 0, 1, None, 0, None, None))
+    return n
+
+
+def plan(cu_seqlens: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, max_seqlen: int,
+         kind: int = 0, causal: bool = True):
+    """Tile map on the device: (records int32 [n, 4], n)."""
+    B = cu_seqlens.numel() - 1
+    s = _contig_shape(T, B, Hq, Hkv, d, max_seqlen)
+    BM, BN = tile_sizes(kind, d)
+    blk = BN if kind == 1 else BM
+    heads = Hkv if kind == 1 else Hq
+    cap = (T // blk + B) * heads
+    tm = torch.empty((max(cap, 1), 4), dtype=torch.int32, device=cu_seqlens.device)
+    n = torch.zeros(1, dtype=torch.int32, device=cu_seqlens.device)
+    check(_lib.load().varlen_attn_plan(ctypes.byref(s), _ptr(cu_seqlens), kind, int(causal),
+                                       _ptr(tm), cap, _ptr(n), _stream(cu_seqlens.device)))
+    k = int(n.item())
+    return tm[:k], k
+
+
+def read_status(ws: torch.Tensor) -> int:
+    st = ctypes.c_int32(-1)
+    check(_lib.load().varlen_read_status(_ptr(ws), ctypes.byref(st), _stream(ws.device)))
+    return st.value
+
+
+def _raise_status(ws: torch.Tensor):
+    st = read_status(ws)
+    if st != 0:
+        raise VarlenError(st, "device-detected error (status word)")
+
+
+def _check_inputs(*ts):
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("q/k/v/out tensors must be CUDA bf16 [T, H, d] with a contiguous last dim")
+
+
+# ----------------------------------------------------------------- attention
+
+def varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,
+                    causal: bool = True, out=None, lse=None, workspace=None, check_status=False):
+    """Forward: returns (out [T,Hq,d] bf16, lse [Hq,T] fp32)."""
+    _check_inputs(q, k, v)
+    T, Hq, d = q.shape
+    B = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    s = make_shape(q, k, v, B, max_seqlen, out)
+    lib = _lib.load()
+    need = lib.varlen_attn_workspace_size(ctypes.byref(s), 0)
+    if need == 0:
+        check(lib.varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(s),
+                                  scale, int(causal), _ptr(out), _ptr(lse), _ptr(None), 0,
+                                  _stream(q.device)))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    check(lib.varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(s), scale,
+                              int(causal), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                              _stream(q.device)))
+    if check_status:
+        _raise_status(workspace)
+    return out, lse
+
+
+def varlen_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int,
+                    scale: float | None = None, causal: bool = True, dq=None, dk=None, dv=None,
+                    workspace=None, check_status=False):
+    """Backward: returns (dq, dk, dv) bf16 with the shapes of q, k, v."""
+    _check_inputs(q, k, v, out, dout)
+    if out.stride() != dout.stride():
+        raise ValueError("out and dout must share strides")
+    T, Hq, d = q.shape
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if dq is None:
+        dq = torch.empty_strided(out.shape, out.stride(), dtype=q.dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    if dv is None:
+        dv = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    if dq.stride() != out.stride() or dk.stride() != k.stride() or dv.stride() != k.stride():
+        raise ValueError("dq must share out's strides and dk/dv k's strides")
+    s = make_shape(q, k, v, B, max_seqlen, out)
+    lib = _lib.load()
+    need = lib.varlen_attn_workspace_size(ctypes.byref(s), 1)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    check(lib.varlen_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                              _ptr(cu_seqlens), ctypes.byref(s), scale, int(causal), _ptr(dq),
+                              _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                              _stream(q.device)))
+    if check_status:
+        _raise_status(workspace)
+    return dq, dk, dv
+
+
+class _VarlenAttn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens, max_seqlen, scale, causal):
+        out, lse = varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen, scale, causal)
+        ctx.save_for_backward(q, k, v, out, lse, cu_seqlens)
+        ctx.max_seqlen, ctx.scale, ctx.causal = max_seqlen, scale, causal
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse, cu = ctx.saved_tensors
+        dout = dout.contiguous() if dout.stride() != out.stride() else dout
+        dq, dk, dv = varlen_attn_bwd(q, k, v, out, lse, dout, cu, ctx.max_seqlen, ctx.scale,
+                                     ctx.causal)
+        return dq, dk, dv, None, None, None, None
+
+
+def varlen_attn(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,
+                causal: bool = True):
+    """Differentiable packed attention: out [T, Hq, d]."""
+    return _VarlenAttn.apply(q, k, v, cu_seqlens, max_seqlen, scale, causal)

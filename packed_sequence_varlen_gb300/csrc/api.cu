@@ -1,0 +1,440 @@
+// Host side of the C ABI: argument checks, workspace layout, launch sequences.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "attn_params.cuh"
+
+namespace va {
+
+// kernels (other translation units)
+cudaError_t launch_metadata_scan(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*,
+                                 cudaStream_t);
+cudaError_t launch_metadata_fill(const int32_t*, int, int, int32_t*, int32_t*, const int32_t*,
+                                 cudaStream_t);
+cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaStream_t);
+cudaError_t launch_plan(const int32_t*, int, int, int, int, int, int, int, TileItem*, int, int32_t*,
+                        int32_t*, cudaStream_t);
+int plan_max_keys();
+cudaError_t launch_fwd_mma(const FwdParams&, int, int, cudaStream_t);
+void fwd_mma_tiles(int*, int*);
+cudaError_t launch_bwd_rowsum(const BwdParams&, int, cudaStream_t);
+cudaError_t launch_bwd_dkdv(const BwdParams&, int, int, cudaStream_t);
+cudaError_t launch_bwd_dq(const BwdParams&, int, int, cudaStream_t);
+void bwd_mma_tiles(int*, int*, int*, int*);
+
+static thread_local std::string g_error;
+
+void set_error(const char* msg) { g_error = msg; }
+
+// ------------------------------------------------------------ launch accounting
+enum KernelId {
+  K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_ROWSUM, K_BWD_DKDV, K_BWD_DQ,
+  K_COUNT
+};
+const char* const kKernelNames[K_COUNT] = {
+    "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan",
+    "fwd",                 "bwd_rowsum",    "bwd_dkdv",      "bwd_dq"};
+
+struct Profiler {
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int32_t> ids;
+  int cap = 0, n = 0;
+};
+static Profiler g_prof;
+static std::atomic<long long> g_launches{0};
+
+// Runs one kernel launch; counts it and, when profiling, brackets it with events.
+template <class F>
+cudaError_t launch(int id, cudaStream_t st, F&& f) {
+  const bool rec = g_prof.cap > 0 && g_prof.n < g_prof.cap;
+  if (rec) cudaEventRecord(g_prof.start[g_prof.n], st);
+  cudaError_t e = f();
+  if (rec) {
+    cudaEventRecord(g_prof.stop[g_prof.n], st);
+    g_prof.ids[g_prof.n++] = id;
+  }
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
+namespace {
+
+va_status fail(va_status st, const std::string& msg) {
+  g_error = msg;
+  return st;
+}
+
+va_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(VA_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+void tiles(int kind, int* BM, int* BN) {
+  if (kind == 0) {
+    fwd_mma_tiles(BM, BN);
+  } else {
+    int a, b, c, d;
+    bwd_mma_tiles(&a, &b, &c, &d);
+    if (kind == 1) {
+      *BM = a;
+      *BN = b;
+    } else {
+      *BM = c;
+      *BN = d;
+    }
+  }
+}
+
+// Upper bound on records of a map: blocks per segment <= l/blk + 1.
+int64_t map_capacity(const va_shape& s, int kind) {
+  int BM, BN;
+  tiles(kind, &BM, &BN);
+  const int blk = kind == 1 ? BN : BM;
+  const int heads = kind == 1 ? s.Hkv : s.Hq;
+  return (static_cast<int64_t>(s.T) / blk + s.B) * heads;
+}
+
+int map_kmax(const va_shape& s, int kind) {
+  int BM, BN;
+  tiles(kind, &BM, &BN);
+  return kind == 1 ? (s.max_seqlen + BM - 1) / BM : (s.max_seqlen + BN - 1) / BN;
+}
+
+va_status check_shape(const va_shape* s) {
+  if (!s) return fail(VA_ERR_INVALID_ARG, "shape is null");
+  if (s->T < 0 || s->B < 1 || s->Hq < 1 || s->Hkv < 1 || s->max_seqlen < 1)
+    return fail(VA_ERR_INVALID_ARG, "shape: T >= 0, B >= 1, heads >= 1, max_seqlen >= 1");
+  if (s->d != 64 && s->d != 128) return fail(VA_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  if (s->Hq % s->Hkv) return fail(VA_ERR_UNSUPPORTED, "Hq must be a multiple of Hkv");
+  if (s->max_seqlen > std::max(s->T, 1)) return fail(VA_ERR_INVALID_ARG, "max_seqlen > T");
+  const int64_t st[8] = {s->q_row_stride, s->q_head_stride, s->k_row_stride, s->k_head_stride,
+                         s->v_row_stride, s->v_head_stride, s->o_row_stride, s->o_head_stride};
+  for (int64_t x : st)
+    if (x <= 0 || x % 8) return fail(VA_ERR_INVALID_ARG, "strides must be positive multiples of 8");
+  for (int64_t x : st)
+    if (x < s->d) return fail(VA_ERR_INVALID_ARG, "row and head strides must be >= d");
+  for (int kind = 0; kind < 3; ++kind)
+    if (map_kmax(*s, kind) > plan_max_keys())
+      return fail(VA_ERR_UNSUPPORTED, "max_seqlen too large for the tile scheduler");
+  return VA_OK;
+}
+
+struct FwdLayout {
+  size_t map, total;
+  int64_t cap;
+};
+FwdLayout fwd_layout(const va_shape& s) {
+  FwdLayout L;
+  L.cap = map_capacity(s, 0);
+  L.map = sizeof(WsHeader);
+  L.total = align256(L.map + static_cast<size_t>(L.cap) * sizeof(TileItem));
+  return L;
+}
+
+struct BwdLayout {
+  size_t dsum, kvmap, qmap, total;
+  int64_t cap_kv, cap_q;
+};
+BwdLayout bwd_layout(const va_shape& s) {
+  BwdLayout L;
+  L.cap_kv = map_capacity(s, 1);
+  L.cap_q = map_capacity(s, 2);
+  L.dsum = sizeof(WsHeader);
+  L.kvmap = align256(L.dsum + static_cast<size_t>(s.Hq) * s.T * sizeof(float));
+  L.qmap = align256(L.kvmap + static_cast<size_t>(L.cap_kv) * sizeof(TileItem));
+  L.total = align256(L.qmap + static_cast<size_t>(L.cap_q) * sizeof(TileItem));
+  return L;
+}
+
+}  // namespace
+}  // namespace va
+
+using namespace va;
+
+extern "C" {
+
+const char* varlen_last_error(void) { return g_error.c_str(); }
+
+const char* varlen_version(void) { return "varlen_attn 0.1 (sm_103a)"; }
+
+void varlen_shape_contiguous(va_shape* s, int32_t T, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                             int32_t max_seqlen) {
+  if (!s) return;
+  s->T = T;
+  s->B = B;
+  s->Hq = Hq;
+  s->Hkv = Hkv;
+  s->d = d;
+  s->max_seqlen = max_seqlen;
+  s->q_row_stride = static_cast<int64_t>(Hq) * d;
+  s->q_head_stride = d;
+  s->k_row_stride = static_cast<int64_t>(Hkv) * d;
+  s->k_head_stride = d;
+  s->v_row_stride = static_cast<int64_t>(Hkv) * d;
+  s->v_head_stride = d;
+  s->o_row_stride = static_cast<int64_t>(Hq) * d;
+  s->o_head_stride = d;
+}
+
+va_status varlen_build_metadata(const int32_t* lengths_dev, int32_t n, int32_t pad_to,
+                                int32_t T_capacity, int32_t* cu_dev, int32_t* pos_dev,
+                                int32_t* seg_dev, int32_t* max_dev, int32_t* status_dev,
+                                va_stream_t stream) {
+  if (n < 0 || pad_to < 0 || T_capacity < 0 || !cu_dev || !max_dev || !status_dev ||
+      (n > 0 && !lengths_dev) || (T_capacity > 0 && (!pos_dev || !seg_dev)))
+    return fail(VA_ERR_INVALID_ARG, "build_metadata: null pointer or negative size");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(K_META_SCAN, cs, [&] {
+    return launch_metadata_scan(lengths_dev, n, pad_to, T_capacity, cu_dev, max_dev, status_dev, cs);
+  });
+  if (e == cudaSuccess && T_capacity > 0)
+    e = launch(K_META_FILL, cs, [&] {
+      return launch_metadata_fill(cu_dev, n, T_capacity, pos_dev, seg_dev, status_dev, cs);
+    });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "build_metadata");
+}
+
+va_status varlen_validate_cu_seqlens(const int32_t* cu_dev, int32_t B, int32_t T, int32_t max_seqlen,
+                                     int32_t* status_dev, va_stream_t stream) {
+  if (!cu_dev || !status_dev || B < 1 || T < 0 || max_seqlen < 1)
+    return fail(VA_ERR_INVALID_ARG, "validate: null pointer or bad size");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(K_VALIDATE, cs, [&] {
+    return launch_validate(cu_dev, B, T, max_seqlen, status_dev, 0, cs);
+  });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "validate");
+}
+
+va_status varlen_attn_tile_sizes(int32_t kind, int32_t d, int32_t* BM, int32_t* BN) {
+  if (kind < 0 || kind > 2 || !BM || !BN) return fail(VA_ERR_INVALID_ARG, "tile_sizes: bad kind");
+  if (d != 64 && d != 128) return fail(VA_ERR_UNSUPPORTED, "tile_sizes: d must be 64 or 128");
+  int a, b;
+  tiles(kind, &a, &b);
+  *BM = a;
+  *BN = b;
+  return VA_OK;
+}
+
+size_t varlen_attn_workspace_size(const va_shape* s, int32_t for_bwd) {
+  if (check_shape(s) != VA_OK) return 0;
+  return for_bwd ? bwd_layout(*s).total : fwd_layout(*s).total;
+}
+
+va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kind, int32_t causal,
+                           int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
+                           va_stream_t stream) {
+  va_status st = check_shape(s);
+  if (st != VA_OK) return st;
+  if (kind < 0 || kind > 2 || !cu_dev || !map_dev || !n_items_dev || capacity < 0)
+    return fail(VA_ERR_INVALID_ARG, "plan: bad kind or null pointer");
+  if (!aligned16(map_dev)) return fail(VA_ERR_INVALID_ARG, "plan: tile map must be 16-byte aligned");
+  if (map_capacity(*s, kind) > capacity)
+    return fail(VA_ERR_WORKSPACE, "plan: capacity below the record bound (ceil(T/blk)+B)*heads");
+  int BM, BN;
+  tiles(kind, &BM, &BN);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(K_PLAN, cs, [&] {
+    return launch_plan(cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
+                       map_kmax(*s, kind), reinterpret_cast<TileItem*>(map_dev), capacity, nullptr,
+                       n_items_dev, cs);
+  });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "plan");
+}
+
+va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
+                          const va_shape* s, float scale, int32_t causal, void* out, float* lse,
+                          void* ws, size_t ws_bytes, va_stream_t stream) {
+  va_status st = check_shape(s);
+  if (st != VA_OK) return st;
+  if (!q || !k || !v || !cu || !out || !lse || !ws)
+    return fail(VA_ERR_INVALID_ARG, "fwd: null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws))
+    return fail(VA_ERR_INVALID_ARG, "fwd: pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !(scale < INFINITY)) return fail(VA_ERR_INVALID_ARG, "fwd: scale must be finite and > 0");
+  const FwdLayout L = fwd_layout(*s);
+  if (ws_bytes < L.total) return fail(VA_ERR_WORKSPACE, "fwd: workspace too small");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  TileItem* map = reinterpret_cast<TileItem*>(w + L.map);
+  cudaError_t e = launch(K_VALIDATE, cs, [&] {
+    return launch_validate(cu, s->B, s->T, s->max_seqlen, &hdr->status, 1, cs);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "fwd validate");
+  if (s->T == 0) return VA_OK;
+  int BM, BN;
+  tiles(0, &BM, &BN);
+  e = launch(K_PLAN, cs, [&] {
+    return launch_plan(cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map_kmax(*s, 0), map,
+                       static_cast<int>(L.cap), &hdr->status, &hdr->n_items[0], cs);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "fwd plan");
+  FwdParams p{};
+  p.q = static_cast<const bf16*>(q);
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.o = static_cast<bf16*>(out);
+  p.lse = lse;
+  p.cu = cu;
+  p.items = map;
+  p.hdr = hdr;
+  p.slot = 0;
+  p.T = s->T;
+  p.Hq = s->Hq;
+  p.Hkv = s->Hkv;
+  p.g = s->Hq / s->Hkv;
+  p.q_rs = s->q_row_stride;
+  p.q_hs = s->q_head_stride;
+  p.k_rs = s->k_row_stride;
+  p.k_hs = s->k_head_stride;
+  p.v_rs = s->v_row_stride;
+  p.v_hs = s->v_head_stride;
+  p.o_rs = s->o_row_stride;
+  p.o_hs = s->o_head_stride;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  e = launch(K_FWD, cs, [&] { return launch_fwd_mma(p, s->d, static_cast<int>(L.cap), cs); });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "fwd kernel");
+}
+
+va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* dout, const int32_t* cu, const va_shape* s,
+                          float scale, int32_t causal, void* dq, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, va_stream_t stream) {
+  va_status st = check_shape(s);
+  if (st != VA_OK) return st;
+  if (!q || !k || !v || !out || !lse || !dout || !cu || !dq || !dk || !dv || !ws)
+    return fail(VA_ERR_INVALID_ARG, "bwd: null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(ws))
+    return fail(VA_ERR_INVALID_ARG, "bwd: pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !(scale < INFINITY)) return fail(VA_ERR_INVALID_ARG, "bwd: scale must be finite and > 0");
+  const BwdLayout L = bwd_layout(*s);
+  if (ws_bytes < L.total) return fail(VA_ERR_WORKSPACE, "bwd: workspace too small");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  TileItem* kvmap = reinterpret_cast<TileItem*>(w + L.kvmap);
+  TileItem* qmap = reinterpret_cast<TileItem*>(w + L.qmap);
+  cudaError_t e = launch(K_VALIDATE, cs, [&] {
+    return launch_validate(cu, s->B, s->T, s->max_seqlen, &hdr->status, 1, cs);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd validate");
+  if (s->T == 0) return VA_OK;
+  int BM, BN;
+  tiles(1, &BM, &BN);
+  e = launch(K_PLAN, cs, [&] {
+    return launch_plan(cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, map_kmax(*s, 1), kvmap,
+                       static_cast<int>(L.cap_kv), &hdr->status, &hdr->n_items[1], cs);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd plan kv");
+  tiles(2, &BM, &BN);
+  e = launch(K_PLAN, cs, [&] {
+    return launch_plan(cu, s->B, s->Hq, BM, BN, 2, causal ? 1 : 0, map_kmax(*s, 2), qmap,
+                       static_cast<int>(L.cap_q), &hdr->status, &hdr->n_items[2], cs);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd plan q");
+  BwdParams p{};
+  p.q = static_cast<const bf16*>(q);
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.o = static_cast<const bf16*>(out);
+  p.dout = static_cast<const bf16*>(dout);
+  p.lse = lse;
+  p.dsum = reinterpret_cast<float*>(w + L.dsum);
+  p.dq = static_cast<bf16*>(dq);
+  p.dk = static_cast<bf16*>(dk);
+  p.dv = static_cast<bf16*>(dv);
+  p.cu = cu;
+  p.kv_items = kvmap;
+  p.q_items = qmap;
+  p.hdr = hdr;
+  p.kv_slot = 1;
+  p.q_slot = 2;
+  p.T = s->T;
+  p.Hq = s->Hq;
+  p.Hkv = s->Hkv;
+  p.g = s->Hq / s->Hkv;
+  p.q_rs = s->q_row_stride;
+  p.q_hs = s->q_head_stride;
+  p.k_rs = s->k_row_stride;
+  p.k_hs = s->k_head_stride;
+  p.v_rs = s->v_row_stride;
+  p.v_hs = s->v_head_stride;
+  p.o_rs = s->o_row_stride;
+  p.o_hs = s->o_head_stride;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  e = launch(K_BWD_ROWSUM, cs, [&] { return launch_bwd_rowsum(p, s->d, cs); });
+  if (e == cudaSuccess)
+    e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv(p, s->d, static_cast<int>(L.cap_kv), cs); });
+  if (e == cudaSuccess)
+    e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq(p, s->d, static_cast<int>(L.cap_q), cs); });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd kernels");
+}
+
+va_status varlen_read_status(const void* ws, int32_t* out, va_stream_t stream) {
+  if (!ws || !out) return fail(VA_ERR_INVALID_ARG, "read_status: null pointer");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "read_status");
+}
+
+va_status varlen_clear_status(void* ws, va_stream_t stream) {
+  if (!ws) return fail(VA_ERR_INVALID_ARG, "clear_status: null pointer");
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "clear_status");
+}
+
+va_status varlen_profile_enable(int32_t capacity) {
+  for (cudaEvent_t e : g_prof.start) cudaEventDestroy(e);
+  for (cudaEvent_t e : g_prof.stop) cudaEventDestroy(e);
+  g_prof = Profiler{};
+  if (capacity < 0) return fail(VA_ERR_INVALID_ARG, "profile_enable: negative capacity");
+  if (capacity == 0) return VA_OK;
+  g_prof.start.resize(capacity);
+  g_prof.stop.resize(capacity);
+  g_prof.ids.resize(capacity);
+  for (int i = 0; i < capacity; ++i) {
+    cudaError_t e = cudaEventCreate(&g_prof.start[i]);
+    if (e == cudaSuccess) e = cudaEventCreate(&g_prof.stop[i]);
+    if (e != cudaSuccess) {
+      g_prof.start.resize(i);
+      g_prof.stop.resize(i);
+      return cuda_fail(e, "profile_enable");
+    }
+  }
+  g_prof.cap = capacity;
+  return VA_OK;
+}
+
+va_status varlen_profile_read(int32_t* ids, float* ms, int32_t capacity, int32_t* count) {
+  if (!count || (capacity > 0 && (!ids || !ms)))
+    return fail(VA_ERR_INVALID_ARG, "profile_read: null pointer");
+  const int n = std::min(g_prof.n, capacity);
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_prof.stop[i]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[i], g_prof.start[i], g_prof.stop[i]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile_read");
+    ids[i] = g_prof.ids[i];
+  }
+  *count = n;
+  g_prof.n = 0;
+  return VA_OK;
+}
+
+const char* varlen_kernel_name(int32_t id) {
+  return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : "";
+}
+
+int64_t varlen_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

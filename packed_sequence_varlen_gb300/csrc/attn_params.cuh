@@ -1,0 +1,48 @@
+// Kernel parameter blocks for the attention kernels.
+#pragma once
+#include "common.cuh"
+
+namespace va {
+
+using bf16 = __nv_bfloat16;
+
+struct FwdParams {
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  bf16* o;
+  float* lse;  // [Hq, T]
+  const int32_t* cu;
+  const TileItem* items;
+  WsHeader* hdr;
+  int slot;
+  int T, Hq, Hkv, g;
+  int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs, o_rs, o_hs;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+};
+
+struct BwdParams {
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  const bf16* o;
+  const bf16* dout;
+  const float* lse;  // [Hq, T], natural log
+  float* dsum;       // D = rowsum(dO * O), [Hq, T]
+  bf16* dq;
+  bf16* dk;
+  bf16* dv;
+  const int32_t* cu;
+  const TileItem* kv_items;  // kv-block map
+  const TileItem* q_items;   // q-block map (dQ pass)
+  WsHeader* hdr;
+  int kv_slot, q_slot;
+  int T, Hq, Hkv, g;
+  int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs, o_rs, o_hs;
+  float scale;
+  float scale_log2;
+  int causal;
+};
+
+}  // namespace va

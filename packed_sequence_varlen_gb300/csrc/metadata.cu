@@ -1,0 +1,136 @@
+// Boundary metadata on the device: lengths -> cu_seqlens, position_ids,
+// segment_ids, max_seqlen; and the cu_seqlens contract check.
+//
+// "Packing与 FlashAttention Varlen", section 3: the cumulative boundary array
+// is int32, starts at 0, ends at the total token count and strictly increases;
+// max_seqlen = max diff and only bounds launches and tiles.  Section 2
+// (packing_row): each sample's positions restart at 0.
+#include "common.cuh"
+
+namespace va {
+
+constexpr int kScanThreads = 1024;
+
+// Block-wide inclusive scan of one int per thread (1024 threads).
+__device__ __forceinline__ int block_inclusive_scan(int x, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  if (warp > 0) x += warp_sums[warp - 1];
+  __syncthreads();
+  return x;
+}
+
+// One block: exclusive scan of the lengths into cu[0..n], tail pad into cu[n+1].
+__global__ void __launch_bounds__(kScanThreads)
+    metadata_scan_kernel(const int32_t* __restrict__ lengths, int n, int pad_to,
+                         int T_capacity, int32_t* __restrict__ cu, int32_t* __restrict__ max_out,
+                         int32_t* __restrict__ status) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry, mx, bad;
+  if (threadIdx.x == 0) {
+    carry = 0;
+    mx = 0;
+    bad = 0;
+    cu[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < n; base += kScanThreads) {
+    const int i = base + threadIdx.x;
+    const int L = i < n ? lengths[i] : 0;
+    if (i < n && L <= 0) atomicOr(&bad, 1);
+    if (i < n) atomicMax(&mx, L);
+    const int incl = block_inclusive_scan(L, warp_sums);
+    if (i < n) cu[i + 1] = carry + incl;
+    __syncthreads();
+    if (threadIdx.x == kScanThreads - 1) carry += incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int total = carry;
+    int last = total;
+    if (pad_to > total) {
+      last = pad_to;
+      mx = max(mx, pad_to - total);
+    } else if (pad_to > 0 && pad_to < total) {
+      bad = 1;
+    }
+    if (last > T_capacity) bad = 1;
+    cu[n + 1] = last;
+    *max_out = mx;
+    *status = bad ? VA_ERR_BAD_SEQLENS : VA_OK;
+  }
+}
+
+// Grid over tokens: segment by binary search over cu[0..nseg], position = t - start.
+__global__ void metadata_fill_kernel(const int32_t* __restrict__ cu, int n, int T_capacity,
+                                     int32_t* __restrict__ pos, int32_t* __restrict__ seg,
+                                     const int32_t* __restrict__ status) {
+  if (*status != VA_OK) return;
+  const int T = cu[n + 1];
+  const int nseg = (cu[n + 1] > cu[n]) ? n + 1 : n;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T && t < T_capacity;
+       t += gridDim.x * blockDim.x) {
+    int lo = 0, hi = nseg;  // find b with cu[b] <= t < cu[b+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu[mid] <= t) lo = mid; else hi = mid;
+    }
+    seg[t] = lo;
+    pos[t] = t - cu[lo];
+  }
+}
+
+// One block: checks the boundary contract and writes the status word (0 or error).
+__global__ void __launch_bounds__(kScanThreads)
+    validate_cu_kernel(const int32_t* __restrict__ cu, int B, int T, int max_seqlen,
+                       int32_t* __restrict__ status, int overwrite) {
+  int bad = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int a = cu[b], c = cu[b + 1];
+    if (c <= a || c - a > max_seqlen) bad = 1;
+  }
+  if (threadIdx.x == 0 && (cu[0] != 0 || cu[B] != T)) bad = 1;
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    if (bad) *status = VA_ERR_BAD_SEQLENS;
+    else if (overwrite) *status = VA_OK;
+  }
+}
+
+cudaError_t launch_metadata_scan(const int32_t* lengths, int n, int pad_to, int T_capacity,
+                                 int32_t* cu, int32_t* max_out, int32_t* status, cudaStream_t st) {
+  metadata_scan_kernel<<<1, kScanThreads, 0, st>>>(lengths, n, pad_to, T_capacity, cu, max_out,
+                                                    status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_metadata_fill(const int32_t* cu, int n, int T_capacity, int32_t* pos,
+                                 int32_t* seg, const int32_t* status, cudaStream_t st) {
+  const int blocks = min(1216, max(1, (T_capacity + 255) / 256));
+  metadata_fill_kernel<<<blocks, 256, 0, st>>>(cu, n, T_capacity, pos, seg, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate(const int32_t* cu, int B, int T, int max_seqlen, int32_t* status,
+                            int overwrite, cudaStream_t st) {
+  validate_cu_kernel<<<1, kScanThreads, 0, st>>>(cu, B, T, max_seqlen, status, overwrite);
+  return cudaGetLastError();
+}
+
+}  // namespace va

@@ -314,3 +314,16 @@ def test_rejects_bad_boundaries():
     for cu in ([0, 3, 3, 5], [1, 5], [0, 4], [0, 6], [0, 3, 2, 5]):
         with pytest.raises(ValueError):
             oa.varlen_forward(q, q, q, cu)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_key_rows_sampler_matches_full_oracle(causal):
+    """The one-key-at-a-time dK/dV checker agrees with the full oracle."""
+    cu, pos, seg, q, k, v, do = random_pack(8, T_max=40, Hq=4, Hkv=2, d=8)
+    o, lse = oa.varlen_forward(q, k, v, cu, 0.3, causal)
+    _, dk, dv = oa.varlen_backward(q, k, v, o, lse, do, cu, 0.3, causal)
+    toks = np.array([0, 3, 17, q.shape[0] - 1, 22])
+    for hk in range(2):
+        rk, rv = oa.key_rows_backward(q, k, v, do, cu, toks, hk, 0.3, causal)
+        assert close(rk, dk[toks, hk], 1e-12, 1e-10)
+        assert close(rv, dv[toks, hk], 1e-12, 1e-10)
