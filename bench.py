@@ -38,7 +38,7 @@ import seeded_inputs as si  # noqa: E402
 METRIC = "varlen causal attn fwd+bwd TFLOP/s (in-segment FLOPs), % of GB300 bf16 peak"
 UNIT = "TFLOP/s"
 WORKLOAD = "sft8k"
-PACKS_PER_STEP = 16
+PACKS_PER_STEP = 16        # --packs changes it (small cases for profiling)
 
 
 def load_peaks():
@@ -410,7 +410,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--packs", type=int, default=PACKS_PER_STEP,
+                    help="packs per step (16 is the benchmark; fewer for profiling cases)")
     args = ap.parse_args()
+    global PACKS_PER_STEP
+    PACKS_PER_STEP = args.packs
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
 
