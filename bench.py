@@ -402,6 +402,7 @@ def run_reference(args, rank, world):
 
 
 def main():
+    global PACKS_PER_STEP
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -410,10 +411,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--packs", type=int, default=PACKS_PER_STEP,
+    ap.add_argument("--packs", type=int, default=16,
                     help="packs per step (16 is the benchmark; fewer for profiling cases)")
     args = ap.parse_args()
-    global PACKS_PER_STEP
     PACKS_PER_STEP = args.packs
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -18,8 +18,8 @@ cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaSt
 cudaError_t launch_plan(const int32_t*, int, int, int, int, int, int, int, TileItem*, int, int32_t*,
                         int32_t*, cudaStream_t);
 int plan_max_keys();
-cudaError_t launch_fwd_mma(const FwdParams&, int, int, cudaStream_t);
-void fwd_mma_tiles(int*, int*);
+cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
+void fwd_tc_tiles(int*, int*);
 cudaError_t launch_bwd_rowsum(const BwdParams&, int, cudaStream_t);
 cudaError_t launch_bwd_dkdv(const BwdParams&, int, int, cudaStream_t);
 cudaError_t launch_bwd_dq(const BwdParams&, int, int, cudaStream_t);
@@ -77,7 +77,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 void tiles(int kind, int* BM, int* BN) {
   if (kind == 0) {
-    fwd_mma_tiles(BM, BN);
+    fwd_tc_tiles(BM, BN);
   } else {
     int a, b, c, d;
     bwd_mma_tiles(&a, &b, &c, &d);
@@ -299,7 +299,7 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   p.o_hs = s->o_head_stride;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
-  e = launch(K_FWD, cs, [&] { return launch_fwd_mma(p, s->d, static_cast<int>(L.cap), cs); });
+  e = launch(K_FWD, cs, [&] { return launch_fwd_tc(p, s->d, static_cast<int>(L.cap), cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "fwd kernel");
 }
 

@@ -1,0 +1,445 @@
+// Forward varlen attention for sm_103a: TMA + tcgen05 MMA (TMEM accumulators),
+// warp-specialised, persistent.
+//
+// What it computes ("Packing与 FlashAttention Varlen", sections 1 and 5): for a
+// work item (segment b, q block m of 256 rows, q head h) the Q/K/V rows are read
+// at offset cu[b] of the flat token axis with extent l = cu[b+1]-cu[b]; key
+// blocks run to ceil(min(l, (m+1)*256)/128) (causal) and the causal mask is
+// applied only on the one key block that crosses each 128-row tile's diagonal.
+// O is written at Q's offsets, rows past l are never stored, and
+// lse = ln sum_j exp(scale q.k_j).
+//
+// CTA layout (384 threads, one CTA per SM, persistent over the tile map):
+//   warp 0      TMA producer: Q tiles once per item, K/V tiles into an NST-slot ring
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T (SS), O_t += P_t V (TS, P in TMEM);
+//               also owns the TMEM allocation
+//   warps 4-7   softmax + epilogue for q tile 0 (rows 0..127 of the block; thread = row)
+//   warps 8-11  softmax + epilogue for q tile 1 (rows 128..255)
+// TMEM (512 columns): S0 | S1 | O0 | O1.  P_t (bf16) overwrites the first half of
+// S_t; the MMA pipe executes in issue order, so the next S_t cannot overwrite P_t
+// before the PV that reads it.  The two q tiles share every K/V tile, halving
+// shared-memory fill traffic per FLOP; while one tile's softmax runs, the tensor
+// core works on the other tile.  The running max is only raised when it grows by
+// more than 2^8, so O in TMEM is rescaled rarely.
+#include <cudaTypedefs.h>
+
+#include "attn_params.cuh"
+#include "sm100_ptx.cuh"
+
+namespace va {
+using namespace sm100;
+
+namespace {
+
+constexpr int kTcBM = 256;  // q rows per work item (two 128-row tiles)
+constexpr int kTcBN = 128;  // key rows per K/V tile
+constexpr int kTcThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct TcCfg {
+  static constexpr int NST = D == 128 ? 4 : 8;         // K/V ring slots
+  static constexpr int TILE = 128 * D * 2;             // bytes of one 128-row Q, K or V tile
+  static constexpr int PANEL = 128 * 128;              // one 64-column (128-byte) panel of a tile
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = 2 * TILE;
+  static constexpr int BAR_OFF = KV_OFF + NST * TILE;
+  // barriers: q_full, q_empty, kv_full[NST], kv_empty[NST], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NST, B_SF = 2 + 2 * NST,
+                       B_PF = B_SF + 2, B_OF = B_PF + 2, B_DR = B_OF + 2, NBAR = B_DR + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + slack to align the base to 1024
+  static constexpr int OCOLS = D;                      // TMEM columns of one O accumulator
+};
+
+struct Item {
+  int s0, l, h, hk, m, nb, nb0;
+  bool t1;
+};
+
+__device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
+  const TileItem it = p.items[idx];
+  Item r;
+  r.s0 = p.cu[it.seg];
+  r.l = p.cu[it.seg + 1] - r.s0;
+  r.h = it.head;
+  r.hk = it.head / p.g;
+  r.m = it.blk;
+  r.nb = it.count;
+  r.t1 = r.m * kTcBM + 128 < r.l;
+  r.nb0 = (p.causal && r.t1) ? r.nb - 1 : r.nb;
+  return r;
+}
+
+// Bounded wait used only while shutting down after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 50000000ull) return;
+  }
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::MISC_OFF + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
+
+  if (p.hdr->status != VA_OK) return;
+  const int n_items = p.hdr->n_items[p.slot];
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_QF), 1);
+    mbar_init(bar(C::B_QE), 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar(C::B_KVF + s), 1);
+      mbar_init(bar(C::B_KVE + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_SF + t), 1);
+      mbar_init(bar(C::B_PF + t), 128);
+      mbar_init(bar(C::B_OF + t), 1);
+    }
+    mbar_init(bar(C::B_DR), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int kv_it = 0, item_cnt = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+        const Item I = decode(p, idx);
+        ok = mbar_wait(bar(C::B_QE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 1);
+        if (!ok) break;
+        mbar_expect_tx(bar(C::B_QF), (I.t1 ? 2 : 1) * C::TILE);
+        for (int t = 0; t < (I.t1 ? 2 : 1); ++t)
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(base + C::Q_OFF + t * C::TILE + pn * C::PANEL, &tq, bar(C::B_QF), pn * 64,
+                        I.h, I.s0 + I.m * kTcBM + t * 128);
+        for (int n = 0; ok && n < I.nb; ++n) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int s = kv_it % C::NST;
+            ok = mbar_wait(bar(C::B_KVE + s), ((kv_it / C::NST) & 1) ^ 1, abort_flag, p.hdr, 2);
+            if (!ok) break;
+            mbar_expect_tx(bar(C::B_KVF + s), C::TILE);
+            for (int pn = 0; pn < D / 64; ++pn)
+              tma_load_3d(base + C::KV_OFF + s * C::TILE + pn * C::PANEL, kv ? &tv : &tk,
+                          bar(C::B_KVF + s), pn * 64, I.hk, I.s0 + n * kTcBN);
+            ++kv_it;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy this thread started land before the CTA exits
+        drain_wait(bar(C::B_QF), (item_cnt & 1));
+        for (int i = kv_it - 1; i >= 0 && i >= kv_it - C::NST; --i)
+          drain_wait(bar(C::B_KVF + i % C::NST), (i / C::NST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, kTcBN, false, false);
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      int kv_it = 0, item_cnt = 0;
+      uint32_t pf[2] = {0, 0};
+      bool ok = true;
+      auto issue_S = [&](int t, int slot) {
+        const uint32_t qa = base + C::Q_OFF + t * C::TILE;
+        const uint32_t ka = base + C::KV_OFF + slot * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 idS, kk > 0);
+        }
+        mma_commit(bar(C::B_SF + t));
+      };
+      auto issue_PV = [&](int t, int slot, bool acc) {
+        const uint32_t va_ = base + C::KV_OFF + slot * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kTcBN / 16; ++kk)
+          mma_ts(tmem + 256 + t * C::OCOLS, tmem + t * 128 + kk * 8,
+                 sdesc_sw128(va_ + kk * 2048, C::PANEL, 1024), idPV, (acc || kk > 0) ? 1u : 0u);
+        mma_commit(bar(C::B_OF + t));
+      };
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+        const Item I = decode(p, idx);
+        ok = mbar_wait(bar(C::B_QF), item_cnt & 1, abort_flag, p.hdr, 3);
+        if (!ok) break;
+        int ks = kv_it % C::NST;
+        ok = mbar_wait(bar(C::B_KVF + ks), (kv_it / C::NST) & 1, abort_flag, p.hdr, 4);
+        if (!ok) break;
+        fence_after_sync();
+        ++kv_it;
+        issue_S(0, ks);
+        if (I.t1) issue_S(1, ks);
+        mma_commit(bar(C::B_KVE + ks));
+        if (I.nb == 1) mma_commit(bar(C::B_QE));
+        for (int n = 0; ok && n < I.nb; ++n) {
+          const int vs = kv_it % C::NST;
+          ok = mbar_wait(bar(C::B_KVF + vs), (kv_it / C::NST) & 1, abort_flag, p.hdr, 5);
+          if (!ok) break;
+          ++kv_it;
+          if (n < I.nb0) {
+            ok = mbar_wait(bar(C::B_PF + 0), pf[0] & 1, abort_flag, p.hdr, 6);
+            if (!ok) break;
+            ++pf[0];
+            fence_after_sync();
+            issue_PV(0, vs, n > 0);
+          }
+          int ks2 = -1;
+          if (n + 1 < I.nb) {
+            ks2 = kv_it % C::NST;
+            ok = mbar_wait(bar(C::B_KVF + ks2), (kv_it / C::NST) & 1, abort_flag, p.hdr, 7);
+            if (!ok) break;
+            ++kv_it;
+            fence_after_sync();
+            if (n + 1 < I.nb0) issue_S(0, ks2);
+          }
+          if (I.t1) {
+            ok = mbar_wait(bar(C::B_PF + 1), pf[1] & 1, abort_flag, p.hdr, 8);
+            if (!ok) break;
+            ++pf[1];
+            fence_after_sync();
+            issue_PV(1, vs, n > 0);
+          }
+          mma_commit(bar(C::B_KVE + vs));
+          if (ks2 >= 0) {
+            if (I.t1) issue_S(1, ks2);
+            mma_commit(bar(C::B_KVE + ks2));
+            if (n + 1 == I.nb - 1) mma_commit(bar(C::B_QE));
+          }
+        }
+      }
+      // every MMA this thread issued must finish before TMEM is released
+      mma_commit(bar(C::B_DR));
+      drain_wait(bar(C::B_DR), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + t * 128;
+    const uint32_t o_addr = tmem + lane_off + 256 + t * C::OCOLS;
+    const float sl2 = p.scale_log2;
+    uint32_t sf = 0, of_base = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      const Item I = decode(p, idx);
+      if (t == 1 && !I.t1) continue;
+      const int nbt = t == 0 ? I.nb0 : I.nb;
+      const int qrow = I.m * kTcBM + t * 128 + r;
+      float m_ref = -INFINITY, lsum = 0.f;
+      for (int n = 0; n < nbt; ++n) {
+        ok = mbar_wait(bar(C::B_SF + t), sf & 1, abort_flag, p.hdr, 9);
+        if (!__all_sync(0xffffffffu, ok)) {  // TMEM loads below are warp-collective
+          ok = false;
+          break;
+        }
+        ++sf;
+        fence_after_sync();
+        // pass 1: row max over the 128 scores, 64 columns at a time
+        const bool need_mask = p.causal ? (n == nbt - 1) : (n * kTcBN + kTcBN > I.l);
+        const int col0 = n * kTcBN;
+        const int lim = p.causal ? qrow - col0 : I.l - 1 - col0;  // columns j > lim are masked
+        float mx = -INFINITY;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[64];
+          tmem_ld32(s_addr + h2 * 64, v);
+          tmem_ld32(s_addr + h2 * 64 + 32, v + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const float x = __uint_as_float(v[j]);
+            mx = (need_mask && h2 * 64 + j > lim) ? mx : fmaxf(mx, x);
+          }
+        }
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        const bool resc = m_new > m_ref + kRescaleThreshold;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = fast_exp2(m_ref - m_new);
+          lsum *= alpha;
+        }
+        if (__any_sync(0xffffffffu, resc && n > 0)) {
+          // O_t holds PV_{n-1}: wait for it, then scale this row in TMEM
+          ok = mbar_wait(bar(C::B_OF + t), (of_base + n - 1) & 1, abort_flag, p.hdr, 10);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(o_addr + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        if (resc) m_ref = m_new;
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        // pass 2: P = exp2(s * scale * log2e - m) as bf16 into the first 64 columns of S_t.
+        // Half h2 reads columns [64 h2, 64 h2 + 64) and writes P columns [32 h2, 32 h2 + 32),
+        // which only overlap score columns already read.
+        float rs = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[64];
+          tmem_ld32(s_addr + h2 * 64, v);
+          tmem_ld32(s_addr + h2 * 64 + 32, v + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * j]), sl2, -mu));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), sl2, -mu));
+            if (need_mask) {
+              if (h2 * 64 + 2 * j > lim) p0 = 0.f;
+              if (h2 * 64 + 2 * j + 1 > lim) p1 = 0.f;
+            }
+            rs += p0 + p1;
+            v[j] = pack_bf16(p0, p1);
+          }
+          tmem_st16(s_addr + h2 * 32, v);
+          tmem_st16(s_addr + h2 * 32 + 16, v + 16);
+        }
+        lsum += rs;
+        tmem_wait_st();
+        fence_before_sync();
+        mbar_arrive(bar(C::B_PF + t));
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16 rows < l; lse
+      ok = mbar_wait(bar(C::B_OF + t), (of_base + nbt - 1) & 1, abort_flag, p.hdr, 11);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      of_base += nbt;
+      fence_after_sync();
+      const float inv = 1.f / lsum;
+      const bool store = qrow < I.l;
+      bf16* orow = p.o + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + c * 32, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      if (store)
+        p.lse[static_cast<int64_t>(I.h) * p.T + I.s0 + qrow] = (m_ref + __log2f(lsum)) * kLn2;
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [T, H, d] bf16 with row/head strides (elements) -> 3-D map (d, H, T), box (64, 1, 128), 128B swizzle.
+static bool make_map(CUtensorMap* m, const void* ptr, int T, int H, int d, int64_t row_stride,
+                     int64_t head_stride) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_stride) * 2,
+                           static_cast<cuuint64_t>(row_stride) * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
+  using C = TcCfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs) ||
+      !make_map(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs) ||
+      !make_map(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = std::min(cap, std::max(sms, 1));
+  if (grid <= 0) return cudaSuccess;
+  fwd_tc_kernel<D><<<grid, kTcThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(const FwdParams& p, int d, int cap, cudaStream_t st) {
+  return d == 64 ? launch_d<64>(p, cap, st) : launch_d<128>(p, cap, st);
+}
+
+void fwd_tc_tiles(int* BM, int* BN) {
+  *BM = kTcBM;
+  *BN = kTcBN;
+}
+
+}  // namespace va
