@@ -21,9 +21,9 @@ int plan_max_keys();
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
 cudaError_t launch_bwd_rowsum(const BwdParams&, int, cudaStream_t);
-cudaError_t launch_bwd_dkdv(const BwdParams&, int, int, cudaStream_t);
-cudaError_t launch_bwd_dq(const BwdParams&, int, int, cudaStream_t);
-void bwd_mma_tiles(int*, int*, int*, int*);
+cudaError_t launch_bwd_dkdv_tc(const BwdParams&, int, int, cudaStream_t);
+cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, cudaStream_t);
+void bwd_tc_tiles(int*, int*, int*, int*);
 
 static thread_local std::string g_error;
 
@@ -80,7 +80,7 @@ void tiles(int kind, int* BM, int* BN) {
     fwd_tc_tiles(BM, BN);
   } else {
     int a, b, c, d;
-    bwd_mma_tiles(&a, &b, &c, &d);
+    bwd_tc_tiles(&a, &b, &c, &d);
     if (kind == 1) {
       *BM = a;
       *BN = b;
@@ -374,9 +374,9 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   p.causal = causal ? 1 : 0;
   e = launch(K_BWD_ROWSUM, cs, [&] { return launch_bwd_rowsum(p, s->d, cs); });
   if (e == cudaSuccess)
-    e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv(p, s->d, static_cast<int>(L.cap_kv), cs); });
+    e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv_tc(p, s->d, static_cast<int>(L.cap_kv), cs); });
   if (e == cudaSuccess)
-    e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq(p, s->d, static_cast<int>(L.cap_q), cs); });
+    e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq_tc(p, s->d, static_cast<int>(L.cap_q), cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd kernels");
 }
 

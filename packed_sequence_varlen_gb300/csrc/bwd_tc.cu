@@ -1,0 +1,711 @@
+// Backward varlen attention for sm_103a: TMA + tcgen05 MMA with TMEM accumulators.
+//
+// The gradient of the forward definition, P recomputed from the forward's lse
+// ("Packing与 FlashAttention Varlen", section 5 names the training branch):
+//   P_ij = exp(scale q_i.k_j - lse_i) on visible (i, j);  D_i = dO_i . O_i;
+//   dV_j = sum_i P_ij dO_i;  dS_ij = P_ij (dO_i . v_j - D_i);
+//   dK_j = scale sum_i dS_ij q_i;  dQ_i = scale sum_j dS_ij k_j.
+//
+// Two kernels, each owning its output rows (no atomics, deterministic):
+//   dkdv_tc_kernel  work item (segment, 128 kv rows, kv head); steps over the
+//                   segment's q blocks of 64 rows at or after the diagonal and
+//                   the kv head's q-head group.  Per step:
+//                     S^T = K Q^T, dP^T = V dO^T          (SS, M=128 kv, N=64 q)
+//                     P^T, dS^T -> bf16 in TMEM            (softmax warps)
+//                     dV += P^T dO, dK += dS^T Q           (TS, A from TMEM)
+//   dq_tc_kernel    work item (segment, 128 q rows, q head); steps over key
+//                   blocks of 64 rows up to the diagonal.  Per step:
+//                     S = Q K^T, dP = dO V^T               (SS, M=128 q, N=64 k)
+//                     dS -> bf16 in TMEM                   (softmax warps)
+//                     dQ += dS K                           (TS)
+// Layout of both (384 threads, one CTA per SM, persistent over the tile map):
+//   warp 0 TMA producer; warp 1 MMA issuer + TMEM owner; warps 4-7 and 8-11 two
+//   softmax warpgroups that take alternate steps, each with its own TMEM S/dP
+//   buffer, so the tensor core computes step i+1 while step i is exponentiated.
+// TMEM: S_0 | S_1 | dP_0 | dP_1 (64 columns each) | accumulators.
+#include "attn_params.cuh"
+#include "sm100_ptx.cuh"
+#include "tmap.cuh"
+
+namespace va {
+using namespace sm100;
+
+namespace {
+
+constexpr int kBwdThreads = 384;
+
+__device__ __forceinline__ void named_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+__device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 50000000ull) return;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t a, uint32_t* v) {
+  tmem_ld32(a, v);
+  tmem_wait_ld();
+}
+
+// ================================================================= dK / dV
+template <int D>
+struct KvCfg {
+  static constexpr int KB = 128, QB = 64;
+  static constexpr int QST = D == 128 ? 4 : 8;   // Q/dO ring slots (one step each)
+  static constexpr int TKV = KB * D * 2;         // one K or V tile
+  static constexpr int TQ = QB * D * 2;          // one Q or dO tile
+  static constexpr int PKV = KB * 128, PQ = QB * 128;  // 64-column panels
+  static constexpr int K_OFF = 0, V_OFF = TKV, RING_OFF = 2 * TKV;
+  static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [2 wg][2 slot][lse | D][64] fp32
+  static constexpr int BAR_OFF = LD_OFF + 2 * 2 * 2 * 64 * 4;
+  static constexpr int B_KVF = 0, B_KVE = 1, B_QF = 2, B_QE = 2 + QST, B_SF = 2 + 2 * QST,
+                       B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
+                       NBAR = B_DR + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+};
+
+struct KvItem {
+  int s0, l, n, hk, m_start, steps;
+};
+
+__device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
+  const TileItem it = p.kv_items[idx];
+  KvItem r;
+  r.s0 = p.cu[it.seg];
+  r.l = p.cu[it.seg + 1] - r.s0;
+  r.n = it.blk;
+  r.hk = it.head;
+  const int Mq = (r.l + 63) / 64;
+  r.m_start = Mq - it.count;
+  r.steps = it.count * p.g;
+  return r;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                   const BwdParams p) {
+  using C = KvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::MISC_OFF + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
+
+  if (p.hdr->status != VA_OK) return;
+  const int n_items = p.hdr->n_items[p.kv_slot];
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KVF), 1);
+    mbar_init(bar(C::B_KVE), 1);
+    for (int s = 0; s < C::QST; ++s) {
+      mbar_init(bar(C::B_QF + s), 1);
+      mbar_init(bar(C::B_QE + s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::B_SF + x), 1);
+      mbar_init(bar(C::B_PF + x), 128);
+    }
+    mbar_init(bar(C::B_AF), 1);
+    mbar_init(bar(C::B_AE), 256);
+    mbar_init(bar(C::B_DR), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    prefetch_tmap(&tdo);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int qit = 0, item_cnt = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+        const KvItem I = kv_decode(p, idx);
+        ok = mbar_wait(bar(C::B_KVE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 21);
+        if (!ok) break;
+        mbar_expect_tx(bar(C::B_KVF), 2 * C::TKV);
+        for (int pn = 0; pn < D / 64; ++pn) {
+          tma_load_3d(base + C::K_OFF + pn * C::PKV, &tk, bar(C::B_KVF), pn * 64, I.hk, I.s0 + I.n * 128);
+          tma_load_3d(base + C::V_OFF + pn * C::PKV, &tv, bar(C::B_KVF), pn * 64, I.hk, I.s0 + I.n * 128);
+        }
+        for (int i = 0; ok && i < I.steps; ++i, ++qit) {
+          const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
+          const int s = qit % C::QST;
+          ok = mbar_wait(bar(C::B_QE + s), ((qit / C::QST) & 1) ^ 1, abort_flag, p.hdr, 22);
+          if (!ok) break;
+          mbar_expect_tx(bar(C::B_QF + s), 2 * C::TQ);
+          const uint32_t dst = base + C::RING_OFF + s * 2 * C::TQ;
+          for (int pn = 0; pn < D / 64; ++pn) {
+            tma_load_3d(dst + pn * C::PQ, &tq, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
+            tma_load_3d(dst + C::TQ + pn * C::PQ, &tdo, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
+          }
+        }
+      }
+      if (!ok) {
+        drain_wait_b(bar(C::B_KVF), item_cnt & 1);
+        for (int i = qit - 1; i >= 0 && i >= qit - C::QST; --i)
+          drain_wait_b(bar(C::B_QF + i % C::QST), (i / C::QST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idG = idesc_bf16(128, D, false, true);
+      int qit = 0, item_cnt = 0;
+      uint32_t pf[2] = {0, 0};
+      bool ok = true;
+      auto issue_SdP = [&](int x, int slot) {
+        const uint32_t q = base + C::RING_OFF + slot * 2 * C::TQ, d = q + C::TQ;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
+          mma_ss(tmem + x * 64, sdesc_sw128(base + C::K_OFF + okv, 16, 1024), sdesc_sw128(q + oq, 16, 1024),
+                 idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
+          mma_ss(tmem + 128 + x * 64, sdesc_sw128(base + C::V_OFF + okv, 16, 1024),
+                 sdesc_sw128(d + oq, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(bar(C::B_SF + x));
+      };
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+        const KvItem I = kv_decode(p, idx);
+        ok = mbar_wait(bar(C::B_KVF), item_cnt & 1, abort_flag, p.hdr, 23);
+        if (!ok) break;
+        for (int j = 0; ok && j < 2 && j < I.steps; ++j) {
+          const int s = (qit + j) % C::QST;
+          ok = mbar_wait(bar(C::B_QF + s), ((qit + j) / C::QST) & 1, abort_flag, p.hdr, 24);
+          if (!ok) break;
+          fence_after_sync();
+          issue_SdP(j, s);
+        }
+        if (!ok) break;
+        if (I.steps <= 2) mma_commit(bar(C::B_KVE));
+        for (int i = 0; ok && i < I.steps; ++i) {
+          const int x = i & 1, s = (qit + i) % C::QST;
+          ok = mbar_wait(bar(C::B_PF + x), pf[x] & 1, abort_flag, p.hdr, 25);
+          if (!ok) break;
+          ++pf[x];
+          if (i == 0) {  // the accumulators must have been read out by the previous epilogue
+            ok = mbar_wait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 26);
+            if (!ok) break;
+          }
+          fence_after_sync();
+          const uint32_t q = base + C::RING_OFF + s * 2 * C::TQ, d = q + C::TQ;
+#pragma unroll
+          for (int kk = 0; kk < C::QB / 16; ++kk)
+            mma_ts(tmem + 256, tmem + x * 64 + kk * 8, sdesc_sw128(d + kk * 2048, C::PQ, 1024), idG,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < C::QB / 16; ++kk)
+            mma_ts(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, sdesc_sw128(q + kk * 2048, C::PQ, 1024),
+                   idG, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(C::B_QE + s));
+          if (i + 2 < I.steps) {
+            const int s2 = (qit + i + 2) % C::QST;
+            ok = mbar_wait(bar(C::B_QF + s2), ((qit + i + 2) / C::QST) & 1, abort_flag, p.hdr, 27);
+            if (!ok) break;
+            fence_after_sync();
+            issue_SdP(x, s2);
+            if (i + 2 == I.steps - 1) mma_commit(bar(C::B_KVE));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(C::B_AF));
+        qit += I.steps;
+      }
+      mma_commit(bar(C::B_DR));
+      drain_wait_b(bar(C::B_DR), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: 0 -> dV, 1 -> dK
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int tid = threadIdx.x - 128 - 128 * x;  // 0..127 within the warpgroup
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + x * 64;
+    const uint32_t dp_addr = tmem + lane_off + 128 + x * 64;
+    const uint32_t acc_addr = tmem + lane_off + 256 + x * D;
+    float* ldbuf = reinterpret_cast<float*>(sm + C::LD_OFF) + x * 2 * 128;  // [slot][lse 64 | D 64]
+    const float sl2 = p.scale_log2;
+    uint32_t sf = 0;
+    int item_cnt = 0;
+    bool ok = true;
+    auto fetch = [&](const KvItem& I, int i, float& lv, float& dv) {
+      if (tid < 64) {
+        const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
+        const int qr = m * 64 + tid;
+        const int64_t at = static_cast<int64_t>(h) * p.T + I.s0 + qr;
+        lv = qr < I.l ? p.lse[at] * kLog2e : INFINITY;
+        dv = qr < I.l ? p.dsum[at] : 0.f;
+      }
+    };
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+      const KvItem I = kv_decode(p, idx);
+      const int kvrow = I.n * 128 + r;
+      int slot = 0;
+      if (x < I.steps) {
+        float lv = 0.f, dv = 0.f;
+        fetch(I, x, lv, dv);
+        if (tid < 64) {
+          ldbuf[tid] = lv;
+          ldbuf[64 + tid] = dv;
+        }
+      }
+      named_sync(1 + x);
+      for (int i = x; i < I.steps; i += 2) {
+        float nlv = 0.f, ndv = 0.f;
+        const bool have_next = i + 2 < I.steps;
+        if (have_next) fetch(I, i + 2, nlv, ndv);
+        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 28);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++sf;
+        fence_after_sync();
+        const int q0 = (I.m_start + i / p.g) * 64;
+        const int lim = kvrow - q0;  // query columns c < lim are masked (key after query)
+        const bool need_mask = p.causal && (I.n * 128 + 127 > q0);
+        const float* L = ldbuf + slot * 128;
+        const float* Dd = L + 64;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sv[32], dpv[32];
+          tmem_ld32(s_addr + hh * 32, sv);
+          tmem_ld32(dp_addr + hh * 32, dpv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 l2 = *reinterpret_cast<const float2*>(L + hh * 32 + c);
+            const float2 d2 = *reinterpret_cast<const float2*>(Dd + hh * 32 + c);
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -l2.x, -l2.y);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            if (need_mask) {
+              if (hh * 32 + c < lim) p0 = 0.f;
+              if (hh * 32 + c + 1 < lim) p1 = 0.f;
+            }
+            float t0, t1;
+            fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -d2.x, -d2.y);
+            sv[c >> 1] = pack_bf16(p0, p1);
+            dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
+          }
+          tmem_st16(s_addr + hh * 16, sv);
+          tmem_st16(dp_addr + hh * 16, dpv);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        mbar_arrive(bar(C::B_PF + x));
+        if (have_next && tid < 64) {
+          ldbuf[(slot ^ 1) * 128 + tid] = nlv;
+          ldbuf[(slot ^ 1) * 128 + 64 + tid] = ndv;
+        }
+        named_sync(1 + x);
+        slot ^= 1;
+      }
+      if (!ok) break;
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+      ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 29);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const float mul = x == 0 ? 1.f : p.scale;
+      const bool store = kvrow < I.l;
+      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>(I.s0 + kvrow) * p.k_rs +
+                  static_cast<int64_t>(I.hk) * p.k_hs;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(acc_addr + c * 32, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      fence_before_sync();
+      mbar_arrive(bar(C::B_AE));
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================= dQ
+namespace {
+
+template <int D>
+struct QCfg {
+  static constexpr int QB = 128, KB = 64;
+  static constexpr int KST = D == 128 ? 4 : 8;   // K/V ring slots (one step each)
+  static constexpr int TQ = QB * D * 2, TKV = KB * D * 2;
+  static constexpr int PQ = QB * 128, PKV = KB * 128;
+  static constexpr int Q_OFF = 0, DO_OFF = TQ, RING_OFF = 2 * TQ;
+  static constexpr int BAR_OFF = RING_OFF + KST * 2 * TKV;
+  static constexpr int B_QDF = 0, B_QDE = 1, B_KF = 2, B_KE = 2 + KST, B_SF = 2 + 2 * KST,
+                       B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
+                       NBAR = B_DR + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+};
+
+struct QItem {
+  int s0, l, m, h, hk, nb;
+};
+
+__device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
+  const TileItem it = p.q_items[idx];
+  QItem r;
+  r.s0 = p.cu[it.seg];
+  r.l = p.cu[it.seg + 1] - r.s0;
+  r.m = it.blk;
+  r.h = it.head;
+  r.hk = it.head / p.g;
+  r.nb = it.count;
+  return r;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                 const BwdParams p) {
+  using C = QCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::MISC_OFF + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
+
+  if (p.hdr->status != VA_OK) return;
+  const int n_items = p.hdr->n_items[p.q_slot];
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_QDF), 1);
+    mbar_init(bar(C::B_QDE), 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bar(C::B_KF + s), 1);
+      mbar_init(bar(C::B_KE + s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::B_SF + x), 1);
+      mbar_init(bar(C::B_PF + x), 128);
+    }
+    mbar_init(bar(C::B_AF), 1);
+    mbar_init(bar(C::B_AE), 256);
+    mbar_init(bar(C::B_DR), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    prefetch_tmap(&tdo);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int kit = 0, item_cnt = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+        const QItem I = q_decode(p, idx);
+        ok = mbar_wait(bar(C::B_QDE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 31);
+        if (!ok) break;
+        mbar_expect_tx(bar(C::B_QDF), 2 * C::TQ);
+        for (int pn = 0; pn < D / 64; ++pn) {
+          tma_load_3d(base + C::Q_OFF + pn * C::PQ, &tq, bar(C::B_QDF), pn * 64, I.h, I.s0 + I.m * 128);
+          tma_load_3d(base + C::DO_OFF + pn * C::PQ, &tdo, bar(C::B_QDF), pn * 64, I.h, I.s0 + I.m * 128);
+        }
+        for (int n = 0; ok && n < I.nb; ++n, ++kit) {
+          const int s = kit % C::KST;
+          ok = mbar_wait(bar(C::B_KE + s), ((kit / C::KST) & 1) ^ 1, abort_flag, p.hdr, 32);
+          if (!ok) break;
+          mbar_expect_tx(bar(C::B_KF + s), 2 * C::TKV);
+          const uint32_t dst = base + C::RING_OFF + s * 2 * C::TKV;
+          for (int pn = 0; pn < D / 64; ++pn) {
+            tma_load_3d(dst + pn * C::PKV, &tk, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
+            tma_load_3d(dst + C::TKV + pn * C::PKV, &tv, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
+          }
+        }
+      }
+      if (!ok) {
+        drain_wait_b(bar(C::B_QDF), item_cnt & 1);
+        for (int i = kit - 1; i >= 0 && i >= kit - C::KST; --i)
+          drain_wait_b(bar(C::B_KF + i % C::KST), (i / C::KST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idG = idesc_bf16(128, D, false, true);
+      int kit = 0, item_cnt = 0;
+      uint32_t pf[2] = {0, 0};
+      bool ok = true;
+      auto issue_SdP = [&](int x, int slot) {
+        const uint32_t kt = base + C::RING_OFF + slot * 2 * C::TKV, vt = kt + C::TKV;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
+          mma_ss(tmem + x * 64, sdesc_sw128(base + C::Q_OFF + oq, 16, 1024), sdesc_sw128(kt + ok_, 16, 1024),
+                 idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
+          mma_ss(tmem + 128 + x * 64, sdesc_sw128(base + C::DO_OFF + oq, 16, 1024),
+                 sdesc_sw128(vt + ok_, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(bar(C::B_SF + x));
+      };
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+        const QItem I = q_decode(p, idx);
+        ok = mbar_wait(bar(C::B_QDF), item_cnt & 1, abort_flag, p.hdr, 33);
+        if (!ok) break;
+        for (int j = 0; ok && j < 2 && j < I.nb; ++j) {
+          const int s = (kit + j) % C::KST;
+          ok = mbar_wait(bar(C::B_KF + s), ((kit + j) / C::KST) & 1, abort_flag, p.hdr, 34);
+          if (!ok) break;
+          fence_after_sync();
+          issue_SdP(j, s);
+        }
+        if (!ok) break;
+        if (I.nb <= 2) mma_commit(bar(C::B_QDE));
+        for (int n = 0; ok && n < I.nb; ++n) {
+          const int x = n & 1, s = (kit + n) % C::KST;
+          ok = mbar_wait(bar(C::B_PF + x), pf[x] & 1, abort_flag, p.hdr, 35);
+          if (!ok) break;
+          ++pf[x];
+          if (n == 0) {
+            ok = mbar_wait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 36);
+            if (!ok) break;
+          }
+          fence_after_sync();
+          const uint32_t kt = base + C::RING_OFF + s * 2 * C::TKV;
+#pragma unroll
+          for (int kk = 0; kk < C::KB / 16; ++kk)
+            mma_ts(tmem + 256, tmem + 128 + x * 64 + kk * 8, sdesc_sw128(kt + kk * 2048, C::PKV, 1024), idG,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(C::B_KE + s));
+          if (n + 2 < I.nb) {
+            const int s2 = (kit + n + 2) % C::KST;
+            ok = mbar_wait(bar(C::B_KF + s2), ((kit + n + 2) / C::KST) & 1, abort_flag, p.hdr, 37);
+            if (!ok) break;
+            fence_after_sync();
+            issue_SdP(x, s2);
+            if (n + 2 == I.nb - 1) mma_commit(bar(C::B_QDE));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(C::B_AF));
+        kit += I.nb;
+      }
+      mma_commit(bar(C::B_DR));
+      drain_wait_b(bar(C::B_DR), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: dQ columns [x D/2, (x+1) D/2)
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + x * 64;
+    const uint32_t dp_addr = tmem + lane_off + 128 + x * 64;
+    const uint32_t acc_addr = tmem + lane_off + 256;
+    const float sl2 = p.scale_log2;
+    uint32_t sf = 0;
+    int item_cnt = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
+      const QItem I = q_decode(p, idx);
+      const int qrow = I.m * 128 + r;
+      const int64_t at = static_cast<int64_t>(I.h) * p.T + I.s0 + qrow;
+      const float lse2 = qrow < I.l ? p.lse[at] * kLog2e : INFINITY;
+      const float dsum = qrow < I.l ? p.dsum[at] : 0.f;
+      for (int n = x; n < I.nb; n += 2) {
+        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 38);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++sf;
+        fence_after_sync();
+        // key columns c > lim are masked: after the query (causal) or past the segment end
+        const int lim = p.causal ? qrow - n * 64 : I.l - 1 - n * 64;
+        const bool need_mask = p.causal ? (n * 64 + 63 > I.m * 128) : (n * 64 + 64 > I.l);
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sv[32], dpv[32];
+          tmem_ld32(s_addr + hh * 32, sv);
+          tmem_ld32(dp_addr + hh * 32, dpv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            if (need_mask) {
+              if (hh * 32 + c > lim) p0 = 0.f;
+              if (hh * 32 + c + 1 > lim) p1 = 0.f;
+            }
+            float t0, t1;
+            fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
+            dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
+          }
+          tmem_st16(dp_addr + hh * 16, dpv);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        mbar_arrive(bar(C::B_PF + x));
+      }
+      if (!ok) break;
+      // epilogue: this warpgroup's half of the dQ columns
+      ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 39);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const bool store = qrow < I.l;
+      bf16* out = p.dq + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
+#pragma unroll 1
+      for (int c = x * (D / 64); c < (x + 1) * (D / 64); ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(acc_addr + c * 32, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * p.scale, __uint_as_float(o[2 * j + 1]) * p.scale);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      fence_before_sync();
+      mbar_arrive(bar(C::B_AE));
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int D>
+static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
+  using C = KvCfg<D>;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!tmap_rows(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs, 64) ||
+      !tmap_rows(&tdo, p.dout, p.T, p.Hq, D, p.o_rs, p.o_hs, 64) ||
+      !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
+      !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = std::min(cap, std::max(sms, 1));
+  if (grid <= 0) return cudaSuccess;
+  dkdv_tc_kernel<D><<<grid, kBwdThreads, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
+  using C = QCfg<D>;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!tmap_rows(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs, 128) ||
+      !tmap_rows(&tdo, p.dout, p.T, p.Hq, D, p.o_rs, p.o_hs, 128) ||
+      !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 64) ||
+      !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 64))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = std::min(cap, std::max(sms, 1));
+  if (grid <= 0) return cudaSuccess;
+  dq_tc_kernel<D><<<grid, kBwdThreads, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv_tc(const BwdParams& p, int d, int cap, cudaStream_t st) {
+  return d == 64 ? launch_dkdv_d<64>(p, cap, st) : launch_dkdv_d<128>(p, cap, st);
+}
+
+cudaError_t launch_bwd_dq_tc(const BwdParams& p, int d, int cap, cudaStream_t st) {
+  return d == 64 ? launch_dq_d<64>(p, cap, st) : launch_dq_d<128>(p, cap, st);
+}
+
+void bwd_tc_tiles(int* kvBM, int* kvBN, int* qBM, int* qBN) {
+  *kvBM = 64;
+  *kvBN = 128;
+  *qBM = 128;
+  *qBN = 64;
+}
+
+}  // namespace va

@@ -21,10 +21,9 @@
 // shared-memory fill traffic per FLOP; while one tile's softmax runs, the tensor
 // core works on the other tile.  The running max is only raised when it grows by
 // more than 2^8, so O in TMEM is rescaled rarely.
-#include <cudaTypedefs.h>
-
 #include "attn_params.cuh"
 #include "sm100_ptx.cuh"
+#include "tmap.cuh"
 
 namespace va {
 using namespace sm100;
@@ -77,6 +76,62 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > 50000000ull) return;
   }
+}
+
+// Row max (x scale*log2e) of the 128 scores at s_addr; columns j > lim are ignored when MASK.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t s_addr, int lim, float sl2) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll 1
+  for (int h2 = 0; h2 < 2; ++h2) {
+    uint32_t v[64];
+    tmem_ld32(s_addr + h2 * 64, v);
+    tmem_ld32(s_addr + h2 * 64 + 32, v + 32);
+    tmem_wait_ld();
+    if (MASK) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (h2 * 64 + j > lim) v[j] = __float_as_uint(-INFINITY);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      m0 = fmax3(m0, __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
+      m1 = fmax3(m1, __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+    }
+  }
+  return fmaxf(m0, m1) * sl2;
+}
+
+// P = exp2(s * sl2 - mu) for the 128 scores at s_addr, written as bf16 pairs into the
+// first 64 columns.  Returns the row sum of P.
+template <bool MASK>
+__device__ __forceinline__ float row_exp(uint32_t s_addr, int lim, float sl2, float mu) {
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  // Quarter q reads score columns [32 q, 32 q + 32) and writes P columns [16 q, 16 q + 16),
+  // which only overlap scores already read.  Not unrolled: unrolled, the TMEM loads of all
+  // quarters are hoisted and the row spills.
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {
+    uint32_t v[32];
+    tmem_ld32(s_addr + q * 32, v);
+    tmem_wait_ld();
+    if (MASK) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (q * 32 + j > lim) v[j] = __float_as_uint(-INFINITY);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float x0, x1;
+      ffma2(x0, x1, __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sl2, sl2, -mu, -mu);
+      const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+      if (j & 1) fadd2(b0, b1, b0, b1, p0, p1);
+      else fadd2(a0, a1, a0, a1, p0, p1);
+      v[j] = pack_bf16(p0, p1);
+    }
+    tmem_st16(s_addr + q * 16, v);
+  }
+  return (a0 + a1) + (b0 + b1);
 }
 
 }  // namespace
@@ -268,75 +323,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         ++sf;
         fence_after_sync();
-        // pass 1: row max over the 128 scores, 64 columns at a time
+        // The causal mask touches only the last key tile of each q tile (its diagonal
+        // tile); non-causal masks only key columns past the segment end.
         const bool need_mask = p.causal ? (n == nbt - 1) : (n * kTcBN + kTcBN > I.l);
-        const int col0 = n * kTcBN;
-        const int lim = p.causal ? qrow - col0 : I.l - 1 - col0;  // columns j > lim are masked
-        float mx = -INFINITY;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t v[64];
-          tmem_ld32(s_addr + h2 * 64, v);
-          tmem_ld32(s_addr + h2 * 64 + 32, v + 32);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float x = __uint_as_float(v[j]);
-            mx = (need_mask && h2 * 64 + j > lim) ? mx : fmaxf(mx, x);
-          }
-        }
-        const float m_new = fmaxf(m_ref, mx * sl2);
-        const bool resc = m_new > m_ref + kRescaleThreshold;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = fast_exp2(m_ref - m_new);
-          lsum *= alpha;
-        }
-        if (__any_sync(0xffffffffu, resc && n > 0)) {
-          // O_t holds PV_{n-1}: wait for it, then scale this row in TMEM
-          ok = mbar_wait(bar(C::B_OF + t), (of_base + n - 1) & 1, abort_flag, p.hdr, 10);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          fence_after_sync();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(o_addr + c * 32, o);
-          }
-          tmem_wait_st();
-        }
-        if (resc) m_ref = m_new;
-        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        // pass 2: P = exp2(s * scale * log2e - m) as bf16 into the first 64 columns of S_t.
-        // Half h2 reads columns [64 h2, 64 h2 + 64) and writes P columns [32 h2, 32 h2 + 32),
-        // which only overlap score columns already read.
-        float rs = 0.f;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t v[64];
-          tmem_ld32(s_addr + h2 * 64, v);
-          tmem_ld32(s_addr + h2 * 64 + 32, v + 32);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * j]), sl2, -mu));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), sl2, -mu));
-            if (need_mask) {
-              if (h2 * 64 + 2 * j > lim) p0 = 0.f;
-              if (h2 * 64 + 2 * j + 1 > lim) p1 = 0.f;
+        const int lim = p.causal ? qrow - n * kTcBN : I.l - 1 - n * kTcBN;  // mask j > lim
+        // Row max first (the exponent pass overwrites scores with P, so it runs once, last).
+        const float mt = need_mask ? row_max<true>(s_addr, lim, sl2) : row_max<false>(s_addr, lim, sl2);
+        if (n == 0) {
+          m_ref = mt;
+        } else {
+          // the reference max is raised only when the row max grew by more than 2^8 (rare);
+          // then O_t, which holds PV_{n-1}, is rescaled in TMEM
+          const bool resc = mt > m_ref + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, resc)) {
+            const float alpha = resc ? fast_exp2(m_ref - mt) : 1.f;
+            if (resc) {
+              m_ref = mt;
+              lsum *= alpha;
             }
-            rs += p0 + p1;
-            v[j] = pack_bf16(p0, p1);
+            ok = mbar_wait(bar(C::B_OF + t), (of_base + n - 1) & 1, abort_flag, p.hdr, 10);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tmem_st32(o_addr + c * 32, o);
+            }
+            tmem_wait_st();
           }
-          tmem_st16(s_addr + h2 * 32, v);
-          tmem_st16(s_addr + h2 * 32 + 16, v + 16);
         }
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        const float rs = need_mask ? row_exp<true>(s_addr, lim, sl2, mu) : row_exp<false>(s_addr, lim, sl2, mu);
         lsum += rs;
         tmem_wait_st();
         fence_before_sync();
@@ -384,43 +408,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// [T, H, d] bf16 with row/head strides (elements) -> 3-D map (d, H, T), box (64, 1, 128), 128B swizzle.
-static bool make_map(CUtensorMap* m, const void* ptr, int T, int H, int d, int64_t row_stride,
-                     int64_t head_stride) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(T)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_stride) * 2,
-                           static_cast<cuuint64_t>(row_stride) * 2};
-  cuuint32_t box[3] = {64, 1, 128};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int D>
 static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
   using C = TcCfg<D>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs) ||
-      !make_map(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs) ||
-      !make_map(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs))
+  if (!tmap_rows(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs, 128) ||
+      !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
+      !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;

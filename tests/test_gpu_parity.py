@@ -307,3 +307,23 @@ def test_device_detected_bad_boundaries(va):
             va.varlen_attn_bwd(q, k, v, q, torch.zeros(H, T, device=DEV), do, cu, mx, dq=dq,
                                check_status=True)
         assert bool((dq == 3.0).all())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_running_max_rescale_path(va, d):
+    """Keys whose magnitude grows along each segment make the row max jump by far more than
+    2^8 between key tiles, which forces the forward to rescale O in TMEM; neighbouring
+    segments sit in the same tiles, so a wrong rescale would also break isolation."""
+    lengths = [700, 90, 1100, 33]
+    cu, _, _, mx = op.build_metadata(lengths)
+    T, H = int(cu[-1]), 4
+    q, k, v, do = si.tensors(T, H, H, d, seed_offset=77)
+    ramp = torch.ones(T)
+    for b in range(len(lengths)):
+        s, e = int(cu[b]), int(cu[b + 1])
+        ramp[s:e] = 1.0 + torch.arange(e - s, dtype=torch.float32) / 48.0
+    k = (k.float() * ramp[:, None, None]).to(torch.bfloat16)
+    o, lse, g = run_gpu(va, q, k, v, do, torch.tensor(cu, device=DEV), mx)
+    ro, rl, rg = run_oracle(q, k, v, do, cu)
+    wl.assert_close_outputs(o, lse, ro, rl)
+    wl.assert_close_grads(g, rg)
