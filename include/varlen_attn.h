@@ -196,6 +196,27 @@ va_status varlen_attn_bwd(const void* q_dev, const void* k_dev, const void* v_de
                           int32_t causal, void* dq_dev, void* dk_dev, void* dv_dev, void* ws_dev,
                           size_t ws_bytes, va_stream_t stream);
 
+/* Forward without a workspace, for callers that cannot allocate device memory
+ * where they run attention (a plugin inside a host runtime that owns all device
+ * allocations, or a serving loop that must not call cudaMalloc because it can
+ * synchronise the device).  The pages have no counterpart: this is a deployment
+ * convenience.  Same arguments, layouts and results as varlen_attn_fwd, without
+ * ws_dev/ws_bytes: the scratch (status header and tile map) lives in a 1 MiB
+ * static device array that every GPU loading this library holds until exit.
+ *   - Limit: (T/256 rounded down + B) * Hq <= 65520 tile records; larger shapes
+ *     return VA_ERR_WORKSPACE with a message.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on that device.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (each call rewrites what it reads).  Calls that overlap on the
+ *     GPU race on it: serialise them (one stream, or events between streams).
+ *   - Allocates nothing.  Device-detected errors (a cu_seqlens that breaks the
+ *     contract) leave out/lse unwritten; the status word is not exposed. */
+va_status varlen_attn_fwd_noalloc(const void* q_dev, const void* k_dev, const void* v_dev,
+                                  const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
+                                  int32_t causal, void* out_dev, float* lse_dev, va_stream_t stream);
+
 /* Copies the workspace status word to *status_host after synchronising the
  * stream.  VA_ERR_CUDA if the copy fails. */
 va_status varlen_read_status(const void* ws_dev, int32_t* status_host, va_stream_t stream);

@@ -24,6 +24,7 @@ EXPORTS = (
     "varlen_attn_workspace_size", "varlen_attn_plan", "varlen_attn_fwd", "varlen_attn_bwd",
     "varlen_read_status", "varlen_clear_status", "varlen_last_error", "varlen_version",
     "varlen_profile_enable", "varlen_profile_read", "varlen_kernel_name", "varlen_launch_count",
+    "varlen_attn_fwd_noalloc",
 )
 
 
@@ -66,6 +67,9 @@ def _declare(lib):
         "varlen_attn_bwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                       c_void_p, POINTER(VaShape), c_float, c_int32, c_void_p,
                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+        "varlen_attn_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
+                                              POINTER(VaShape), c_float, c_int32, c_void_p,
+                                              c_void_p, c_void_p]),
         "varlen_read_status": (c_int32, [c_void_p, i32p, c_void_p]),
         "varlen_clear_status": (c_int32, [c_void_p, c_void_p]),
         "varlen_profile_enable": (c_int32, [c_int32]),
