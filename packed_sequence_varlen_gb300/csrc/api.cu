@@ -18,6 +18,7 @@ cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaSt
 cudaError_t launch_plan(const int32_t*, int, int, int, int, int, int, int, TileItem*, int, int32_t*,
                         int32_t*, cudaStream_t);
 int plan_max_keys();
+cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, cudaStream_t);
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
 cudaError_t launch_bwd_rowsum(const BwdParams&, int, cudaStream_t);
@@ -32,11 +33,11 @@ void set_error(const char* msg) { g_error = msg; }
 // ------------------------------------------------------------ launch accounting
 enum KernelId {
   K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_ROWSUM, K_BWD_DKDV, K_BWD_DQ,
-  K_COUNT
+  K_VALIDATE_PLAN, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
-    "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan",
-    "fwd",                 "bwd_rowsum",    "bwd_dkdv",      "bwd_dq"};
+    "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan", "fwd",
+    "bwd_rowsum",          "bwd_dkdv",      "bwd_dq",        "validate_plan"};
 
 struct Profiler {
   std::vector<cudaEvent_t> start, stop;
@@ -263,16 +264,18 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   uint8_t* w = static_cast<uint8_t*>(ws);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
   TileItem* map = reinterpret_cast<TileItem*>(w + L.map);
-  cudaError_t e = launch(K_VALIDATE, cs, [&] {
-    return launch_validate(cu, s->B, s->T, s->max_seqlen, &hdr->status, 1, cs);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "fwd validate");
-  if (s->T == 0) return VA_OK;
+  if (s->T == 0) {  // nothing to compute; still report a contract violation
+    cudaError_t e = launch(K_VALIDATE, cs, [&] {
+      return launch_validate(cu, s->B, s->T, s->max_seqlen, &hdr->status, 1, cs);
+    });
+    return e == cudaSuccess ? VA_OK : cuda_fail(e, "fwd validate");
+  }
   int BM, BN;
   tiles(0, &BM, &BN);
-  e = launch(K_PLAN, cs, [&] {
-    return launch_plan(cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map_kmax(*s, 0), map,
-                       static_cast<int>(L.cap), &hdr->status, &hdr->n_items[0], cs);
+  const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map_kmax(*s, 0), map,
+                    static_cast<int>(L.cap), &hdr->status, &hdr->n_items[0]};
+  cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
+    return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cs);
   });
   if (e != cudaSuccess) return cuda_fail(e, "fwd plan");
   FwdParams p{};
@@ -322,24 +325,24 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
   TileItem* kvmap = reinterpret_cast<TileItem*>(w + L.kvmap);
   TileItem* qmap = reinterpret_cast<TileItem*>(w + L.qmap);
-  cudaError_t e = launch(K_VALIDATE, cs, [&] {
-    return launch_validate(cu, s->B, s->T, s->max_seqlen, &hdr->status, 1, cs);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "bwd validate");
-  if (s->T == 0) return VA_OK;
-  int BM, BN;
+  if (s->T == 0) {
+    cudaError_t e = launch(K_VALIDATE, cs, [&] {
+      return launch_validate(cu, s->B, s->T, s->max_seqlen, &hdr->status, 1, cs);
+    });
+    return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd validate");
+  }
+  int BM, BN, BM2, BN2;
   tiles(1, &BM, &BN);
-  e = launch(K_PLAN, cs, [&] {
-    return launch_plan(cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, map_kmax(*s, 1), kvmap,
-                       static_cast<int>(L.cap_kv), &hdr->status, &hdr->n_items[1], cs);
+  tiles(2, &BM2, &BN2);
+  const PlanArgs pa[2] = {
+      {cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, map_kmax(*s, 1), kvmap, static_cast<int>(L.cap_kv),
+       &hdr->status, &hdr->n_items[1]},
+      {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, map_kmax(*s, 2), qmap, static_cast<int>(L.cap_q),
+       &hdr->status, &hdr->n_items[2]}};
+  cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
+    return launch_validate_plan(pa, 2, s->T, s->max_seqlen, cs);
   });
-  if (e != cudaSuccess) return cuda_fail(e, "bwd plan kv");
-  tiles(2, &BM, &BN);
-  e = launch(K_PLAN, cs, [&] {
-    return launch_plan(cu, s->B, s->Hq, BM, BN, 2, causal ? 1 : 0, map_kmax(*s, 2), qmap,
-                       static_cast<int>(L.cap_q), &hdr->status, &hdr->n_items[2], cs);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "bwd plan q");
+  if (e != cudaSuccess) return cuda_fail(e, "bwd plan");
   BwdParams p{};
   p.q = static_cast<const bf16*>(q);
   p.k = static_cast<const bf16*>(k);

@@ -54,18 +54,20 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t a, uint32_t* v) {
 template <int D>
 struct KvCfg {
   static constexpr int KB = 128, QB = 64;
-  static constexpr int QST = D == 128 ? 4 : 8;   // Q/dO ring slots (one step each)
+  static constexpr int QST = D == 128 ? 3 : 8;   // Q/dO ring slots (one step each)
   static constexpr int TKV = KB * D * 2;         // one K or V tile
   static constexpr int TQ = QB * D * 2;          // one Q or dO tile
   static constexpr int PKV = KB * 128, PQ = QB * 128;  // 64-column panels
-  static constexpr int K_OFF = 0, V_OFF = TKV, RING_OFF = 2 * TKV;
+  // two K/V buffers (items alternate): buffer b holds K at KV_OFF(b), V right after
+  static constexpr int RING_OFF = 4 * TKV;
   static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [2 wg][2 slot][lse | D][64] fp32
   static constexpr int BAR_OFF = LD_OFF + 2 * 2 * 2 * 64 * 4;
-  static constexpr int B_KVF = 0, B_KVE = 1, B_QF = 2, B_QE = 2 + QST, B_SF = 2 + 2 * QST,
+  static constexpr int B_KVF = 0, B_KVE = 2, B_QF = 4, B_QE = 4 + QST, B_SF = 4 + 2 * QST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
                        NBAR = B_DR + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+  static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
+  __host__ __device__ static constexpr uint32_t kv_off(int b) { return static_cast<uint32_t>(b) * 2 * TKV; }
 };
 
 struct KvItem {
@@ -93,10 +95,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const BwdParams p) {
   using C = KvCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sm = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw;
+  if (base & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicCAS(&p.hdr->status, 0, VA_ERR_CUDA);
+    return;
+  }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,8 +112,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::B_KVF), 1);
-    mbar_init(bar(C::B_KVE), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_KVF + b), 1);
+      mbar_init(bar(C::B_KVE + b), 1);
+    }
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(C::B_QF + s), 1);
       mbar_init(bar(C::B_QE + s), 1);
@@ -143,14 +150,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int qit = 0, item_cnt = 0;
       bool ok = true;
+      KvItem nxt = kv_decode(p, blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const KvItem I = kv_decode(p, idx);
-        ok = mbar_wait(bar(C::B_KVE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 21);
+        const KvItem I = nxt;
+        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = kv_decode(p, idx + gridDim.x);
+        const int kb = item_cnt & 1;
+        ok = mbar_wait(bar(C::B_KVE + kb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 21);
         if (!ok) break;
-        mbar_expect_tx(bar(C::B_KVF), 2 * C::TKV);
+        mbar_expect_tx(bar(C::B_KVF + kb), 2 * C::TKV);
         for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(base + C::K_OFF + pn * C::PKV, &tk, bar(C::B_KVF), pn * 64, I.hk, I.s0 + I.n * 128);
-          tma_load_3d(base + C::V_OFF + pn * C::PKV, &tv, bar(C::B_KVF), pn * 64, I.hk, I.s0 + I.n * 128);
+          tma_load_3d(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, I.hk,
+                      I.s0 + I.n * 128);
+          tma_load_3d(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
+                      I.hk, I.s0 + I.n * 128);
         }
         for (int i = 0; ok && i < I.steps; ++i, ++qit) {
           const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (!ok) {
-        drain_wait_b(bar(C::B_KVF), item_cnt & 1);
+        drain_wait_b(bar(C::B_KVF + (item_cnt & 1)), (item_cnt >> 1) & 1);
         for (int i = qit - 1; i >= 0 && i >= qit - C::QST; --i)
           drain_wait_b(bar(C::B_QF + i % C::QST), (i / C::QST) & 1);
       }
@@ -179,25 +191,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int qit = 0, item_cnt = 0;
       uint32_t pf[2] = {0, 0};
       bool ok = true;
+      int kb = 0;
       auto issue_SdP = [&](int x, int slot) {
         const uint32_t q = base + C::RING_OFF + slot * 2 * C::TQ, d = q + C::TQ;
+        const uint32_t kt = base + C::kv_off(kb), vt = kt + C::TKV;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
-          mma_ss(tmem + x * 64, sdesc_sw128(base + C::K_OFF + okv, 16, 1024), sdesc_sw128(q + oq, 16, 1024),
-                 idS, kk > 0);
+          mma_ss(tmem + x * 64, sdesc_sw128(kt + okv, 16, 1024), sdesc_sw128(q + oq, 16, 1024), idS,
+                 kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
-          mma_ss(tmem + 128 + x * 64, sdesc_sw128(base + C::V_OFF + okv, 16, 1024),
-                 sdesc_sw128(d + oq, 16, 1024), idS, kk > 0);
+          mma_ss(tmem + 128 + x * 64, sdesc_sw128(vt + okv, 16, 1024), sdesc_sw128(d + oq, 16, 1024), idS,
+                 kk > 0);
         }
         mma_commit(bar(C::B_SF + x));
       };
+      KvItem nxt = kv_decode(p, blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const KvItem I = kv_decode(p, idx);
-        ok = mbar_wait(bar(C::B_KVF), item_cnt & 1, abort_flag, p.hdr, 23);
+        const KvItem I = nxt;
+        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = kv_decode(p, idx + gridDim.x);
+        kb = item_cnt & 1;
+        ok = mbar_wait(bar(C::B_KVF + kb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 23);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.steps; ++j) {
           const int s = (qit + j) % C::QST;
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           issue_SdP(j, s);
         }
         if (!ok) break;
-        if (I.steps <= 2) mma_commit(bar(C::B_KVE));
+        if (I.steps <= 2) mma_commit(bar(C::B_KVE + kb));
         for (int i = 0; ok && i < I.steps; ++i) {
           const int x = i & 1, s = (qit + i) % C::QST;
           ok = mbar_wait(bar(C::B_PF + x), pf[x] & 1, abort_flag, p.hdr, 25);
@@ -234,7 +251,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             fence_after_sync();
             issue_SdP(x, s2);
-            if (i + 2 == I.steps - 1) mma_commit(bar(C::B_KVE));
+            if (i + 2 == I.steps - 1) mma_commit(bar(C::B_KVE + kb));
           }
         }
         if (!ok) break;
@@ -268,8 +285,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         dv = qr < I.l ? p.dsum[at] : 0.f;
       }
     };
+    KvItem nxt = kv_decode(p, blockIdx.x);
     for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-      const KvItem I = kv_decode(p, idx);
+      const KvItem I = nxt;
+      if (idx + static_cast<int>(gridDim.x) < n_items) nxt = kv_decode(p, idx + gridDim.x);
       const int kvrow = I.n * 128 + r;
       int slot = 0;
       if (x < I.steps) {
@@ -377,16 +396,18 @@ namespace {
 template <int D>
 struct QCfg {
   static constexpr int QB = 128, KB = 64;
-  static constexpr int KST = D == 128 ? 4 : 8;   // K/V ring slots (one step each)
+  static constexpr int KST = D == 128 ? 3 : 8;   // K/V ring slots (one step each)
   static constexpr int TQ = QB * D * 2, TKV = KB * D * 2;
   static constexpr int PQ = QB * 128, PKV = KB * 128;
-  static constexpr int Q_OFF = 0, DO_OFF = TQ, RING_OFF = 2 * TQ;
+  // two Q/dO buffers (items alternate): buffer b holds Q at qd_off(b), dO right after
+  static constexpr int RING_OFF = 4 * TQ;
   static constexpr int BAR_OFF = RING_OFF + KST * 2 * TKV;
-  static constexpr int B_QDF = 0, B_QDE = 1, B_KF = 2, B_KE = 2 + KST, B_SF = 2 + 2 * KST,
+  static constexpr int B_QDF = 0, B_QDE = 2, B_KF = 4, B_KE = 4 + KST, B_SF = 4 + 2 * KST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
                        NBAR = B_DR + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+  static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
+  __host__ __device__ static constexpr uint32_t qd_off(int b) { return static_cast<uint32_t>(b) * 2 * TQ; }
 };
 
 struct QItem {
@@ -413,10 +434,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  const BwdParams p) {
   using C = QCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sm = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw;
+  if (base & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicCAS(&p.hdr->status, 0, VA_ERR_CUDA);
+    return;
+  }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -427,8 +451,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::B_QDF), 1);
-    mbar_init(bar(C::B_QDE), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_QDF + b), 1);
+      mbar_init(bar(C::B_QDE + b), 1);
+    }
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bar(C::B_KF + s), 1);
       mbar_init(bar(C::B_KE + s), 1);
@@ -463,14 +489,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int kit = 0, item_cnt = 0;
       bool ok = true;
+      QItem nxt = q_decode(p, blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const QItem I = q_decode(p, idx);
-        ok = mbar_wait(bar(C::B_QDE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 31);
+        const QItem I = nxt;
+        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = q_decode(p, idx + gridDim.x);
+        const int qb = item_cnt & 1;
+        ok = mbar_wait(bar(C::B_QDE + qb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 31);
         if (!ok) break;
-        mbar_expect_tx(bar(C::B_QDF), 2 * C::TQ);
+        mbar_expect_tx(bar(C::B_QDF + qb), 2 * C::TQ);
         for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(base + C::Q_OFF + pn * C::PQ, &tq, bar(C::B_QDF), pn * 64, I.h, I.s0 + I.m * 128);
-          tma_load_3d(base + C::DO_OFF + pn * C::PQ, &tdo, bar(C::B_QDF), pn * 64, I.h, I.s0 + I.m * 128);
+          tma_load_3d(base + C::qd_off(qb) + pn * C::PQ, &tq, bar(C::B_QDF + qb), pn * 64, I.h,
+                      I.s0 + I.m * 128);
+          tma_load_3d(base + C::qd_off(qb) + C::TQ + pn * C::PQ, &tdo, bar(C::B_QDF + qb), pn * 64, I.h,
+                      I.s0 + I.m * 128);
         }
         for (int n = 0; ok && n < I.nb; ++n, ++kit) {
           const int s = kit % C::KST;
@@ -485,7 +516,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (!ok) {
-        drain_wait_b(bar(C::B_QDF), item_cnt & 1);
+        drain_wait_b(bar(C::B_QDF + (item_cnt & 1)), (item_cnt >> 1) & 1);
         for (int i = kit - 1; i >= 0 && i >= kit - C::KST; --i)
           drain_wait_b(bar(C::B_KF + i % C::KST), (i / C::KST) & 1);
       }
@@ -498,25 +529,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int kit = 0, item_cnt = 0;
       uint32_t pf[2] = {0, 0};
       bool ok = true;
+      int qb = 0;
       auto issue_SdP = [&](int x, int slot) {
         const uint32_t kt = base + C::RING_OFF + slot * 2 * C::TKV, vt = kt + C::TKV;
+        const uint32_t qt = base + C::qd_off(qb), dt = qt + C::TQ;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
-          mma_ss(tmem + x * 64, sdesc_sw128(base + C::Q_OFF + oq, 16, 1024), sdesc_sw128(kt + ok_, 16, 1024),
-                 idS, kk > 0);
+          mma_ss(tmem + x * 64, sdesc_sw128(qt + oq, 16, 1024), sdesc_sw128(kt + ok_, 16, 1024), idS,
+                 kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
-          mma_ss(tmem + 128 + x * 64, sdesc_sw128(base + C::DO_OFF + oq, 16, 1024),
-                 sdesc_sw128(vt + ok_, 16, 1024), idS, kk > 0);
+          mma_ss(tmem + 128 + x * 64, sdesc_sw128(dt + oq, 16, 1024), sdesc_sw128(vt + ok_, 16, 1024), idS,
+                 kk > 0);
         }
         mma_commit(bar(C::B_SF + x));
       };
+      QItem nxt = q_decode(p, blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const QItem I = q_decode(p, idx);
-        ok = mbar_wait(bar(C::B_QDF), item_cnt & 1, abort_flag, p.hdr, 33);
+        const QItem I = nxt;
+        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = q_decode(p, idx + gridDim.x);
+        qb = item_cnt & 1;
+        ok = mbar_wait(bar(C::B_QDF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 33);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.nb; ++j) {
           const int s = (kit + j) % C::KST;
@@ -526,7 +562,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           issue_SdP(j, s);
         }
         if (!ok) break;
-        if (I.nb <= 2) mma_commit(bar(C::B_QDE));
+        if (I.nb <= 2) mma_commit(bar(C::B_QDE + qb));
         for (int n = 0; ok && n < I.nb; ++n) {
           const int x = n & 1, s = (kit + n) % C::KST;
           ok = mbar_wait(bar(C::B_PF + x), pf[x] & 1, abort_flag, p.hdr, 35);
@@ -549,7 +585,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             fence_after_sync();
             issue_SdP(x, s2);
-            if (n + 2 == I.nb - 1) mma_commit(bar(C::B_QDE));
+            if (n + 2 == I.nb - 1) mma_commit(bar(C::B_QDE + qb));
           }
         }
         if (!ok) break;
@@ -572,8 +608,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t sf = 0;
     int item_cnt = 0;
     bool ok = true;
+    QItem nxt = q_decode(p, blockIdx.x);
     for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-      const QItem I = q_decode(p, idx);
+      const QItem I = nxt;
+      if (idx + static_cast<int>(gridDim.x) < n_items) nxt = q_decode(p, idx + gridDim.x);
       const int qrow = I.m * 128 + r;
       const int64_t at = static_cast<int64_t>(I.h) * p.T + I.s0 + qrow;
       const float lse2 = qrow < I.l ? p.lse[at] * kLog2e : INFINITY;

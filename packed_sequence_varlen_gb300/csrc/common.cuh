@@ -24,6 +24,21 @@ struct alignas(16) TileItem {  // one scheduler record
   int32_t seg, blk, head, count;
 };
 
+// Arguments of one tile-map build (see plan.cu).
+struct PlanArgs {
+  const int32_t* cu;
+  int B;
+  int heads;
+  int BM, BN;
+  int kind;  // 0/2: q-block map, 1: kv-block map
+  int causal;
+  int kmax;  // largest possible key
+  TileItem* out;
+  int capacity;
+  int32_t* status;   // may be null: no status to honour or report
+  int32_t* n_items;  // out
+};
+
 __device__ __forceinline__ void set_status(WsHeader* h, int code) {
   atomicCAS(&h->status, 0, code);
 }

@@ -37,14 +37,15 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct TcCfg {
-  static constexpr int NST = D == 128 ? 4 : 8;         // K/V ring slots
+  static constexpr int NST = D == 128 ? 3 : 8;         // K/V ring slots
   static constexpr int TILE = 128 * D * 2;             // bytes of one 128-row Q, K or V tile
   static constexpr int PANEL = 128 * 128;              // one 64-column (128-byte) panel of a tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = 2 * TILE;
+  static constexpr int Q_OFF = 0;                      // two Q buffers (items alternate), 2 tiles each
+  static constexpr int KV_OFF = 4 * TILE;
   static constexpr int BAR_OFF = KV_OFF + NST * TILE;
-  // barriers: q_full, q_empty, kv_full[NST], kv_empty[NST], s_full[2], p_full[2], o_full[2], drain
-  static constexpr int B_QF = 0, B_QE = 1, B_KVF = 2, B_KVE = 2 + NST, B_SF = 2 + 2 * NST,
+  // barriers: q_full[2], q_empty[2], kv_full[NST], kv_empty[NST], s_full[2], p_full[2],
+  // o_full[2], drain
+  static constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + NST, B_SF = 4 + 2 * NST,
                        B_PF = B_SF + 2, B_OF = B_PF + 2, B_DR = B_OF + 2, NBAR = B_DR + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + slack to align the base to 1024
@@ -79,27 +80,27 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Row max (x scale*log2e) of the 128 scores at s_addr; columns j > lim are ignored when MASK.
+// One TMEM round trip: all four 32-column loads, then one wait.
 template <bool MASK>
 __device__ __forceinline__ float row_max(uint32_t s_addr, int lim, float sl2) {
-  float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll 1
-  for (int h2 = 0; h2 < 2; ++h2) {
-    uint32_t v[64];
-    tmem_ld32(s_addr + h2 * 64, v);
-    tmem_ld32(s_addr + h2 * 64 + 32, v + 32);
-    tmem_wait_ld();
-    if (MASK) {
+  uint32_t v[128];
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (h2 * 64 + j > lim) v[j] = __float_as_uint(-INFINITY);
-    }
+  for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
+  tmem_wait_ld();
+  if (MASK) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      m0 = fmax3(m0, __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
-      m1 = fmax3(m1, __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-    }
+    for (int j = 0; j < 128; ++j)
+      if (j > lim) v[j] = __float_as_uint(-INFINITY);
   }
-  return fmaxf(m0, m1) * sl2;
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    m0 = fmax3(m0, __uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]));
+    m1 = fmax3(m1, __uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+    m2 = fmax3(m2, __uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+    m3 = fmax3(m3, __uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
 }
 
 // P = exp2(s * sl2 - mu) for the 128 scores at s_addr, written as bf16 pairs into the
@@ -107,21 +108,22 @@ __device__ __forceinline__ float row_max(uint32_t s_addr, int lim, float sl2) {
 template <bool MASK>
 __device__ __forceinline__ float row_exp(uint32_t s_addr, int lim, float sl2, float mu) {
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  // Quarter q reads score columns [32 q, 32 q + 32) and writes P columns [16 q, 16 q + 16),
-  // which only overlap scores already read.  Not unrolled: unrolled, the TMEM loads of all
-  // quarters are hoisted and the row spills.
+  // Half h reads score columns [64 h, 64 h + 64) and writes P columns [32 h, 32 h + 32),
+  // which only overlap scores already read.  Not unrolled: unrolled, the TMEM loads of both
+  // halves are hoisted and the row spills.
 #pragma unroll 1
-  for (int q = 0; q < 4; ++q) {
-    uint32_t v[32];
-    tmem_ld32(s_addr + q * 32, v);
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v[64];
+    tmem_ld32(s_addr + h * 64, v);
+    tmem_ld32(s_addr + h * 64 + 32, v + 32);
     tmem_wait_ld();
     if (MASK) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (q * 32 + j > lim) v[j] = __float_as_uint(-INFINITY);
+      for (int j = 0; j < 64; ++j)
+        if (h * 64 + j > lim) v[j] = __float_as_uint(-INFINITY);
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 32; ++j) {
       float x0, x1;
       ffma2(x0, x1, __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sl2, sl2, -mu, -mu);
       const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -129,7 +131,7 @@ __device__ __forceinline__ float row_exp(uint32_t s_addr, int lim, float sl2, fl
       else fadd2(a0, a1, a0, a1, p0, p1);
       v[j] = pack_bf16(p0, p1);
     }
-    tmem_st16(s_addr + q * 16, v);
+    tmem_st32(s_addr + h * 32, v);
   }
   return (a0 + a1) + (b0 + b1);
 }
@@ -155,8 +157,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::B_QF), 1);
-    mbar_init(bar(C::B_QE), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_QF + b), 1);
+      mbar_init(bar(C::B_QE + b), 1);
+    }
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KVF + s), 1);
       mbar_init(bar(C::B_KVE + s), 1);
@@ -189,15 +193,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int kv_it = 0, item_cnt = 0;
       bool ok = true;
+      Item nxt = decode(p, blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const Item I = decode(p, idx);
-        ok = mbar_wait(bar(C::B_QE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 1);
+        const Item I = nxt;
+        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = decode(p, idx + gridDim.x);
+        const int qb = item_cnt & 1;
+        ok = mbar_wait(bar(C::B_QE + qb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 1);
         if (!ok) break;
-        mbar_expect_tx(bar(C::B_QF), (I.t1 ? 2 : 1) * C::TILE);
+        mbar_expect_tx(bar(C::B_QF + qb), (I.t1 ? 2 : 1) * C::TILE);
         for (int t = 0; t < (I.t1 ? 2 : 1); ++t)
           for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(base + C::Q_OFF + t * C::TILE + pn * C::PANEL, &tq, bar(C::B_QF), pn * 64,
-                        I.h, I.s0 + I.m * kTcBM + t * 128);
+            tma_load_3d(base + C::Q_OFF + (2 * qb + t) * C::TILE + pn * C::PANEL, &tq,
+                        bar(C::B_QF + qb), pn * 64, I.h, I.s0 + I.m * kTcBM + t * 128);
         for (int n = 0; ok && n < I.nb; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
             const int s = kv_it % C::NST;
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) {
         // let every copy this thread started land before the CTA exits
-        drain_wait(bar(C::B_QF), (item_cnt & 1));
+        drain_wait(bar(C::B_QF + (item_cnt & 1)), (item_cnt >> 1) & 1);
         for (int i = kv_it - 1; i >= 0 && i >= kv_it - C::NST; --i)
           drain_wait(bar(C::B_KVF + i % C::NST), (i / C::NST) & 1);
       }
@@ -226,8 +233,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int kv_it = 0, item_cnt = 0;
       uint32_t pf[2] = {0, 0};
       bool ok = true;
+      int qb = 0;
       auto issue_S = [&](int t, int slot) {
-        const uint32_t qa = base + C::Q_OFF + t * C::TILE;
+        const uint32_t qa = base + C::Q_OFF + (2 * qb + t) * C::TILE;
         const uint32_t ka = base + C::KV_OFF + slot * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -245,9 +253,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  sdesc_sw128(va_ + kk * 2048, C::PANEL, 1024), idPV, (acc || kk > 0) ? 1u : 0u);
         mma_commit(bar(C::B_OF + t));
       };
+      Item nxt = decode(p, blockIdx.x);
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const Item I = decode(p, idx);
-        ok = mbar_wait(bar(C::B_QF), item_cnt & 1, abort_flag, p.hdr, 3);
+        const Item I = nxt;
+        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = decode(p, idx + gridDim.x);
+        qb = item_cnt & 1;
+        ok = mbar_wait(bar(C::B_QF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 3);
         if (!ok) break;
         int ks = kv_it % C::NST;
         ok = mbar_wait(bar(C::B_KVF + ks), (kv_it / C::NST) & 1, abort_flag, p.hdr, 4);
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         issue_S(0, ks);
         if (I.t1) issue_S(1, ks);
         mma_commit(bar(C::B_KVE + ks));
-        if (I.nb == 1) mma_commit(bar(C::B_QE));
+        if (I.nb == 1) mma_commit(bar(C::B_QE + qb));
         for (int n = 0; ok && n < I.nb; ++n) {
           const int vs = kv_it % C::NST;
           ok = mbar_wait(bar(C::B_KVF + vs), (kv_it / C::NST) & 1, abort_flag, p.hdr, 5);
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (ks2 >= 0) {
             if (I.t1) issue_S(1, ks2);
             mma_commit(bar(C::B_KVE + ks2));
-            if (n + 1 == I.nb - 1) mma_commit(bar(C::B_QE));
+            if (n + 1 == I.nb - 1) mma_commit(bar(C::B_QE + qb));
           }
         }
       }
@@ -309,8 +320,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t sf = 0, of_base = 0;
     bool ok = true;
+    Item nxt = decode(p, blockIdx.x);
     for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
-      const Item I = decode(p, idx);
+      const Item I = nxt;
+      if (idx + static_cast<int>(gridDim.x) < n_items) nxt = decode(p, idx + gridDim.x);
       if (t == 1 && !I.t1) continue;
       const int nbt = t == 0 ? I.nb0 : I.nb;
       const int qrow = I.m * kTcBM + t * 128 + r;

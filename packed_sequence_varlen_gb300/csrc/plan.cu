@@ -16,19 +16,7 @@
 
 namespace va {
 
-struct PlanArgs {
-  const int32_t* cu;
-  int B;
-  int heads;
-  int BM, BN;
-  int kind;  // 0/2: q-block map, 1: kv-block map
-  int causal;
-  int kmax;  // largest possible key
-  TileItem* out;
-  int capacity;
-  int32_t* status;   // may be null: no status to honour or report
-  int32_t* n_items;  // out
-};
+
 
 // Blocks of one segment (length l) whose key equals k: first block and count.
 __device__ __forceinline__ int seg_key_blocks(const PlanArgs& a, int l, int k, int& first) {
@@ -69,15 +57,15 @@ __device__ __forceinline__ int seg_key_blocks(const PlanArgs& a, int l, int k, i
 constexpr int kPlanThreads = 1024;
 constexpr int kMaxKeys = 4096;
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
-  __shared__ int count[kMaxKeys + 1];
-  __shared__ int offset[kMaxKeys + 2];
-  __shared__ int overflow;
+struct PlanSmem {
+  int count[kMaxKeys + 1];
+  int offset[kMaxKeys + 2];
+  int overflow;
+};
+
+// Builds one map (all 1024 threads of the block take part).
+__device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (a.status && *a.status != VA_OK) {
-    if (threadIdx.x == 0) *a.n_items = 0;
-    return;
-  }
   // pass 1: records per key
   for (int k = a.kmax - warp; k >= 1; k -= 32) {
     int total = 0;
@@ -89,23 +77,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
       total += cnt;
     }
-    if (lane == 0) count[k] = total;
+    if (lane == 0) sh.count[k] = total;
   }
   __syncthreads();
   // exclusive scan over keys, longest first
   if (threadIdx.x == 0) {
     int run = 0;
     for (int k = a.kmax; k >= 1; --k) {
-      offset[k] = run;
-      run += count[k] * a.heads;
+      sh.offset[k] = run;
+      run += sh.count[k] * a.heads;
     }
-    offset[0] = run;
-    overflow = run > a.capacity;
-    *a.n_items = overflow ? 0 : run;
-    if (overflow && a.status) atomicCAS(a.status, VA_OK, VA_ERR_WORKSPACE);
+    sh.offset[0] = run;
+    sh.overflow = run > a.capacity;
+    *a.n_items = sh.overflow ? 0 : run;
+    if (sh.overflow && a.status) atomicCAS(a.status, VA_OK, VA_ERR_WORKSPACE);
   }
   __syncthreads();
-  if (overflow) return;
+  if (sh.overflow) return;
   // pass 2: place records; rank = earlier segments with the same key
   for (int k = a.kmax - warp; k >= 1; k -= 32) {
     int base = 0;
@@ -121,7 +109,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       }
       const int rank = base + incl - cnt;
       for (int j = 0; j < cnt; ++j) {
-        TileItem* dst = a.out + offset[k] + (rank + j) * a.heads;
+        TileItem* dst = a.out + sh.offset[k] + (rank + j) * a.heads;
         for (int h = 0; h < a.heads; ++h) {
           TileItem t;
           t.seg = b;
@@ -134,6 +122,46 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
+  __shared__ PlanSmem sh;
+  if (a.status && *a.status != VA_OK) {
+    if (threadIdx.x == 0) *a.n_items = 0;
+    return;
+  }
+  plan_body(a, sh);
+}
+
+struct PlanPair {
+  PlanArgs map[2];
+  int nmaps;
+  int T, max_seqlen;
+};
+
+// One launch per attention call: checks the cu_seqlens contract (cu[0] == 0,
+// cu[B] == T, strictly increasing, every length <= max_seqlen), writes the status
+// word (OK or VA_ERR_BAD_SEQLENS), and only if it holds builds the call's maps.
+__global__ void __launch_bounds__(kPlanThreads) validate_plan_kernel(PlanPair pp) {
+  __shared__ PlanSmem sh;
+  const PlanArgs& a0 = pp.map[0];
+  int bad = 0;
+  for (int b = threadIdx.x; b < a0.B; b += blockDim.x) {
+    const int x = a0.cu[b], y = a0.cu[b + 1];
+    if (y <= x || y - x > pp.max_seqlen) bad = 1;
+  }
+  if (threadIdx.x == 0 && (a0.cu[0] != 0 || a0.cu[a0.B] != pp.T)) bad = 1;
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (threadIdx.x == 0) {
+      *a0.status = VA_ERR_BAD_SEQLENS;
+      for (int i = 0; i < pp.nmaps; ++i) *pp.map[i].n_items = 0;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) *a0.status = VA_OK;
+  for (int i = 0; i < pp.nmaps; ++i) plan_body(pp.map[i], sh);
 }
 
 cudaError_t launch_plan(const int32_t* cu, int B, int heads, int BM, int BN, int kind, int causal,
@@ -141,6 +169,17 @@ cudaError_t launch_plan(const int32_t* cu, int B, int heads, int BM, int BN, int
                         int32_t* n_items, cudaStream_t st) {
   PlanArgs a{cu, B, heads, BM, BN, kind, causal, kmax, out, capacity, status, n_items};
   plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_plan(const PlanArgs* maps, int nmaps, int T, int max_seqlen,
+                                 cudaStream_t st) {
+  PlanPair pp{};
+  for (int i = 0; i < nmaps && i < 2; ++i) pp.map[i] = maps[i];
+  pp.nmaps = nmaps;
+  pp.T = T;
+  pp.max_seqlen = max_seqlen;
+  validate_plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
   return cudaGetLastError();
 }
 
