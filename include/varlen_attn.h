@@ -144,21 +144,24 @@ size_t varlen_attn_workspace_size(const va_shape* shape, int32_t for_bwd);
 
 /* Builds a tile map on the device.  Source: "Packing与 FlashAttention
  * Varlen", section 5 (a q block exists only while m*BM < l; its key blocks
- * stop at ceil(min(l, (m+1)*BM)/BN) when causal, ceil(l/BN) otherwise); the
- * order -- longest first, ties by (segment, block, head) -- is this library's
- * reading, the page fixes none.
+ * stop at ceil(min(l, (m+1)*BM)/BN) when causal, ceil(l/BN) otherwise).  The
+ * order is this library's reading (the page fixes none): records reading the
+ * same K/V tiles are adjacent and longer work goes first,
+ *     key = (-floor(log2(C_b)), segment b, head, -count, block)
+ * with C_b the segment's total tile count.
  *   kind 0: records {segment, q block, q head, n key blocks}
  *   kind 1: records {segment, kv block, kv head, n q blocks} where the q blocks
  *           of a kv block n start at floor(n*BN/BM) (causal)
  *   kind 2: as kind 0 with the dQ kernel's tile sizes
- *   tile_map_dev    device out, int32 [capacity][4]
+ *   tile_map_dev    device out, int32 [capacity][4], 16-byte aligned
  *   n_items_dev     device out, int32
+ *   scratch_dev     device scratch, int32 [B + 4]
  *   capacity        records available; VA_ERR_WORKSPACE if the bound
- *                   (ceil(T/BM)+B)*heads exceeds it
+ *                   (T/blk + B)*heads exceeds it
  * Asynchronous. */
 va_status varlen_attn_plan(const va_shape* shape, const int32_t* cu_seqlens_dev, int32_t kind,
                            int32_t causal, int32_t* tile_map_dev, int32_t capacity,
-                           int32_t* n_items_dev, va_stream_t stream);
+                           int32_t* n_items_dev, int32_t* scratch_dev, va_stream_t stream);
 
 /* ---------------------------------------------------------------- attention
  * Forward.  Source: "Packing与 FlashAttention Varlen", section 5 (each segment

@@ -10,13 +10,21 @@ m * BM < l, and its key blocks of BN columns run up to
 which equals ceil(min(l, (m + 1) * BM) / BN).  Blocks wholly outside a segment
 or wholly above its causal diagonal are never listed.
 
-Order (the pages do not fix one; reading taken here): longest first, ties by
-segment, then block, then head -- key (-n_blocks, b, m, h).  Heads are last so
-that q heads of one GQA group sit next to each other.
+Order (the pages do not fix one; reading taken here).  Records that read the
+same K/V tiles sit together so that they run at the same time and share those
+tiles through L2, and longer work goes first:
+
+    key = (-class_b, b, h, -n_blocks, m),   class_b = floor(log2(C_b)),
+    C_b = sum over the segment's q blocks of n_blocks
+
+i.e. segments by cost class (a power-of-two bucket of their total tile count,
+largest first; ties by segment index), then the segment's heads in order, then
+its blocks with the most key tiles first.
 
 The backward map lists kv blocks: for kv block n of BN rows the q blocks of BM
 rows run from m_start = floor(n * BN / BM) (causal; 0 otherwise) to
-ceil(l / BM) - 1, ordered by (-n_q, b, n, h_kv).
+ceil(l / BM) - 1; with C_b = sum over kv blocks of n_q its order is
+(-class_b, b, h_kv, -n_q, n).
 """
 from __future__ import annotations
 
@@ -27,33 +35,45 @@ def _ceil(a: int, b: int) -> int:
     return -(-a // b)
 
 
+def _cost_class(c: int) -> int:
+    return c.bit_length() - 1          # floor(log2(c)) for c >= 1
+
+
 def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True):
-    """Items (b, m, h, n_blocks) as an int32 array [N, 4], sorted longest first."""
+    """Items (b, m, h, n_blocks) as an int32 array [N, 4], in the order above."""
     cu = [int(x) for x in cu_seqlens]
     items = []
     for b in range(len(cu) - 1):
         l = cu[b + 1] - cu[b]
+        blocks = []
         for m in range(_ceil(l, BM)):
             nb = _ceil(min(l, (m + 1) * BM), BN) if causal else _ceil(l, BN)
-            for h in range(Hq):
-                items.append((b, m, h, nb))
-    items.sort(key=lambda t: (-t[3], t[0], t[1], t[2]))
-    return np.asarray(items, dtype=np.int32).reshape(-1, 4)
+            blocks.append((m, nb))
+        cls = _cost_class(sum(nb for _, nb in blocks))
+        for h in range(Hq):
+            for m, nb in blocks:
+                items.append(((-cls, b, h, -nb, m), (b, m, h, nb)))
+    items.sort(key=lambda t: t[0])
+    return np.asarray([r for _, r in items], dtype=np.int32).reshape(-1, 4)
 
 
 def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True):
-    """Items (b, n, h_kv, n_q) as an int32 array [N, 4], sorted longest first."""
+    """Items (b, n, h_kv, n_q) as an int32 array [N, 4], in the order above."""
     cu = [int(x) for x in cu_seqlens]
     items = []
     for b in range(len(cu) - 1):
         l = cu[b + 1] - cu[b]
         Mq = _ceil(l, BM)
+        blocks = []
         for n in range(_ceil(l, BN)):
             m_start = (n * BN) // BM if causal else 0
-            for h in range(Hkv):
-                items.append((b, n, h, Mq - m_start))
-    items.sort(key=lambda t: (-t[3], t[0], t[1], t[2]))
-    return np.asarray(items, dtype=np.int32).reshape(-1, 4)
+            blocks.append((n, Mq - m_start))
+        cls = _cost_class(sum(nq for _, nq in blocks))
+        for h in range(Hkv):
+            for n, nq in blocks:
+                items.append(((-cls, b, h, -nq, n), (b, n, h, nq)))
+    items.sort(key=lambda t: t[0])
+    return np.asarray([r for _, r in items], dtype=np.int32).reshape(-1, 4)
 
 
 def fwd_item_edges(cu_seqlens, item, BM: int, BN: int):

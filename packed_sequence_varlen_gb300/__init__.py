@@ -122,7 +122,7 @@ def workspace_size(T, B, Hq, Hkv, d, max_seqlen, for_bwd: bool) -> int:
     lib = _lib.load()
     n = lib.varlen_attn_workspace_size(ctypes.byref(s), int(for_bwd))
     if n == 0:  # the shape check failed: the plan entry point reports why
-        check(lib.varlen_attn_plan(ctypes.byref(s), None, 0, 1, None, 0, None, None))
+        check(lib.varlen_attn_plan(ctypes.byref(s), None, 0, 1, None, 0, None, None, None))
     return n
 
 
@@ -137,8 +137,10 @@ def plan(cu_seqlens: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, max_seqlen
     cap = (T // blk + B) * heads
     tm = torch.empty((max(cap, 1), 4), dtype=torch.int32, device=cu_seqlens.device)
     n = torch.zeros(1, dtype=torch.int32, device=cu_seqlens.device)
+    scratch = torch.empty(B + 4, dtype=torch.int32, device=cu_seqlens.device)
     check(_lib.load().varlen_attn_plan(ctypes.byref(s), _ptr(cu_seqlens), kind, int(causal),
-                                       _ptr(tm), cap, _ptr(n), _stream(cu_seqlens.device)))
+                                       _ptr(tm), cap, _ptr(n), _ptr(scratch),
+                                       _stream(cu_seqlens.device)))
     k = int(n.item())
     return tm[:k], k
 

@@ -60,7 +60,7 @@ def _declare(lib):
         "varlen_attn_tile_sizes": (c_int32, [c_int32, c_int32, i32p, i32p]),
         "varlen_attn_workspace_size": (c_size_t, [POINTER(VaShape), c_int32]),
         "varlen_attn_plan": (c_int32, [POINTER(VaShape), c_void_p, c_int32, c_int32, c_void_p,
-                                       c_int32, c_void_p, c_void_p]),
+                                       c_int32, c_void_p, c_void_p, c_void_p]),
         "varlen_attn_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(VaShape),
                                       c_float, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
                                       c_void_p]),

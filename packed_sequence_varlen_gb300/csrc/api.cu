@@ -15,9 +15,7 @@ cudaError_t launch_metadata_scan(const int32_t*, int, int, int, int32_t*, int32_
 cudaError_t launch_metadata_fill(const int32_t*, int, int, int32_t*, int32_t*, const int32_t*,
                                  cudaStream_t);
 cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaStream_t);
-cudaError_t launch_plan(const int32_t*, int, int, int, int, int, int, int, TileItem*, int, int32_t*,
-                        int32_t*, cudaStream_t);
-int plan_max_keys();
+cudaError_t launch_plan(const PlanArgs&, cudaStream_t);
 cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, cudaStream_t);
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
@@ -101,12 +99,6 @@ int64_t map_capacity(const va_shape& s, int kind) {
   return (static_cast<int64_t>(s.T) / blk + s.B) * heads;
 }
 
-int map_kmax(const va_shape& s, int kind) {
-  int BM, BN;
-  tiles(kind, &BM, &BN);
-  return kind == 1 ? (s.max_seqlen + BM - 1) / BM : (s.max_seqlen + BN - 1) / BN;
-}
-
 va_status check_shape(const va_shape* s) {
   if (!s) return fail(VA_ERR_INVALID_ARG, "shape is null");
   if (s->T < 0 || s->B < 1 || s->Hq < 1 || s->Hkv < 1 || s->max_seqlen < 1)
@@ -120,26 +112,26 @@ va_status check_shape(const va_shape* s) {
     if (x <= 0 || x % 8) return fail(VA_ERR_INVALID_ARG, "strides must be positive multiples of 8");
   for (int64_t x : st)
     if (x < s->d) return fail(VA_ERR_INVALID_ARG, "row and head strides must be >= d");
-  for (int kind = 0; kind < 3; ++kind)
-    if (map_kmax(*s, kind) > plan_max_keys())
-      return fail(VA_ERR_UNSUPPORTED, "max_seqlen too large for the tile scheduler");
+  if (static_cast<int64_t>(s->T) * std::max(s->Hq, s->Hkv) >= (int64_t(1) << 31))
+    return fail(VA_ERR_UNSUPPORTED, "T * heads must stay below 2^31");
   return VA_OK;
 }
 
 struct FwdLayout {
-  size_t map, total;
+  size_t map, segoff, total;
   int64_t cap;
 };
 FwdLayout fwd_layout(const va_shape& s) {
   FwdLayout L;
   L.cap = map_capacity(s, 0);
   L.map = sizeof(WsHeader);
-  L.total = align256(L.map + static_cast<size_t>(L.cap) * sizeof(TileItem));
+  L.segoff = align256(L.map + static_cast<size_t>(L.cap) * sizeof(TileItem));
+  L.total = align256(L.segoff + static_cast<size_t>(s.B) * sizeof(int32_t));
   return L;
 }
 
 struct BwdLayout {
-  size_t dsum, kvmap, qmap, total;
+  size_t dsum, kvmap, qmap, segoff, total;
   int64_t cap_kv, cap_q;
 };
 BwdLayout bwd_layout(const va_shape& s) {
@@ -149,7 +141,8 @@ BwdLayout bwd_layout(const va_shape& s) {
   L.dsum = sizeof(WsHeader);
   L.kvmap = align256(L.dsum + static_cast<size_t>(s.Hq) * s.T * sizeof(float));
   L.qmap = align256(L.kvmap + static_cast<size_t>(L.cap_kv) * sizeof(TileItem));
-  L.total = align256(L.qmap + static_cast<size_t>(L.cap_q) * sizeof(TileItem));
+  L.segoff = align256(L.qmap + static_cast<size_t>(L.cap_q) * sizeof(TileItem));
+  L.total = align256(L.segoff + static_cast<size_t>(s.B) * sizeof(int32_t));
   return L;
 }
 
@@ -229,22 +222,21 @@ size_t varlen_attn_workspace_size(const va_shape* s, int32_t for_bwd) {
 
 va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kind, int32_t causal,
                            int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
-                           va_stream_t stream) {
+                           int32_t* scratch_dev, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
-  if (kind < 0 || kind > 2 || !cu_dev || !map_dev || !n_items_dev || capacity < 0)
+  if (kind < 0 || kind > 2 || !cu_dev || !map_dev || !n_items_dev || !scratch_dev || capacity < 0)
     return fail(VA_ERR_INVALID_ARG, "plan: bad kind or null pointer");
   if (!aligned16(map_dev)) return fail(VA_ERR_INVALID_ARG, "plan: tile map must be 16-byte aligned");
   if (map_capacity(*s, kind) > capacity)
-    return fail(VA_ERR_WORKSPACE, "plan: capacity below the record bound (ceil(T/blk)+B)*heads");
+    return fail(VA_ERR_WORKSPACE, "plan: capacity below the record bound (T/blk + B) * heads");
   int BM, BN;
   tiles(kind, &BM, &BN);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch(K_PLAN, cs, [&] {
-    return launch_plan(cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
-                       map_kmax(*s, kind), reinterpret_cast<TileItem*>(map_dev), capacity, nullptr,
-                       n_items_dev, cs);
-  });
+  const PlanArgs pa{cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
+                    reinterpret_cast<TileItem*>(map_dev), capacity, nullptr, n_items_dev,
+                    scratch_dev + 4, scratch_dev};
+  cudaError_t e = launch(K_PLAN, cs, [&] { return launch_plan(pa, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "plan");
 }
 
@@ -272,8 +264,9 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   }
   int BM, BN;
   tiles(0, &BM, &BN);
-  const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map_kmax(*s, 0), map,
-                    static_cast<int>(L.cap), &hdr->status, &hdr->n_items[0]};
+  const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map, static_cast<int>(L.cap),
+                    &hdr->status, &hdr->n_items[0],
+                    reinterpret_cast<int32_t*>(w + L.segoff), &hdr->counter[0]};
   cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
     return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cs);
   });
@@ -288,6 +281,7 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   p.items = map;
   p.hdr = hdr;
   p.slot = 0;
+  p.counter = &hdr->counter[0];
   p.T = s->T;
   p.Hq = s->Hq;
   p.Hkv = s->Hkv;
@@ -334,11 +328,12 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   int BM, BN, BM2, BN2;
   tiles(1, &BM, &BN);
   tiles(2, &BM2, &BN2);
+  int32_t* segoff = reinterpret_cast<int32_t*>(w + L.segoff);
   const PlanArgs pa[2] = {
-      {cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, map_kmax(*s, 1), kvmap, static_cast<int>(L.cap_kv),
-       &hdr->status, &hdr->n_items[1]},
-      {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, map_kmax(*s, 2), qmap, static_cast<int>(L.cap_q),
-       &hdr->status, &hdr->n_items[2]}};
+      {cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, kvmap, static_cast<int>(L.cap_kv), &hdr->status,
+       &hdr->n_items[1], segoff, &hdr->counter[1]},
+      {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, qmap, static_cast<int>(L.cap_q), &hdr->status,
+       &hdr->n_items[2], segoff, &hdr->counter[2]}};
   cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
     return launch_validate_plan(pa, 2, s->T, s->max_seqlen, cs);
   });
@@ -360,6 +355,8 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   p.hdr = hdr;
   p.kv_slot = 1;
   p.q_slot = 2;
+  p.kv_counter = &hdr->counter[1];
+  p.q_counter = &hdr->counter[2];
   p.T = s->T;
   p.Hq = s->Hq;
   p.Hkv = s->Hkv;

@@ -16,6 +16,7 @@ struct FwdParams {
   const TileItem* items;
   WsHeader* hdr;
   int slot;
+  int32_t* counter;  // work counter (records are pulled in list order)
   int T, Hq, Hkv, g;
   int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs, o_rs, o_hs;
   float scale_log2;  // scale * log2(e)
@@ -38,6 +39,8 @@ struct BwdParams {
   const TileItem* q_items;   // q-block map (dQ pass)
   WsHeader* hdr;
   int kv_slot, q_slot;
+  int32_t* kv_counter;
+  int32_t* q_counter;
   int T, Hq, Hkv, g;
   int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs, o_rs, o_hs;
   float scale;

@@ -19,11 +19,13 @@
 //                     dS -> bf16 in TMEM                   (softmax warps)
 //                     dQ += dS K                           (TS)
 // Layout of both (384 threads, one CTA per SM, persistent over the tile map):
-//   warp 0 TMA producer; warp 1 MMA issuer + TMEM owner; warps 4-7 and 8-11 two
+//   warp 0 TMA producer, which also pulls work items from the map's counter and
+//   publishes them (sched.cuh); warp 1 MMA issuer + TMEM owner; warps 4-7 and 8-11 two
 //   softmax warpgroups that take alternate steps, each with its own TMEM S/dP
 //   buffer, so the tensor core computes step i+1 while step i is exponentiated.
 // TMEM: S_0 | S_1 | dP_0 | dP_1 (64 columns each) | accumulators.
 #include "attn_params.cuh"
+#include "sched.cuh"
 #include "sm100_ptx.cuh"
 #include "tmap.cuh"
 
@@ -64,14 +66,16 @@ struct KvCfg {
   static constexpr int BAR_OFF = LD_OFF + 2 * 2 * 2 * 64 * 4;
   static constexpr int B_KVF = 0, B_KVE = 2, B_QF = 4, B_QE = 4 + QST, B_SF = 4 + 2 * QST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
-                       NBAR = B_DR + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+                       B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;
+  static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
+  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 32;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
   __host__ __device__ static constexpr uint32_t kv_off(int b) { return static_cast<uint32_t>(b) * 2 * TKV; }
 };
 
 struct KvItem {
   int s0, l, n, hk, m_start, steps;
+  int valid;
 };
 
 __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
@@ -107,6 +111,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
 
+  KvItem* queue = reinterpret_cast<KvItem*>(sm + C::QUEUE_OFF);
+  auto dec = [&](int idx) { return kv_decode(p, idx); };
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.kv_slot];
   if (static_cast<int>(blockIdx.x) >= n_items) return;
@@ -127,6 +133,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::B_AF), 1);
     mbar_init(bar(C::B_AE), 256);
     mbar_init(bar(C::B_DR), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_IF + b), 1);
+      mbar_init(bar(C::B_IE + b), 1 + 256);  // MMA thread + both softmax warpgroups
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -150,10 +160,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int qit = 0, item_cnt = 0;
       bool ok = true;
-      KvItem nxt = kv_decode(p, blockIdx.x);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const KvItem I = nxt;
-        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = kv_decode(p, idx + gridDim.x);
+      KvItem nxt;
+      bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
+                                abort_flag, p.hdr, ok);
+      for (; ok && more; ++item_cnt) {
+        const KvItem I = nxt;  // publish the next record first: its decode overlaps this one
+        more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items,
+                             dec, nxt, abort_flag, p.hdr, ok);
+        if (!ok) break;
         const int kb = item_cnt & 1;
         ok = mbar_wait(bar(C::B_KVE + kb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 21);
         if (!ok) break;
@@ -209,10 +223,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(bar(C::B_SF + x));
       };
-      KvItem nxt = kv_decode(p, blockIdx.x);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const KvItem I = nxt;
-        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = kv_decode(p, idx + gridDim.x);
+      for (;; ++item_cnt) {
+        KvItem I;
+        if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
         kb = item_cnt & 1;
         ok = mbar_wait(bar(C::B_KVF + kb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 23);
         if (!ok) break;
@@ -285,10 +298,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         dv = qr < I.l ? p.dsum[at] : 0.f;
       }
     };
-    KvItem nxt = kv_decode(p, blockIdx.x);
-    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-      const KvItem I = nxt;
-      if (idx + static_cast<int>(gridDim.x) < n_items) nxt = kv_decode(p, idx + gridDim.x);
+    for (;; ++item_cnt) {
+      KvItem I;
+      const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (!got) break;
       const int kvrow = I.n * 128 + r;
       int slot = 0;
       if (x < I.steps) {
@@ -404,14 +421,16 @@ struct QCfg {
   static constexpr int BAR_OFF = RING_OFF + KST * 2 * TKV;
   static constexpr int B_QDF = 0, B_QDE = 2, B_KF = 4, B_KE = 4 + KST, B_SF = 4 + 2 * KST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
-                       NBAR = B_DR + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+                       B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;
+  static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
+  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 32;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
   __host__ __device__ static constexpr uint32_t qd_off(int b) { return static_cast<uint32_t>(b) * 2 * TQ; }
 };
 
 struct QItem {
   int s0, l, m, h, hk, nb;
+  int valid;
 };
 
 __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
@@ -446,6 +465,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
 
+  QItem* queue = reinterpret_cast<QItem*>(sm + C::QUEUE_OFF);
+  auto dec = [&](int idx) { return q_decode(p, idx); };
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.q_slot];
   if (static_cast<int>(blockIdx.x) >= n_items) return;
@@ -466,6 +487,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::B_AF), 1);
     mbar_init(bar(C::B_AE), 256);
     mbar_init(bar(C::B_DR), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_IF + b), 1);
+      mbar_init(bar(C::B_IE + b), 1 + 256);  // MMA thread + both softmax warpgroups
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -489,10 +514,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int kit = 0, item_cnt = 0;
       bool ok = true;
-      QItem nxt = q_decode(p, blockIdx.x);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const QItem I = nxt;
-        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = q_decode(p, idx + gridDim.x);
+      QItem nxt;
+      bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
+                                abort_flag, p.hdr, ok);
+      for (; ok && more; ++item_cnt) {
+        const QItem I = nxt;  // publish the next record first: its decode overlaps this one
+        more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items,
+                             dec, nxt, abort_flag, p.hdr, ok);
+        if (!ok) break;
         const int qb = item_cnt & 1;
         ok = mbar_wait(bar(C::B_QDE + qb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 31);
         if (!ok) break;
@@ -547,10 +576,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(bar(C::B_SF + x));
       };
-      QItem nxt = q_decode(p, blockIdx.x);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const QItem I = nxt;
-        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = q_decode(p, idx + gridDim.x);
+      for (;; ++item_cnt) {
+        QItem I;
+        if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
         qb = item_cnt & 1;
         ok = mbar_wait(bar(C::B_QDF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 33);
         if (!ok) break;
@@ -608,10 +636,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t sf = 0;
     int item_cnt = 0;
     bool ok = true;
-    QItem nxt = q_decode(p, blockIdx.x);
-    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-      const QItem I = nxt;
-      if (idx + static_cast<int>(gridDim.x) < n_items) nxt = q_decode(p, idx + gridDim.x);
+    for (;; ++item_cnt) {
+      QItem I;
+      const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (!got) break;
       const int qrow = I.m * 128 + r;
       const int64_t at = static_cast<int64_t>(I.h) * p.T + I.s0 + qrow;
       const float lse2 = qrow < I.l ? p.lse[at] * kLog2e : INFINITY;

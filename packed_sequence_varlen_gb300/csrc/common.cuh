@@ -10,13 +10,15 @@ namespace va {
 
 // Workspace header: the first 256 bytes of every workspace.
 //   int32 status      -- 0 ok, else a va_status written by a kernel
-//   int32 n_items[4]  -- item counts written by the plan kernels
+//   int32 n_items[4]  -- record counts written by the plan kernels
 //   int32 where       -- diagnostic (which wait gave up)
+//   int32 counter[4]  -- work counters the attention kernels pull records from
 struct WsHeader {
   int32_t status;
   int32_t n_items[4];
   int32_t where;
-  int32_t pad[58];
+  int32_t counter[4];
+  int32_t pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -32,11 +34,12 @@ struct PlanArgs {
   int BM, BN;
   int kind;  // 0/2: q-block map, 1: kv-block map
   int causal;
-  int kmax;  // largest possible key
   TileItem* out;
   int capacity;
   int32_t* status;   // may be null: no status to honour or report
   int32_t* n_items;  // out
+  int32_t* seg_off;  // scratch [B]: first record of each segment
+  int32_t* counter;  // work counter the attention kernel pulls items from; zeroed here
 };
 
 __device__ __forceinline__ void set_status(WsHeader* h, int code) {

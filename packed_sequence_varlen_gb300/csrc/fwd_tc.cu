@@ -10,7 +10,8 @@
 // lse = ln sum_j exp(scale q.k_j).
 //
 // CTA layout (384 threads, one CTA per SM, persistent over the tile map):
-//   warp 0      TMA producer: Q tiles once per item, K/V tiles into an NST-slot ring
+//   warp 0      TMA producer: pulls work items from the map's counter and publishes them
+//               (sched.cuh); Q tiles once per item, K/V tiles into an NST-slot ring
 //   warp 1      MMA issuer (one thread): S_t = Q_t K^T (SS), O_t += P_t V (TS, P in TMEM);
 //               also owns the TMEM allocation
 //   warps 4-7   softmax + epilogue for q tile 0 (rows 0..127 of the block; thread = row)
@@ -22,6 +23,7 @@
 // core works on the other tile.  The running max is only raised when it grows by
 // more than 2^8, so O in TMEM is rescaled rarely.
 #include "attn_params.cuh"
+#include "sched.cuh"
 #include "sm100_ptx.cuh"
 #include "tmap.cuh"
 
@@ -46,15 +48,18 @@ struct TcCfg {
   // barriers: q_full[2], q_empty[2], kv_full[NST], kv_empty[NST], s_full[2], p_full[2],
   // o_full[2], drain
   static constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + NST, B_SF = 4 + 2 * NST,
-                       B_PF = B_SF + 2, B_OF = B_PF + 2, B_DR = B_OF + 2, NBAR = B_DR + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+                       B_PF = B_SF + 2, B_OF = B_PF + 2, B_DR = B_OF + 2, B_IF = B_DR + 1,
+                       B_IE = B_IF + 2, NBAR = B_IE + 2;
+  static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;          // two Item slots
+  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 48;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + slack to align the base to 1024
   static constexpr int OCOLS = D;                      // TMEM columns of one O accumulator
 };
 
 struct Item {
   int s0, l, h, hk, m, nb, nb0;
-  bool t1;
+  int t1;
+  int valid;
 };
 
 __device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
@@ -66,7 +71,7 @@ __device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
   r.hk = it.head / p.g;
   r.m = it.blk;
   r.nb = it.count;
-  r.t1 = r.m * kTcBM + 128 < r.l;
+  r.t1 = r.m * kTcBM + 128 < r.l ? 1 : 0;
   r.nb0 = (p.causal && r.t1) ? r.nb - 1 : r.nb;
   return r;
 }
@@ -149,8 +154,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sm = smem_raw + (base - raw);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::MISC_OFF + 4);
+  Item* queue = reinterpret_cast<Item*>(sm + C::QUEUE_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
+  auto dec = [&](int idx) { return decode(p, idx); };
 
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.slot];
@@ -171,6 +178,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(C::B_OF + t), 1);
     }
     mbar_init(bar(C::B_DR), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_IF + b), 1);
+      mbar_init(bar(C::B_IE + b), 1 + 256);  // MMA thread + both softmax warpgroups
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -193,10 +204,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int kv_it = 0, item_cnt = 0;
       bool ok = true;
-      Item nxt = decode(p, blockIdx.x);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const Item I = nxt;
-        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = decode(p, idx + gridDim.x);
+      Item nxt;
+      bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items, dec, nxt,
+                                abort_flag, p.hdr, ok);
+      for (; ok && more; ++item_cnt) {
+        const Item I = nxt;  // publish the next record first: its decode overlaps this one
+        more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items,
+                             dec, nxt, abort_flag, p.hdr, ok);
+        if (!ok) break;
         const int qb = item_cnt & 1;
         ok = mbar_wait(bar(C::B_QE + qb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 1);
         if (!ok) break;
@@ -253,10 +268,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  sdesc_sw128(va_ + kk * 2048, C::PANEL, 1024), idPV, (acc || kk > 0) ? 1u : 0u);
         mma_commit(bar(C::B_OF + t));
       };
-      Item nxt = decode(p, blockIdx.x);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x, ++item_cnt) {
-        const Item I = nxt;
-        if (idx + static_cast<int>(gridDim.x) < n_items) nxt = decode(p, idx + gridDim.x);
+      for (;; ++item_cnt) {
+        Item I;
+        if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
         qb = item_cnt & 1;
         ok = mbar_wait(bar(C::B_QF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 3);
         if (!ok) break;
@@ -320,10 +334,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t sf = 0, of_base = 0;
     bool ok = true;
-    Item nxt = decode(p, blockIdx.x);
-    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
-      const Item I = nxt;
-      if (idx + static_cast<int>(gridDim.x) < n_items) nxt = decode(p, idx + gridDim.x);
+    for (int k = 0;; ++k) {
+      Item I;
+      const bool got = queue_take(k, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (!got) break;
       if (t == 1 && !I.t1) continue;
       const int nbt = t == 0 ? I.nb0 : I.nb;
       const int qrow = I.m * kTcBM + t * 128 + r;

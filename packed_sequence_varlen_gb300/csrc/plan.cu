@@ -1,125 +1,134 @@
 // Segment-aware tile scheduler: builds the work list the attention kernels walk.
 //
-// "Packing与 FlashAttention Varlen", section 5: the launch bound comes from
-// max_seqlen, a q block m of segment b exists only while m*BM < l_b, and its key
-// blocks stop at ceil(min(l_b, (m+1)*BM) / BN) under causality (ceil(l_b/BN)
-// otherwise).  Instead of launching max_seqlen-shaped grids whose CTAs exit
-// early, the list holds only blocks that have work, ordered longest first
-// (ties by segment, block, head -- this library's reading).
+// "Packing与 FlashAttention Varlen", section 5: a q block m of segment b exists only
+// while m*BM < l_b, and its key blocks stop at ceil(min(l_b, (m+1)*BM) / BN) under
+// causality (ceil(l_b/BN) otherwise).  Instead of launching max_seqlen-shaped grids
+// whose CTAs exit early, the list holds only blocks that have work.
 //
-// One CTA of 1024 threads.  A forward segment has at most one q block per key
-// when BM is a multiple of BN (causal), and a backward segment at most one kv
-// block per key when BN is a multiple of BM, so each key's records are "the
-// segments that have this key, in segment order": each warp owns a set of
-// keys and ranks the segments with ballots; no global sort is needed.
+// Order (this library's reading; the page fixes none): records that read the same
+// K/V tiles are adjacent, so the attention kernels -- which pull records in list
+// order from an atomic counter -- run them at the same time and share those tiles
+// through L2; longer work goes first:
+//   key = (-class_b, b, head, -count, block),  class_b = floor(log2(C_b)),
+// with C_b the segment's total tile count (key tiles summed over its q blocks for
+// the forward/dQ maps, q blocks summed over its kv blocks for the dK/dV map).
+//
+// One CTA of 1024 threads: a warp per cost class counts and ranks the segments of
+// its class with warp scans (the segment's first record goes to a small scratch
+// array), then a warp per segment writes the segment's records.
 #include "common.cuh"
 
 namespace va {
 
+namespace {
 
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Blocks of one segment (length l) whose key equals k: first block and count.
-__device__ __forceinline__ int seg_key_blocks(const PlanArgs& a, int l, int k, int& first) {
+// Blocks of a segment of length l and its total tile count.
+__device__ __forceinline__ void seg_cost(const PlanArgs& a, int l, int& nblk, int& cost) {
   if (a.kind != 1) {
-    const int M = (l + a.BM - 1) / a.BM;
-    const int Lk = (l + a.BN - 1) / a.BN;
-    if (!a.causal) {
-      first = 0;
-      return k == Lk ? M : 0;
-    }
-    const int c = a.BM / a.BN;
-    if (k == Lk) {
-      first = M - 1;
-      return 1;
-    }
-    if (k % c == 0 && k / c - 1 < M - 1) {
-      first = k / c - 1;
-      return 1;
-    }
-    return 0;
+    const int M = ceil_div(l, a.BM), Lk = ceil_div(l, a.BN);
+    nblk = M;
+    cost = a.causal ? (a.BM / a.BN) * (M - 1) * M / 2 + Lk : M * Lk;
   } else {
-    const int N = (l + a.BN - 1) / a.BN;
-    const int Mq = (l + a.BM - 1) / a.BM;
-    if (!a.causal) {
-      first = 0;
-      return k == Mq ? N : 0;
-    }
-    const int c = a.BN / a.BM;
-    const int d = Mq - k;
-    if (d < 0 || d % c) return 0;
-    const int n = d / c;
-    if (n >= N) return 0;
-    first = n;
-    return 1;
+    const int N = ceil_div(l, a.BN), Mq = ceil_div(l, a.BM);
+    nblk = N;
+    cost = a.causal ? N * Mq - (a.BN / a.BM) * N * (N - 1) / 2 : N * Mq;
   }
 }
 
+// The j-th record of one (segment, head): most tiles first.
+__device__ __forceinline__ void seg_record(const PlanArgs& a, int l, int nblk, int j, int& blk,
+                                           int& count) {
+  if (a.kind != 1) {
+    const int Lk = ceil_div(l, a.BN);
+    blk = a.causal ? nblk - 1 - j : j;
+    count = a.causal ? min(Lk, (a.BM / a.BN) * (blk + 1)) : Lk;
+  } else {
+    const int Mq = ceil_div(l, a.BM);
+    blk = j;
+    count = a.causal ? Mq - (j * a.BN) / a.BM : Mq;
+  }
+}
+
+__device__ __forceinline__ int cost_class(int c) { return 31 - __clz(max(c, 1)); }
+
+}  // namespace
+
 constexpr int kPlanThreads = 1024;
-constexpr int kMaxKeys = 4096;
 
 struct PlanSmem {
-  int count[kMaxKeys + 1];
-  int offset[kMaxKeys + 2];
+  int count[32];
+  int offset[32];
   int overflow;
 };
 
 // Builds one map (all 1024 threads of the block take part).
 __device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // pass 1: records per key
-  for (int k = a.kmax - warp; k >= 1; k -= 32) {
-    int total = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-      const int b = b0 + lane;
-      int cnt = 0, first;
-      if (b < a.B) cnt = seg_key_blocks(a, a.cu[b + 1] - a.cu[b], k, first);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      total += cnt;
+  const int k = 31 - warp;  // this warp's cost class
+  // records per class
+  int total = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int b = b0 + lane;
+    int cnt = 0;
+    if (b < a.B) {
+      int nblk, cost;
+      seg_cost(a, a.cu[b + 1] - a.cu[b], nblk, cost);
+      if (cost_class(cost) == k) cnt = nblk * a.heads;
     }
-    if (lane == 0) sh.count[k] = total;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    total += cnt;
   }
+  if (lane == 0) sh.count[k] = total;
   __syncthreads();
-  // exclusive scan over keys, longest first
   if (threadIdx.x == 0) {
     int run = 0;
-    for (int k = a.kmax; k >= 1; --k) {
-      sh.offset[k] = run;
-      run += sh.count[k] * a.heads;
+    for (int c = 31; c >= 0; --c) {
+      sh.offset[c] = run;
+      run += sh.count[c];
     }
-    sh.offset[0] = run;
     sh.overflow = run > a.capacity;
     *a.n_items = sh.overflow ? 0 : run;
+    *a.counter = 0;
     if (sh.overflow && a.status) atomicCAS(a.status, VA_OK, VA_ERR_WORKSPACE);
   }
   __syncthreads();
   if (sh.overflow) return;
-  // pass 2: place records; rank = earlier segments with the same key
-  for (int k = a.kmax - warp; k >= 1; k -= 32) {
-    int base = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-      const int b = b0 + lane;
-      int cnt = 0, first = 0;
-      if (b < a.B) cnt = seg_key_blocks(a, a.cu[b + 1] - a.cu[b], k, first);
-      int incl = cnt;
+  // first record of every segment: class offset + earlier segments of the same class
+  int base = sh.offset[k];
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int b = b0 + lane;
+    int cnt = 0;
+    if (b < a.B) {
+      int nblk, cost;
+      seg_cost(a, a.cu[b + 1] - a.cu[b], nblk, cost);
+      if (cost_class(cost) == k) cnt = nblk * a.heads;
+    }
+    int incl = cnt;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int rank = base + incl - cnt;
-      for (int j = 0; j < cnt; ++j) {
-        TileItem* dst = a.out + sh.offset[k] + (rank + j) * a.heads;
-        for (int h = 0; h < a.heads; ++h) {
-          TileItem t;
-          t.seg = b;
-          t.blk = first + j;
-          t.head = h;
-          t.count = k;
-          dst[h] = t;
-        }
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (cnt > 0) a.seg_off[b] = base + incl - cnt;
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncthreads();
+  // records: a warp per segment, heads outer, blocks inner
+  for (int b = warp; b < a.B; b += 32) {
+    const int l = a.cu[b + 1] - a.cu[b];
+    int nblk, cost;
+    seg_cost(a, l, nblk, cost);
+    const int off = a.seg_off[b];
+    for (int r = lane; r < nblk * a.heads; r += 32) {
+      const int h = r / nblk, j = r - h * nblk;
+      TileItem t;
+      seg_record(a, l, nblk, j, t.blk, t.count);
+      t.seg = b;
+      t.head = h;
+      a.out[off + r] = t;
     }
   }
   __syncthreads();
@@ -164,10 +173,7 @@ __global__ void __launch_bounds__(kPlanThreads) validate_plan_kernel(PlanPair pp
   for (int i = 0; i < pp.nmaps; ++i) plan_body(pp.map[i], sh);
 }
 
-cudaError_t launch_plan(const int32_t* cu, int B, int heads, int BM, int BN, int kind, int causal,
-                        int kmax, TileItem* out, int capacity, int32_t* status,
-                        int32_t* n_items, cudaStream_t st) {
-  PlanArgs a{cu, B, heads, BM, BN, kind, causal, kmax, out, capacity, status, n_items};
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
   plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
@@ -182,7 +188,5 @@ cudaError_t launch_validate_plan(const PlanArgs* maps, int nmaps, int T, int max
   validate_plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
   return cudaGetLastError();
 }
-
-int plan_max_keys() { return kMaxKeys; }
 
 }  // namespace va

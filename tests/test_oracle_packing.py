@@ -191,8 +191,17 @@ def test_fwd_tile_map_covers_each_allowed_edge_once(BM, BN, seed):
             last_row = s + min(l, (m + 1) * BM) - 1
             assert (last_row, s + (nb - 1) * BN) in allowed      # last kv tile is needed
         assert sorted(seen) == sorted(allowed)                  # each edge exactly once
-    keys = [(-r[3], r[0], r[1], r[2]) for r in tm]
+    # order: segments by cost class (floor log2 of their total key tiles), then head,
+    # then most key tiles first
+    cost = {}
+    for b, m, h, nb in tm:
+        if h == 0:
+            cost[int(b)] = cost.get(int(b), 0) + int(nb)
+    keys = [(-(cost[int(r[0])].bit_length() - 1), r[0], r[2], -r[3], r[1]) for r in tm]
     assert keys == sorted(keys)
+    # records of one (segment, head) are contiguous
+    groups = [(r[0], r[2]) for r in tm]
+    assert len(set(groups)) == len([g for i, g in enumerate(groups) if i == 0 or g != groups[i - 1]])
 
 
 @pytest.mark.parametrize("BM,BN", [(2, 2), (2, 4), (4, 2), (128, 128), (64, 128)])
@@ -219,3 +228,19 @@ def test_tile_map_noncausal_counts():
     cu = [0, 300, 301]
     tm = ot.fwd_tile_map(cu, 1, 128, 128, causal=False)
     assert tm.tolist() == [[0, 0, 0, 3], [0, 1, 0, 3], [0, 2, 0, 3], [1, 0, 0, 1]]
+
+
+def test_tile_map_order_small_example():
+    """Segments 300 and 1000 at BM=256, BN=128, causal, 2 heads: the long segment (cost
+    2+4+6+8 = 20, class 4) precedes the short one (2+3 = 5, class 2); within a (segment, head)
+    the block with the most key tiles comes first."""
+    tm = ot.fwd_tile_map([0, 300, 1300], 2, 256, 128)
+    assert tm.tolist() == [[1, 3, 0, 8], [1, 2, 0, 6], [1, 1, 0, 4], [1, 0, 0, 2],
+                           [1, 3, 1, 8], [1, 2, 1, 6], [1, 1, 1, 4], [1, 0, 1, 2],
+                           [0, 1, 0, 3], [0, 0, 0, 2], [0, 1, 1, 3], [0, 0, 1, 2]]
+    tb = ot.bwd_tile_map([0, 300, 1300], 1, 64, 128)
+    # segment 1 (l=1000): Mq=16, kv blocks 0..7 with n_q = 16,14,...,2 (sum 72, class 6);
+    # segment 0 (l=300): Mq=5, kv blocks 0..2 with n_q = 5,3,1 (sum 9, class 3)
+    assert tb[:, 0].tolist() == [1] * 8 + [0] * 3
+    assert tb[:8, 3].tolist() == [16, 14, 12, 10, 8, 6, 4, 2]
+    assert tb[8:, 3].tolist() == [5, 3, 1]
