@@ -206,20 +206,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pf[2] = {0, 0};
       bool ok = true;
       int kb = 0;
+      const uint64_t kvdesc0 = sdesc_sw128(base, 16, 1024);               // K-major, from base
+      const uint64_t ringK0 = sdesc_sw128(base + C::RING_OFF, 16, 1024);  // Q/dO as K-major B
+      const uint64_t ringM0 = sdesc_sw128(base + C::RING_OFF, C::PQ, 1024);  // as MN-major B
       auto issue_SdP = [&](int x, int slot) {
-        const uint32_t q = base + C::RING_OFF + slot * 2 * C::TQ, d = q + C::TQ;
-        const uint32_t kt = base + C::kv_off(kb), vt = kt + C::TKV;
+        const uint64_t qd = sdesc_add(ringK0, slot * 2 * C::TQ), dd = sdesc_add(qd, C::TQ);
+        const uint64_t kd = sdesc_add(kvdesc0, C::kv_off(kb)), vd = sdesc_add(kd, C::TKV);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
-          mma_ss(tmem + x * 64, sdesc_sw128(kt + okv, 16, 1024), sdesc_sw128(q + oq, 16, 1024), idS,
-                 kk > 0);
+          mma_ss(tmem + x * 64, sdesc_add(kd, okv), sdesc_add(qd, oq), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
-          mma_ss(tmem + 128 + x * 64, sdesc_sw128(vt + okv, 16, 1024), sdesc_sw128(d + oq, 16, 1024), idS,
-                 kk > 0);
+          mma_ss(tmem + 128 + x * 64, sdesc_add(vd, okv), sdesc_add(dd, oq), idS, kk > 0);
         }
         mma_commit(bar(C::B_SF + x));
       };
@@ -248,15 +249,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
           }
           fence_after_sync();
-          const uint32_t q = base + C::RING_OFF + s * 2 * C::TQ, d = q + C::TQ;
+          const uint64_t qm = sdesc_add(ringM0, s * 2 * C::TQ), dm = sdesc_add(qm, C::TQ);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts(tmem + 256, tmem + x * 64 + kk * 8, sdesc_sw128(d + kk * 2048, C::PQ, 1024), idG,
+            mma_ts(tmem + 256, tmem + x * 64 + kk * 8, sdesc_add(dm, kk * 2048), idG,
                    (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, sdesc_sw128(q + kk * 2048, C::PQ, 1024),
-                   idG, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, sdesc_add(qm, kk * 2048), idG,
+                   (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(C::B_QE + s));
           if (i + 2 < I.steps) {
             const int s2 = (qit + i + 2) % C::QST;
@@ -559,20 +560,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pf[2] = {0, 0};
       bool ok = true;
       int qb = 0;
+      const uint64_t qdesc0 = sdesc_sw128(base, 16, 1024);                  // Q/dO, K-major A
+      const uint64_t ringK0 = sdesc_sw128(base + C::RING_OFF, 16, 1024);     // K/V as K-major B
+      const uint64_t ringM0 = sdesc_sw128(base + C::RING_OFF, C::PKV, 1024); // K as MN-major B
       auto issue_SdP = [&](int x, int slot) {
-        const uint32_t kt = base + C::RING_OFF + slot * 2 * C::TKV, vt = kt + C::TKV;
-        const uint32_t qt = base + C::qd_off(qb), dt = qt + C::TQ;
+        const uint64_t kd = sdesc_add(ringK0, slot * 2 * C::TKV), vd = sdesc_add(kd, C::TKV);
+        const uint64_t qd = sdesc_add(qdesc0, C::qd_off(qb)), dd = sdesc_add(qd, C::TQ);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
-          mma_ss(tmem + x * 64, sdesc_sw128(qt + oq, 16, 1024), sdesc_sw128(kt + ok_, 16, 1024), idS,
-                 kk > 0);
+          mma_ss(tmem + x * 64, sdesc_add(qd, oq), sdesc_add(kd, ok_), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
-          mma_ss(tmem + 128 + x * 64, sdesc_sw128(dt + oq, 16, 1024), sdesc_sw128(vt + ok_, 16, 1024), idS,
-                 kk > 0);
+          mma_ss(tmem + 128 + x * 64, sdesc_add(dd, oq), sdesc_add(vd, ok_), idS, kk > 0);
         }
         mma_commit(bar(C::B_SF + x));
       };
@@ -601,10 +603,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
           }
           fence_after_sync();
-          const uint32_t kt = base + C::RING_OFF + s * 2 * C::TKV;
+          const uint64_t km = sdesc_add(ringM0, s * 2 * C::TKV);
 #pragma unroll
           for (int kk = 0; kk < C::KB / 16; ++kk)
-            mma_ts(tmem + 256, tmem + 128 + x * 64 + kk * 8, sdesc_sw128(kt + kk * 2048, C::PKV, 1024), idG,
+            mma_ts(tmem + 256, tmem + 128 + x * 64 + kk * 8, sdesc_add(km, kk * 2048), idG,
                    (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(C::B_KE + s));
           if (n + 2 < I.nb) {

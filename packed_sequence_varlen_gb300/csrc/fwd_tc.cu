@@ -39,14 +39,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct TcCfg {
-  static constexpr int NST = D == 128 ? 3 : 8;         // K/V ring slots
+  static constexpr int NST = D == 128 ? 5 : 12;        // K/V ring slots
   static constexpr int TILE = 128 * D * 2;             // bytes of one 128-row Q, K or V tile
   static constexpr int PANEL = 128 * 128;              // one 64-column (128-byte) panel of a tile
-  static constexpr int Q_OFF = 0;                      // two Q buffers (items alternate), 2 tiles each
-  static constexpr int KV_OFF = 4 * TILE;
+  static constexpr int Q_OFF = 0;                      // Q tiles 0 and 1
+  static constexpr int KV_OFF = 2 * TILE;
   static constexpr int BAR_OFF = KV_OFF + NST * TILE;
-  // barriers: q_full[2], q_empty[2], kv_full[NST], kv_empty[NST], s_full[2], p_full[2],
-  // o_full[2], drain
+  // barriers: q_full[tile], q_empty[tile], kv_full[NST], kv_empty[NST], s_full[2], p_full[2],
+  // o_full[2], drain, item queue full[2] / empty[2]
   static constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + NST, B_SF = 4 + 2 * NST,
                        B_PF = B_SF + 2, B_OF = B_PF + 2, B_DR = B_OF + 2, B_IF = B_DR + 1,
                        B_IE = B_IF + 2, NBAR = B_IE + 2;
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int kv_it = 0, item_cnt = 0;
+      int kv_it = 0, item_cnt = 0, qcnt[2] = {0, 0};
       bool ok = true;
       Item nxt;
       bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items, dec, nxt,
@@ -212,14 +212,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items,
                              dec, nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
-        const int qb = item_cnt & 1;
-        ok = mbar_wait(bar(C::B_QE + qb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 1);
-        if (!ok) break;
-        mbar_expect_tx(bar(C::B_QF + qb), (I.t1 ? 2 : 1) * C::TILE);
-        for (int t = 0; t < (I.t1 ? 2 : 1); ++t)
+        // Q tile t is released by the item's last S_t MMA (tile 0 one key tile before tile 1)
+        for (int t = 0; ok && t < (I.t1 ? 2 : 1); ++t) {
+          ok = mbar_wait(bar(C::B_QE + t), (qcnt[t] & 1) ^ 1, abort_flag, p.hdr, 1);
+          if (!ok) break;
+          mbar_expect_tx(bar(C::B_QF + t), C::TILE);
           for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(base + C::Q_OFF + (2 * qb + t) * C::TILE + pn * C::PANEL, &tq,
-                        bar(C::B_QF + qb), pn * 64, I.h, I.s0 + I.m * kTcBM + t * 128);
+            tma_load_3d(base + C::Q_OFF + t * C::TILE + pn * C::PANEL, &tq, bar(C::B_QF + t), pn * 64,
+                        I.h, I.s0 + I.m * kTcBM + t * 128);
+          ++qcnt[t];
+        }
+        if (!ok) break;
         for (int n = 0; ok && n < I.nb; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
             const int s = kv_it % C::NST;
@@ -235,7 +238,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) {
         // let every copy this thread started land before the CTA exits
-        drain_wait(bar(C::B_QF + (item_cnt & 1)), (item_cnt >> 1) & 1);
+        for (int t = 0; t < 2; ++t)
+          if (qcnt[t] > 0) drain_wait(bar(C::B_QF + t), (qcnt[t] - 1) & 1);
         for (int i = kv_it - 1; i >= 0 && i >= kv_it - C::NST; --i)
           drain_wait(bar(C::B_KVF + i % C::NST), (i / C::NST) & 1);
       }
@@ -248,41 +252,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int kv_it = 0, item_cnt = 0;
       uint32_t pf[2] = {0, 0};
       bool ok = true;
-      int qb = 0;
+      uint32_t qcnt[2] = {0, 0};
+      const uint64_t qdesc[2] = {sdesc_sw128(base + C::Q_OFF, 16, 1024),
+                                 sdesc_sw128(base + C::Q_OFF + C::TILE, 16, 1024)};
+      const uint64_t kdesc0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(base + C::KV_OFF, C::PANEL, 1024);
       auto issue_S = [&](int t, int slot) {
-        const uint32_t qa = base + C::Q_OFF + (2 * qb + t) * C::TILE;
-        const uint32_t ka = base + C::KV_OFF + slot * C::TILE;
+        const uint64_t qd = qdesc[t], kd = sdesc_add(kdesc0, slot * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 idS, kk > 0);
+          mma_ss(tmem + t * 128, sdesc_add(qd, off), sdesc_add(kd, off), idS, kk > 0);
         }
         mma_commit(bar(C::B_SF + t));
       };
       auto issue_PV = [&](int t, int slot, bool acc) {
-        const uint32_t va_ = base + C::KV_OFF + slot * C::TILE;
+        const uint64_t vd = sdesc_add(vdesc0, slot * C::TILE);
+        const uint32_t d_tm = tmem + 256 + t * C::OCOLS, p_tm = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kTcBN / 16; ++kk)
-          mma_ts(tmem + 256 + t * C::OCOLS, tmem + t * 128 + kk * 8,
-                 sdesc_sw128(va_ + kk * 2048, C::PANEL, 1024), idPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d_tm, p_tm + kk * 8, sdesc_add(vd, kk * 2048), idPV, (acc || kk > 0) ? 1u : 0u);
         mma_commit(bar(C::B_OF + t));
       };
       for (;; ++item_cnt) {
         Item I;
         if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
-        qb = item_cnt & 1;
-        ok = mbar_wait(bar(C::B_QF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 3);
+        ok = mbar_wait(bar(C::B_QF + 0), qcnt[0] & 1, abort_flag, p.hdr, 3);
         if (!ok) break;
+        if (I.t1) {
+          ok = mbar_wait(bar(C::B_QF + 1), qcnt[1] & 1, abort_flag, p.hdr, 3);
+          if (!ok) break;
+        }
         int ks = kv_it % C::NST;
         ok = mbar_wait(bar(C::B_KVF + ks), (kv_it / C::NST) & 1, abort_flag, p.hdr, 4);
         if (!ok) break;
         fence_after_sync();
         ++kv_it;
         issue_S(0, ks);
-        if (I.t1) issue_S(1, ks);
+        if (I.nb0 == 1) {
+          mma_commit(bar(C::B_QE + 0));  // last S_0 of the item: Q tile 0 may be reloaded
+          ++qcnt[0];
+        }
+        if (I.t1) {
+          issue_S(1, ks);
+          if (I.nb == 1) {
+            mma_commit(bar(C::B_QE + 1));
+            ++qcnt[1];
+          }
+        }
         mma_commit(bar(C::B_KVE + ks));
-        if (I.nb == 1) mma_commit(bar(C::B_QE + qb));
         for (int n = 0; ok && n < I.nb; ++n) {
           const int vs = kv_it % C::NST;
           ok = mbar_wait(bar(C::B_KVF + vs), (kv_it / C::NST) & 1, abort_flag, p.hdr, 5);
@@ -302,7 +320,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) break;
             ++kv_it;
             fence_after_sync();
-            if (n + 1 < I.nb0) issue_S(0, ks2);
+            if (n + 1 < I.nb0) {
+              issue_S(0, ks2);
+              if (n + 1 == I.nb0 - 1) {
+                mma_commit(bar(C::B_QE + 0));
+                ++qcnt[0];
+              }
+            }
           }
           if (I.t1) {
             ok = mbar_wait(bar(C::B_PF + 1), pf[1] & 1, abort_flag, p.hdr, 8);
@@ -313,9 +337,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           mma_commit(bar(C::B_KVE + vs));
           if (ks2 >= 0) {
-            if (I.t1) issue_S(1, ks2);
+            if (I.t1) {
+              issue_S(1, ks2);
+              if (n + 1 == I.nb - 1) {
+                mma_commit(bar(C::B_QE + 1));
+                ++qcnt[1];
+              }
+            }
             mma_commit(bar(C::B_KVE + ks2));
-            if (n + 1 == I.nb - 1) mma_commit(bar(C::B_QE + qb));
           }
         }
       }
@@ -325,6 +354,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
+    // warps 4-7 own q tile 0, warps 8-11 q tile 1; a warp reaches TMEM lanes 32*(warp % 4)
     const int t = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -409,19 +439,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float inv = 1.f / lsum;
       const bool store = qrow < I.l;
       bf16* orow = p.o + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
+      {
+        uint32_t o[D];  // the whole row in one TMEM round trip
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + c * 32, o);
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(o_addr + c * 32, o + c * 32);
         tmem_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+        for (int j = 0; j < D / 2; ++j)
+          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < D / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
       }
       if (store)
