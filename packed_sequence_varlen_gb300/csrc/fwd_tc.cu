@@ -35,6 +35,11 @@ namespace {
 constexpr int kTcBM = 256;  // q rows per work item (two 128-row tiles)
 constexpr int kTcBN = 128;  // key rows per K/V tile
 constexpr int kTcThreads = 384;
+// setmaxnreg moves registers within what the CTA was launched with (168 per thread for
+// 384 threads); a split above that total would make the increase wait forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtl = 80, kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kTcThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -84,14 +89,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Row max (x scale*log2e) of the 128 scores at s_addr; columns j > lim are ignored when MASK.
-// One TMEM round trip: all four 32-column loads, then one wait.
-template <bool MASK>
-__device__ __forceinline__ float row_max(uint32_t s_addr, int lim, float sl2) {
-  uint32_t v[128];
+// The 128 scores of this thread's row: one TMEM round trip.
+__device__ __forceinline__ void row_load(uint32_t s_addr, uint32_t* v) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
   tmem_wait_ld();
+}
+
+// Masks columns j > lim (when MASK) and returns the row max x sl2.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t* v, int lim, float sl2) {
   if (MASK) {
 #pragma unroll
     for (int j = 0; j < 128; ++j)
@@ -108,35 +115,17 @@ __device__ __forceinline__ float row_max(uint32_t s_addr, int lim, float sl2) {
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
 }
 
-// P = exp2(s * sl2 - mu) for the 128 scores at s_addr, written as bf16 pairs into the
-// first 64 columns.  Returns the row sum of P.
-template <bool MASK>
-__device__ __forceinline__ float row_exp(uint32_t s_addr, int lim, float sl2, float mu) {
+// p = exp2(s * sl2 - mu) packed in place as bf16 pairs into v[0..63]; returns the row sum.
+__device__ __forceinline__ float row_exp(uint32_t* v, float sl2, float mu) {
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  // Half h reads score columns [64 h, 64 h + 64) and writes P columns [32 h, 32 h + 32),
-  // which only overlap scores already read.  Not unrolled: unrolled, the TMEM loads of both
-  // halves are hoisted and the row spills.
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
-    uint32_t v[64];
-    tmem_ld32(s_addr + h * 64, v);
-    tmem_ld32(s_addr + h * 64 + 32, v + 32);
-    tmem_wait_ld();
-    if (MASK) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (h * 64 + j > lim) v[j] = __float_as_uint(-INFINITY);
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float x0, x1;
-      ffma2(x0, x1, __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sl2, sl2, -mu, -mu);
-      const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-      if (j & 1) fadd2(b0, b1, b0, b1, p0, p1);
-      else fadd2(a0, a1, a0, a1, p0, p1);
-      v[j] = pack_bf16(p0, p1);
-    }
-    tmem_st32(s_addr + h * 32, v);
+  for (int j = 0; j < 64; ++j) {
+    float x0, x1;
+    ffma2(x0, x1, __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sl2, sl2, -mu, -mu);
+    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+    if (j & 1) fadd2(b0, b1, b0, b1, p0, p1);
+    else fadd2(a0, a1, a0, a1, p0, p1);
+    v[j] = pack_bf16(p0, p1);
   }
   return (a0 + a1) + (b0 + b1);
 }
@@ -199,8 +188,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Registers: what the producer/MMA warpgroup (warps 0-3) gives back goes to the two
+  // softmax warpgroups, which hold a whole 128-score row.  Every warp sets its budget at
+  // the top of its role.
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    regs_dec<kRegsCtl>();
     if (lane == 0) {
       int kv_it = 0, item_cnt = 0, qcnt[2] = {0, 0};
       bool ok = true;
@@ -246,6 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_dec<kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kTcBN, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
@@ -253,25 +247,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t pf[2] = {0, 0};
       bool ok = true;
       uint32_t qcnt[2] = {0, 0};
-      const uint64_t qdesc[2] = {sdesc_sw128(base + C::Q_OFF, 16, 1024),
-                                 sdesc_sw128(base + C::Q_OFF + C::TILE, 16, 1024)};
-      const uint64_t kdesc0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
-      const uint64_t vdesc0 = sdesc_sw128(base + C::KV_OFF, C::PANEL, 1024);
+      const uint32_t qlo[2] = {sdesc_lo(base + C::Q_OFF, 16), sdesc_lo(base + C::Q_OFF + C::TILE, 16)};
+      const uint32_t klo0 = sdesc_lo(base + C::KV_OFF, 16);
+      const uint32_t vlo0 = sdesc_lo(base + C::KV_OFF, C::PANEL);
       auto issue_S = [&](int t, int slot) {
-        const uint64_t qd = qdesc[t], kd = sdesc_add(kdesc0, slot * C::TILE);
+        const uint32_t qd = qlo[t], kd = klo0 + ((slot * C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, sdesc_add(qd, off), sdesc_add(kd, off), idS, kk > 0);
+          const uint32_t off = ((kk >> 2) * C::PANEL + (kk & 3) * 32) >> 4;
+          mma_ss_lo(tmem + t * 128, qd + off, kd + off, idS, kk > 0);
         }
         mma_commit(bar(C::B_SF + t));
       };
       auto issue_PV = [&](int t, int slot, bool acc) {
-        const uint64_t vd = sdesc_add(vdesc0, slot * C::TILE);
+        const uint32_t vd = vlo0 + ((slot * C::TILE) >> 4);
         const uint32_t d_tm = tmem + 256 + t * C::OCOLS, p_tm = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kTcBN / 16; ++kk)
-          mma_ts(d_tm, p_tm + kk * 8, sdesc_add(vd, kk * 2048), idPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_lo(d_tm, p_tm + kk * 8, vd + kk * (2048 >> 4), idPV, (acc || kk > 0) ? 1u : 0u);
         mma_commit(bar(C::B_OF + t));
       };
       for (;; ++item_cnt) {
@@ -352,9 +345,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mma_commit(bar(C::B_DR));
       drain_wait(bar(C::B_DR), 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kRegsCtl>();  // warps 2 and 3 have no role
+  } else {
     // ------------------------------------------------------------ softmax + epilogue
     // warps 4-7 own q tile 0, warps 8-11 q tile 1; a warp reaches TMEM lanes 32*(warp % 4)
+    regs_inc<kRegsSoftmax>();
     const int t = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -388,13 +384,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // tile); non-causal masks only key columns past the segment end.
         const bool need_mask = p.causal ? (n == nbt - 1) : (n * kTcBN + kTcBN > I.l);
         const int lim = p.causal ? qrow - n * kTcBN : I.l - 1 - n * kTcBN;  // mask j > lim
-        // Row max first (the exponent pass overwrites scores with P, so it runs once, last).
-        const float mt = need_mask ? row_max<true>(s_addr, lim, sl2) : row_max<false>(s_addr, lim, sl2);
+        // One TMEM round trip per tile: the row into registers, its max, then
+        // p = exp2(s * sl2 - m_ref) packed in place and stored over the first half of S_t.
+        // The reference max m_ref is raised only when the row max grew by more than 2^8
+        // (rare); O_t, which holds PV_{n-1}, is then rescaled in TMEM first.
+        uint32_t v[128];
+        row_load(s_addr, v);
+        const float mt = need_mask ? row_max<true>(v, lim, sl2) : row_max<false>(v, lim, sl2);
         if (n == 0) {
           m_ref = mt;
         } else {
-          // the reference max is raised only when the row max grew by more than 2^8 (rare);
-          // then O_t, which holds PV_{n-1}, is rescaled in TMEM
           const bool resc = mt > m_ref + kRescaleThreshold;
           if (__any_sync(0xffffffffu, resc)) {
             const float alpha = resc ? fast_exp2(m_ref - mt) : 1.f;
@@ -420,8 +419,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tmem_wait_st();
           }
         }
-        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        const float rs = need_mask ? row_exp<true>(s_addr, lim, sl2, mu) : row_exp<false>(s_addr, lim, sl2, mu);
+        const float rs = row_exp(v, sl2, m_ref == -INFINITY ? 0.f : m_ref);
+        tmem_st32(s_addr, v);  // P over the first 64 columns of S_t
+        tmem_st32(s_addr + 32, v + 32);
         lsum += rs;
         tmem_wait_st();
         fence_before_sync();
@@ -478,6 +478,11 @@ static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  // the in-kernel register split assumes the full launch budget; refuse rather than wait
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
