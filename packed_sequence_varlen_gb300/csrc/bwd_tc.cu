@@ -35,6 +35,11 @@ using namespace sm100;
 namespace {
 
 constexpr int kBwdThreads = 384;
+// setmaxnreg moves registers within what the CTA was launched with (168 per thread for
+// 384 threads); a split above that total would make the increase wait forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtl = 80, kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kBwdThreads * kLaunchRegs, "register split exceeds the launch");
 
 __device__ __forceinline__ void named_sync(int id) {
   asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
@@ -157,6 +162,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    regs_dec<kRegsCtl>();
     if (lane == 0) {
       int qit = 0, item_cnt = 0;
       bool ok = true;
@@ -199,28 +205,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_dec<kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idG = idesc_bf16(128, D, false, true);
       int qit = 0, item_cnt = 0;
-      uint32_t pf[2] = {0, 0};
+      uint32_t pf0 = 0, pf1 = 0;  // p_full phases per buffer (scalars: a runtime index would spill)
       bool ok = true;
       int kb = 0;
-      const uint64_t kvdesc0 = sdesc_sw128(base, 16, 1024);               // K-major, from base
-      const uint64_t ringK0 = sdesc_sw128(base + C::RING_OFF, 16, 1024);  // Q/dO as K-major B
-      const uint64_t ringM0 = sdesc_sw128(base + C::RING_OFF, C::PQ, 1024);  // as MN-major B
+      const uint32_t kvlo0 = sdesc_lo(base, 16);                 // K/V, K-major A
+      const uint32_t ringK0 = sdesc_lo(base + C::RING_OFF, 16);    // Q/dO as K-major B
+      const uint32_t ringM0 = sdesc_lo(base + C::RING_OFF, C::PQ); // Q/dO as MN-major B
       auto issue_SdP = [&](int x, int slot) {
-        const uint64_t qd = sdesc_add(ringK0, slot * 2 * C::TQ), dd = sdesc_add(qd, C::TQ);
-        const uint64_t kd = sdesc_add(kvdesc0, C::kv_off(kb)), vd = sdesc_add(kd, C::TKV);
+        const uint32_t qd = ringK0 + ((slot * 2 * C::TQ) >> 4), dd = qd + (C::TQ >> 4);
+        const uint32_t kd = kvlo0 + (C::kv_off(kb) >> 4), vd = kd + (C::TKV >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
-          mma_ss(tmem + x * 64, sdesc_add(kd, okv), sdesc_add(qd, oq), idS, kk > 0);
+          const uint32_t okv = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4, oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4;
+          mma_ss_lo(tmem + x * 64, kd + okv, qd + oq, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t okv = (kk >> 2) * C::PKV + (kk & 3) * 32, oq = (kk >> 2) * C::PQ + (kk & 3) * 32;
-          mma_ss(tmem + 128 + x * 64, sdesc_add(vd, okv), sdesc_add(dd, oq), idS, kk > 0);
+          const uint32_t okv = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4, oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4;
+          mma_ss_lo(tmem + 128 + x * 64, vd + okv, dd + oq, idS, kk > 0);
         }
         mma_commit(bar(C::B_SF + x));
       };
@@ -241,23 +248,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (I.steps <= 2) mma_commit(bar(C::B_KVE + kb));
         for (int i = 0; ok && i < I.steps; ++i) {
           const int x = i & 1, s = (qit + i) % C::QST;
-          ok = mbar_wait(bar(C::B_PF + x), pf[x] & 1, abort_flag, p.hdr, 25);
+          ok = mbar_wait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 25);
           if (!ok) break;
-          ++pf[x];
+          if (x) ++pf1;
+          else ++pf0;
           if (i == 0) {  // the accumulators must have been read out by the previous epilogue
             ok = mbar_wait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 26);
             if (!ok) break;
           }
           fence_after_sync();
-          const uint64_t qm = sdesc_add(ringM0, s * 2 * C::TQ), dm = sdesc_add(qm, C::TQ);
+          const uint32_t qm = ringM0 + ((s * 2 * C::TQ) >> 4), dm = qm + (C::TQ >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts(tmem + 256, tmem + x * 64 + kk * 8, sdesc_add(dm, kk * 2048), idG,
-                   (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_lo(tmem + 256, tmem + x * 64 + kk * 8, dm + kk * (2048 >> 4), idG, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, sdesc_add(qm, kk * 2048), idG,
-                   (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_lo(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, qm + kk * (2048 >> 4), idG,
+                      (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(C::B_QE + s));
           if (i + 2 < I.steps) {
             const int s2 = (qit + i + 2) % C::QST;
@@ -275,8 +282,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(bar(C::B_DR));
       drain_wait_b(bar(C::B_DR), 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kRegsCtl>();  // warps 2 and 3 have no role
+  } else {
     // ------------------------------------------------------------ softmax + epilogue
+    regs_inc<kRegsSoftmax>();
     const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: 0 -> dV, 1 -> dK
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -334,31 +344,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool need_mask = p.causal && (I.n * 128 + 127 > q0);
         const float* L = ldbuf + slot * 128;
         const float* Dd = L + 64;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sv[32], dpv[32];
-          tmem_ld32(s_addr + hh * 32, sv);
-          tmem_ld32(dp_addr + hh * 32, dpv);
-          tmem_wait_ld();
+        // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(s_addr, sv);
+        tmem_ld32(s_addr + 32, sv + 32);
+        tmem_ld32(dp_addr, dpv);
+        tmem_ld32(dp_addr + 32, dpv + 32);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 l2 = *reinterpret_cast<const float2*>(L + hh * 32 + c);
-            const float2 d2 = *reinterpret_cast<const float2*>(Dd + hh * 32 + c);
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(L + c);
+          const float4 d4 = *reinterpret_cast<const float4*>(Dd + c);
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int j = c + e;
+            const float la = e ? l4.z : l4.x, lb = e ? l4.w : l4.y;
+            const float da = e ? d4.z : d4.x, db = e ? d4.w : d4.y;
             float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -l2.x, -l2.y);
+            ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), sl2, sl2, -la, -lb);
             float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             if (need_mask) {
-              if (hh * 32 + c < lim) p0 = 0.f;
-              if (hh * 32 + c + 1 < lim) p1 = 0.f;
+              if (j < lim) p0 = 0.f;
+              if (j + 1 < lim) p1 = 0.f;
             }
             float t0, t1;
-            fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -d2.x, -d2.y);
-            sv[c >> 1] = pack_bf16(p0, p1);
-            dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
+            fadd2(t0, t1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -da, -db);
+            sv[j >> 1] = pack_bf16(p0, p1);
+            dpv[j >> 1] = pack_bf16(p0 * t0, p1 * t1);
           }
-          tmem_st16(s_addr + hh * 16, sv);
-          tmem_st16(dp_addr + hh * 16, dpv);
         }
+        tmem_st32(s_addr, sv);
+        tmem_st32(dp_addr, dpv);
         tmem_wait_st();
         fence_before_sync();
         mbar_arrive(bar(C::B_PF + x));
@@ -381,18 +397,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool store = kvrow < I.l;
       bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>(I.s0 + kvrow) * p.k_rs +
                   static_cast<int64_t>(I.hk) * p.k_hs;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(acc_addr + c * 32, o);
-        uint32_t pk[16];
+      {
+        uint32_t o[D];  // the whole accumulator row in one TMEM round trip
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(acc_addr + c * 32, o + c * 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < D / 2; ++j)
+          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < D / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
       }
       fence_before_sync();
@@ -512,6 +528,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    regs_dec<kRegsCtl>();
     if (lane == 0) {
       int kit = 0, item_cnt = 0;
       bool ok = true;
@@ -553,28 +570,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_dec<kRegsCtl>();
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idG = idesc_bf16(128, D, false, true);
       int kit = 0, item_cnt = 0;
-      uint32_t pf[2] = {0, 0};
+      uint32_t pf0 = 0, pf1 = 0;  // p_full phases per buffer (scalars: a runtime index would spill)
       bool ok = true;
       int qb = 0;
-      const uint64_t qdesc0 = sdesc_sw128(base, 16, 1024);                  // Q/dO, K-major A
-      const uint64_t ringK0 = sdesc_sw128(base + C::RING_OFF, 16, 1024);     // K/V as K-major B
-      const uint64_t ringM0 = sdesc_sw128(base + C::RING_OFF, C::PKV, 1024); // K as MN-major B
+      const uint32_t qlo0 = sdesc_lo(base, 16);                    // Q/dO, K-major A
+      const uint32_t ringK0 = sdesc_lo(base + C::RING_OFF, 16);      // K/V as K-major B
+      const uint32_t ringM0 = sdesc_lo(base + C::RING_OFF, C::PKV);  // K as MN-major B
       auto issue_SdP = [&](int x, int slot) {
-        const uint64_t kd = sdesc_add(ringK0, slot * 2 * C::TKV), vd = sdesc_add(kd, C::TKV);
-        const uint64_t qd = sdesc_add(qdesc0, C::qd_off(qb)), dd = sdesc_add(qd, C::TQ);
+        const uint32_t kd = ringK0 + ((slot * 2 * C::TKV) >> 4), vd = kd + (C::TKV >> 4);
+        const uint32_t qd = qlo0 + (C::qd_off(qb) >> 4), dd = qd + (C::TQ >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
-          mma_ss(tmem + x * 64, sdesc_add(qd, oq), sdesc_add(kd, ok_), idS, kk > 0);
+          const uint32_t oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4, ok_ = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4;
+          mma_ss_lo(tmem + x * 64, qd + oq, kd + ok_, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oq = (kk >> 2) * C::PQ + (kk & 3) * 32, ok_ = (kk >> 2) * C::PKV + (kk & 3) * 32;
-          mma_ss(tmem + 128 + x * 64, sdesc_add(dd, oq), sdesc_add(vd, ok_), idS, kk > 0);
+          const uint32_t oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4, ok_ = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4;
+          mma_ss_lo(tmem + 128 + x * 64, dd + oq, vd + ok_, idS, kk > 0);
         }
         mma_commit(bar(C::B_SF + x));
       };
@@ -595,19 +613,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (I.nb <= 2) mma_commit(bar(C::B_QDE + qb));
         for (int n = 0; ok && n < I.nb; ++n) {
           const int x = n & 1, s = (kit + n) % C::KST;
-          ok = mbar_wait(bar(C::B_PF + x), pf[x] & 1, abort_flag, p.hdr, 35);
+          ok = mbar_wait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 35);
           if (!ok) break;
-          ++pf[x];
+          if (x) ++pf1;
+          else ++pf0;
           if (n == 0) {
             ok = mbar_wait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 36);
             if (!ok) break;
           }
           fence_after_sync();
-          const uint64_t km = sdesc_add(ringM0, s * 2 * C::TKV);
+          const uint32_t km = ringM0 + ((s * 2 * C::TKV) >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::KB / 16; ++kk)
-            mma_ts(tmem + 256, tmem + 128 + x * 64 + kk * 8, sdesc_add(km, kk * 2048), idG,
-                   (n > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_lo(tmem + 256, tmem + 128 + x * 64 + kk * 8, km + kk * (2048 >> 4), idG,
+                      (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(C::B_KE + s));
           if (n + 2 < I.nb) {
             const int s2 = (kit + n + 2) % C::KST;
@@ -625,8 +644,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(bar(C::B_DR));
       drain_wait_b(bar(C::B_DR), 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kRegsCtl>();  // warps 2 and 3 have no role
+  } else {
     // ------------------------------------------------------------ softmax + epilogue
+    regs_inc<kRegsSoftmax>();
     const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: dQ columns [x D/2, (x+1) D/2)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -661,27 +683,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // key columns c > lim are masked: after the query (causal) or past the segment end
         const int lim = p.causal ? qrow - n * 64 : I.l - 1 - n * 64;
         const bool need_mask = p.causal ? (n * 64 + 63 > I.m * 128) : (n * 64 + 64 > I.l);
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sv[32], dpv[32];
-          tmem_ld32(s_addr + hh * 32, sv);
-          tmem_ld32(dp_addr + hh * 32, dpv);
-          tmem_wait_ld();
+        // one TMEM round trip: the step's 64 scores and 64 dP values of this q row
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(s_addr, sv);
+        tmem_ld32(s_addr + 32, sv + 32);
+        tmem_ld32(dp_addr, dpv);
+        tmem_ld32(dp_addr + 32, dpv + 32);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
-            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            if (need_mask) {
-              if (hh * 32 + c > lim) p0 = 0.f;
-              if (hh * 32 + c + 1 > lim) p1 = 0.f;
-            }
-            float t0, t1;
-            fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
-            dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
+        for (int c = 0; c < 64; c += 2) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
+          float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          if (need_mask) {
+            if (c > lim) p0 = 0.f;
+            if (c + 1 > lim) p1 = 0.f;
           }
-          tmem_st16(dp_addr + hh * 16, dpv);
+          float t0, t1;
+          fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
+          dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
         }
+        tmem_st32(dp_addr, dpv);
         tmem_wait_st();
         fence_before_sync();
         mbar_arrive(bar(C::B_PF + x));
@@ -696,18 +718,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_after_sync();
       const bool store = qrow < I.l;
       bf16* out = p.dq + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
-#pragma unroll 1
-      for (int c = x * (D / 64); c < (x + 1) * (D / 64); ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(acc_addr + c * 32, o);
-        uint32_t pk[16];
+      {
+        constexpr int HC = D / 2;  // this warpgroup's columns [x HC, (x + 1) HC), one round trip
+        uint32_t o[HC];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * p.scale, __uint_as_float(o[2 * j + 1]) * p.scale);
+        for (int c = 0; c < HC / 32; ++c) tmem_ld32(acc_addr + x * HC + c * 32, o + c * 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < HC / 2; ++j)
+          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * p.scale, __uint_as_float(o[2 * j + 1]) * p.scale);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(out + x * HC);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < HC / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
       }
       fence_before_sync();
@@ -736,6 +759,11 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  // the in-kernel register split assumes the full launch budget; refuse rather than wait
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -756,6 +784,11 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  // the in-kernel register split assumes the full launch budget; refuse rather than wait
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
