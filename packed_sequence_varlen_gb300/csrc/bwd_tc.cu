@@ -20,7 +20,8 @@
 //                     dQ += dS K                           (TS)
 // Layout of both (384 threads, one CTA per SM, persistent over the tile map):
 //   warp 0 TMA producer, which also pulls work items from the map's counter and
-//   publishes them (sched.cuh); warp 1 MMA issuer + TMEM owner; warps 4-7 and 8-11 two
+//   publishes them (sched.cuh); warp 1 MMA issuer + TMEM owner; warp 2 (dK/dV only) stages
+//   lse and D of each step in shared memory; warps 4-7 and 8-11 two
 //   softmax warpgroups that take alternate steps, each with its own TMEM S/dP
 //   buffer, so the tensor core computes step i+1 while step i is exponentiated.
 // TMEM: S_0 | S_1 | dP_0 | dP_1 (64 columns each) | accumulators.
@@ -41,20 +42,11 @@ constexpr int kLaunchRegs = 168;
 constexpr int kRegsCtl = 80, kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kBwdThreads * kLaunchRegs, "register split exceeds the launch");
 
-__device__ __forceinline__ void named_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
-}
-
 __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > 50000000ull) return;
   }
-}
-
-__device__ __forceinline__ void tmem_ld32_wait(uint32_t a, uint32_t* v) {
-  tmem_ld32(a, v);
-  tmem_wait_ld();
 }
 
 // ================================================================= dK / dV
@@ -67,11 +59,13 @@ struct KvCfg {
   static constexpr int PKV = KB * 128, PQ = QB * 128;  // 64-column panels
   // two K/V buffers (items alternate): buffer b holds K at KV_OFF(b), V right after
   static constexpr int RING_OFF = 4 * TKV;
-  static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [2 wg][2 slot][lse | D][64] fp32
-  static constexpr int BAR_OFF = LD_OFF + 2 * 2 * 2 * 64 * 4;
+  static constexpr int LDS = 4;                            // lse/D ring slots (one step each)
+  static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [LDS][lse*log2e 64 | D 64] fp32
+  static constexpr int BAR_OFF = LD_OFF + LDS * 2 * 64 * 4;
   static constexpr int B_KVF = 0, B_KVE = 2, B_QF = 4, B_QE = 4 + QST, B_SF = 4 + 2 * QST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
-                       B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;
+                       B_IF = B_DR + 1, B_IE = B_IF + 2, B_LF = B_IE + 2, B_LE = B_LF + LDS,
+                       NBAR = B_LE + LDS;
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
   static constexpr int MISC_OFF = QUEUE_OFF + 2 * 32;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
@@ -140,7 +134,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::B_DR), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_IF + b), 1);
-      mbar_init(bar(C::B_IE + b), 1 + 256);  // MMA thread + both softmax warpgroups
+      mbar_init(bar(C::B_IE + b), 1 + 256 + 32);  // MMA thread, softmax warpgroups, lse/D warp
+    }
+    for (int b = 0; b < C::LDS; ++b) {
+      mbar_init(bar(C::B_LF + b), 32);
+      mbar_init(bar(C::B_LE + b), 128);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -282,33 +280,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(bar(C::B_DR));
       drain_wait_b(bar(C::B_DR), 0);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ lse / D loader
+    // For every step, in the order the softmax warpgroups take them: lse * log2(e) and
+    // D of the step's 64 q rows into a shared-memory ring (out-of-segment rows get
+    // +inf / 0, so their P is 0).
+    regs_dec<kRegsCtl>();
+    int g = 0;  // steps of this CTA so far
+    bool ok = true;
+    for (int item_cnt = 0;; ++item_cnt) {
+      KvItem I;
+      const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+      if (!__all_sync(0xffffffffu, ok) || !got) break;
+      for (int i = 0; i < I.steps; ++i, ++g) {
+        const int slot = g % C::LDS;
+        ok = mbar_wait(bar(C::B_LE + slot), ((g / C::LDS) & 1) ^ 1, abort_flag, p.hdr, 30);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
+        float* dst = reinterpret_cast<float*>(sm + C::LD_OFF) + slot * 128;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = lane + 32 * e;
+          const int qr = m * 64 + c;
+          const int64_t at = static_cast<int64_t>(h) * p.T + I.s0 + qr;
+          const bool in = qr < I.l;
+          dst[c] = in ? p.lse[at] * kLog2e : INFINITY;
+          dst[64 + c] = in ? p.dsum[at] : 0.f;
+        }
+        mbar_arrive(bar(C::B_LF + slot));  // release: this lane's values are visible
+      }
+      if (!ok) break;
+    }
   } else if (warp < 4) {
-    regs_dec<kRegsCtl>();  // warps 2 and 3 have no role
+    regs_dec<kRegsCtl>();  // warp 3 has no role
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     regs_inc<kRegsSoftmax>();
     const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: 0 -> dV, 1 -> dK
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int tid = threadIdx.x - 128 - 128 * x;  // 0..127 within the warpgroup
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + x * 64;
     const uint32_t dp_addr = tmem + lane_off + 128 + x * 64;
     const uint32_t acc_addr = tmem + lane_off + 256 + x * D;
-    float* ldbuf = reinterpret_cast<float*>(sm + C::LD_OFF) + x * 2 * 128;  // [slot][lse 64 | D 64]
+    const float* ldring = reinterpret_cast<const float*>(sm + C::LD_OFF);  // [slot][lse 64 | D 64]
     const float sl2 = p.scale_log2;
     uint32_t sf = 0;
     int item_cnt = 0;
     bool ok = true;
-    auto fetch = [&](const KvItem& I, int i, float& lv, float& dv) {
-      if (tid < 64) {
-        const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
-        const int qr = m * 64 + tid;
-        const int64_t at = static_cast<int64_t>(h) * p.T + I.s0 + qr;
-        lv = qr < I.l ? p.lse[at] * kLog2e : INFINITY;
-        dv = qr < I.l ? p.dsum[at] : 0.f;
-      }
-    };
+    int g0 = 0;  // this CTA's steps before the current item (the lse/D ring index)
     for (;; ++item_cnt) {
       KvItem I;
       const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
@@ -318,20 +338,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!got) break;
       const int kvrow = I.n * 128 + r;
-      int slot = 0;
-      if (x < I.steps) {
-        float lv = 0.f, dv = 0.f;
-        fetch(I, x, lv, dv);
-        if (tid < 64) {
-          ldbuf[tid] = lv;
-          ldbuf[64 + tid] = dv;
-        }
-      }
-      named_sync(1 + x);
       for (int i = x; i < I.steps; i += 2) {
-        float nlv = 0.f, ndv = 0.f;
-        const bool have_next = i + 2 < I.steps;
-        if (have_next) fetch(I, i + 2, nlv, ndv);
+        const int gs = g0 + i, ls = gs % C::LDS;
+        ok = mbar_wait(bar(C::B_LF + ls), (gs / C::LDS) & 1, abort_flag, p.hdr, 19);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
         ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 28);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -342,7 +355,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q0 = (I.m_start + i / p.g) * 64;
         const int lim = kvrow - q0;  // query columns c < lim are masked (key after query)
         const bool need_mask = p.causal && (I.n * 128 + 127 > q0);
-        const float* L = ldbuf + slot * 128;
+        const float* L = ldring + ls * 128;
         const float* Dd = L + 64;
         // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
         uint32_t sv[64], dpv[64];
@@ -375,17 +388,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tmem_st32(s_addr, sv);
         tmem_st32(dp_addr, dpv);
+        mbar_arrive(bar(C::B_LE + ls));  // this thread has read the slot's lse/D
         tmem_wait_st();
         fence_before_sync();
         mbar_arrive(bar(C::B_PF + x));
-        if (have_next && tid < 64) {
-          ldbuf[(slot ^ 1) * 128 + tid] = nlv;
-          ldbuf[(slot ^ 1) * 128 + 64 + tid] = ndv;
-        }
-        named_sync(1 + x);
-        slot ^= 1;
       }
       if (!ok) break;
+      g0 += I.steps;
       // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
       ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 29);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -405,11 +414,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int j = 0; j < D / 2; ++j)
           o[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(out);
+        uint4 ov[D / 8];
 #pragma unroll
-          for (int j = 0; j < D / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
+        for (int j = 0; j < D / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        store_rows_coalesced(ov, out, p.k_rs, store);
       }
       fence_before_sync();
       mbar_arrive(bar(C::B_AE));
@@ -727,7 +735,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int j = 0; j < HC / 2; ++j)
           o[j] = pack_bf16(__uint_as_float(o[2 * j]) * p.scale, __uint_as_float(o[2 * j + 1]) * p.scale);
-        if (store) {
+        if constexpr (HC % 64 == 0) {
+          uint4 ov[HC / 8];
+#pragma unroll
+          for (int j = 0; j < HC / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          store_rows_coalesced(ov, out + x * HC, p.o_rs, store);
+        } else if (store) {
           uint4* dst = reinterpret_cast<uint4*>(out + x * HC);
 #pragma unroll
           for (int j = 0; j < HC / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);

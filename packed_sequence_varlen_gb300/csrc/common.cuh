@@ -123,4 +123,42 @@ __device__ __forceinline__ uint32_t swz(int r, int c16) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Stores 32 rows held one per lane (W 16-byte chunks each, W a multiple of 8) so that
+// every 8 lanes write 128 contiguous bytes.  Within each group of 8 lanes an 8 x 8
+// transpose of 16-byte chunks (three xor-shuffle stages) leaves lane j with chunk j of
+// each of the group's 8 rows; store k then writes row (group base + k).  `row` is this
+// lane's row, rows of consecutive lanes are `stride` elements apart, and a row is written
+// only when its own lane passed valid = true.  Warp-collective.
+template <int W, class T>
+__device__ __forceinline__ void store_rows_coalesced(uint4 (&a)[W], T* row, int64_t stride, bool valid) {
+  static_assert(W % 8 == 0, "rows must be a multiple of 128 bytes");
+  const int lane = threadIdx.x & 31, j = lane & 7;
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+  for (int b = 0; b < W / 8; ++b) {
+    uint4* c = a + 8 * b;
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1) {
+      const bool hi = (j & d) != 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i & d) continue;
+        const uint4 send = hi ? c[i] : c[i + d];
+        uint4 recv;
+        recv.x = __shfl_xor_sync(0xffffffffu, send.x, d);
+        recv.y = __shfl_xor_sync(0xffffffffu, send.y, d);
+        recv.z = __shfl_xor_sync(0xffffffffu, send.z, d);
+        recv.w = __shfl_xor_sync(0xffffffffu, send.w, d);
+        if (hi) c[i] = recv;
+        else c[i + d] = recv;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if ((vmask >> ((lane & ~7) + k)) & 1u)
+        reinterpret_cast<uint4*>(row + static_cast<int64_t>(k - j) * stride)[8 * b + j] = c[k];
+    }
+  }
+}
+
 }  // namespace va
