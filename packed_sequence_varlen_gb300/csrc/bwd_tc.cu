@@ -162,27 +162,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
     if (lane == 0) {
-      int qit = 0, item_cnt = 0;
+      int qit = 0, item_cnt = 0, kv_issued = 0;  // kv_issued: items whose K/V load went out
       bool ok = true;
       KvItem nxt;
+      // K/V of this CTA's j-th item into buffer j & 1, once item j-2's S/dP MMAs are done
+      // with it
+      auto load_kv = [&](const KvItem& J, int j) -> bool {
+        const int kb = j & 1;
+        if (!mbar_wait(bar(C::B_KVE + kb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
+        mbar_expect_tx(bar(C::B_KVF + kb), 2 * C::TKV);
+        for (int pn = 0; pn < D / 64; ++pn) {
+          tma_load_3d(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, J.hk,
+                      J.s0 + J.n * 128);
+          tma_load_3d(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
+                      J.hk, J.s0 + J.n * 128);
+        }
+        kv_issued = j + 1;
+        return true;
+      };
       bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
                                 abort_flag, p.hdr, ok);
+      if (ok && more) ok = load_kv(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const KvItem I = nxt;  // publish the next record first: its decode overlaps this one
         more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items,
                              dec, nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
-        const int kb = item_cnt & 1;
-        ok = mbar_wait(bar(C::B_KVE + kb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 21);
-        if (!ok) break;
-        mbar_expect_tx(bar(C::B_KVF + kb), 2 * C::TKV);
-        for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, I.hk,
-                      I.s0 + I.n * 128);
-          tma_load_3d(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
-                      I.hk, I.s0 + I.n * 128);
-        }
-        for (int i = 0; ok && i < I.steps; ++i, ++qit) {
+        // the next item's K/V goes out right after this item's first two Q/dO steps, a whole
+        // item ahead of its use
+        const int kv_at = I.steps < 2 ? I.steps : 2;
+        for (int i = 0; ok && i <= I.steps; ++i) {
+          if (i == kv_at && more) {
+            ok = load_kv(nxt, item_cnt + 1);
+            if (!ok) break;
+          }
+          if (i == I.steps) break;
           const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
           const int s = qit % C::QST;
           ok = mbar_wait(bar(C::B_QE + s), ((qit / C::QST) & 1) ^ 1, abort_flag, p.hdr, 22);
@@ -193,10 +207,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d(dst + pn * C::PQ, &tq, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
             tma_load_3d(dst + C::TQ + pn * C::PQ, &tdo, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
           }
+          ++qit;
         }
       }
       if (!ok) {
-        drain_wait_b(bar(C::B_KVF + (item_cnt & 1)), (item_cnt >> 1) & 1);
+        // let every copy this thread started land before the CTA exits
+        for (int j = kv_issued - 1; j >= 0 && j >= kv_issued - 2; --j)
+          drain_wait_b(bar(C::B_KVF + (j & 1)), (j >> 1) & 1);
         for (int i = qit - 1; i >= 0 && i >= qit - C::QST; --i)
           drain_wait_b(bar(C::B_QF + i % C::QST), (i / C::QST) & 1);
       }
@@ -538,27 +555,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
     if (lane == 0) {
-      int kit = 0, item_cnt = 0;
+      int kit = 0, item_cnt = 0, qd_issued = 0;  // qd_issued: items whose Q/dO load went out
       bool ok = true;
       QItem nxt;
+      // Q/dO of this CTA's j-th item into buffer j & 1, once item j-2's S/dP MMAs are done
+      // with it
+      auto load_qd = [&](const QItem& J, int j) -> bool {
+        const int qb = j & 1;
+        if (!mbar_wait(bar(C::B_QDE + qb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 31)) return false;
+        mbar_expect_tx(bar(C::B_QDF + qb), 2 * C::TQ);
+        for (int pn = 0; pn < D / 64; ++pn) {
+          tma_load_3d(base + C::qd_off(qb) + pn * C::PQ, &tq, bar(C::B_QDF + qb), pn * 64, J.h,
+                      J.s0 + J.m * 128);
+          tma_load_3d(base + C::qd_off(qb) + C::TQ + pn * C::PQ, &tdo, bar(C::B_QDF + qb), pn * 64, J.h,
+                      J.s0 + J.m * 128);
+        }
+        qd_issued = j + 1;
+        return true;
+      };
       bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
                                 abort_flag, p.hdr, ok);
+      if (ok && more) ok = load_qd(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const QItem I = nxt;  // publish the next record first: its decode overlaps this one
         more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items,
                              dec, nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
-        const int qb = item_cnt & 1;
-        ok = mbar_wait(bar(C::B_QDE + qb), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 31);
-        if (!ok) break;
-        mbar_expect_tx(bar(C::B_QDF + qb), 2 * C::TQ);
-        for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(base + C::qd_off(qb) + pn * C::PQ, &tq, bar(C::B_QDF + qb), pn * 64, I.h,
-                      I.s0 + I.m * 128);
-          tma_load_3d(base + C::qd_off(qb) + C::TQ + pn * C::PQ, &tdo, bar(C::B_QDF + qb), pn * 64, I.h,
-                      I.s0 + I.m * 128);
-        }
-        for (int n = 0; ok && n < I.nb; ++n, ++kit) {
+        // the next item's Q/dO goes out right after this item's first two K/V steps
+        const int qd_at = I.nb < 2 ? I.nb : 2;
+        for (int n = 0; ok && n <= I.nb; ++n) {
+          if (n == qd_at && more) {
+            ok = load_qd(nxt, item_cnt + 1);
+            if (!ok) break;
+          }
+          if (n == I.nb) break;
           const int s = kit % C::KST;
           ok = mbar_wait(bar(C::B_KE + s), ((kit / C::KST) & 1) ^ 1, abort_flag, p.hdr, 32);
           if (!ok) break;
@@ -568,10 +598,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d(dst + pn * C::PKV, &tk, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
             tma_load_3d(dst + C::TKV + pn * C::PKV, &tv, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
           }
+          ++kit;
         }
       }
       if (!ok) {
-        drain_wait_b(bar(C::B_QDF + (item_cnt & 1)), (item_cnt >> 1) & 1);
+        // let every copy this thread started land before the CTA exits
+        for (int j = qd_issued - 1; j >= 0 && j >= qd_issued - 2; --j)
+          drain_wait_b(bar(C::B_QDF + (j & 1)), (j >> 1) & 1);
         for (int i = kit - 1; i >= 0 && i >= kit - C::KST; --i)
           drain_wait_b(bar(C::B_KF + i % C::KST), (i / C::KST) & 1);
       }
@@ -678,8 +711,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!got) break;
       const int qrow = I.m * 128 + r;
       const int64_t at = static_cast<int64_t>(I.h) * p.T + I.s0 + qrow;
-      const float lse2 = qrow < I.l ? p.lse[at] * kLog2e : INFINITY;
-      const float dsum = qrow < I.l ? p.dsum[at] : 0.f;
+      // the row's lse and D: loads issued here, first used after the S wait below, so their
+      // latency overlaps it
+      const bool qin = qrow < I.l;
+      float lse_raw = 0.f, dsum = 0.f;
+      if (qin) {
+        lse_raw = __ldg(p.lse + at);
+        dsum = __ldg(p.dsum + at);
+      }
       for (int n = x; n < I.nb; n += 2) {
         ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 38);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -688,6 +727,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         ++sf;
         fence_after_sync();
+        const float lse2 = qin ? lse_raw * kLog2e : INFINITY;
         // key columns c > lim are masked: after the query (causal) or past the segment end
         const int lim = p.causal ? qrow - n * 64 : I.l - 1 - n * 64;
         const bool need_mask = p.causal ? (n * 64 + 63 > I.m * 128) : (n * 64 + 64 > I.l);

@@ -57,14 +57,22 @@ __device__ __forceinline__ int cost_class(int c) { return 31 - __clz(max(c, 1));
 
 constexpr int kPlanThreads = 1024;
 
+// Up to this many segments the boundaries and per-segment offsets live in shared memory
+// (one coalesced read of cu_seqlens per launch); beyond it they are read from and kept in
+// global memory.
+constexpr int kSmemSegs = 4096;
+
 struct PlanSmem {
   int count[32];
   int offset[32];
   int overflow;
+  int cu[kSmemSegs + 1];
+  int off[kSmemSegs];
 };
 
-// Builds one map (all 1024 threads of the block take part).
-__device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
+// Builds one map (all 1024 threads of the block take part).  cu: the boundaries (the
+// shared-memory copy or a.cu); seg_off: where the per-segment offsets go.
+__device__ void plan_body(const PlanArgs& a, PlanSmem& sh, const int* cu, int* seg_off) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int k = 31 - warp;  // this warp's cost class
   // records per class
@@ -74,7 +82,7 @@ __device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
     int cnt = 0;
     if (b < a.B) {
       int nblk, cost;
-      seg_cost(a, a.cu[b + 1] - a.cu[b], nblk, cost);
+      seg_cost(a, cu[b + 1] - cu[b], nblk, cost);
       if (cost_class(cost) == k) cnt = nblk * a.heads;
     }
 #pragma unroll
@@ -103,7 +111,7 @@ __device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
     int cnt = 0;
     if (b < a.B) {
       int nblk, cost;
-      seg_cost(a, a.cu[b + 1] - a.cu[b], nblk, cost);
+      seg_cost(a, cu[b + 1] - cu[b], nblk, cost);
       if (cost_class(cost) == k) cnt = nblk * a.heads;
     }
     int incl = cnt;
@@ -112,16 +120,16 @@ __device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    if (cnt > 0) a.seg_off[b] = base + incl - cnt;
+    if (cnt > 0) seg_off[b] = base + incl - cnt;
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
   __syncthreads();
   // records: a warp per segment, heads outer, blocks inner
   for (int b = warp; b < a.B; b += 32) {
-    const int l = a.cu[b + 1] - a.cu[b];
+    const int l = cu[b + 1] - cu[b];
     int nblk, cost;
     seg_cost(a, l, nblk, cost);
-    const int off = a.seg_off[b];
+    const int off = seg_off[b];
     for (int r = lane; r < nblk * a.heads; r += 32) {
       const int h = r / nblk, j = r - h * nblk;
       TileItem t;
@@ -134,13 +142,22 @@ __device__ void plan_body(const PlanArgs& a, PlanSmem& sh) {
   __syncthreads();
 }
 
+// Copies cu[0..B] into shared memory when it fits; returns the array to read.
+__device__ const int* stage_cu(const int32_t* cu, int B, PlanSmem& sh) {
+  if (B + 1 > kSmemSegs) return cu;
+  for (int i = threadIdx.x; i <= B; i += blockDim.x) sh.cu[i] = cu[i];
+  __syncthreads();
+  return sh.cu;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   __shared__ PlanSmem sh;
   if (a.status && *a.status != VA_OK) {
     if (threadIdx.x == 0) *a.n_items = 0;
     return;
   }
-  plan_body(a, sh);
+  const int* cu = stage_cu(a.cu, a.B, sh);
+  plan_body(a, sh, cu, a.B + 1 > kSmemSegs ? a.seg_off : sh.off);
 }
 
 struct PlanPair {
@@ -155,12 +172,13 @@ struct PlanPair {
 __global__ void __launch_bounds__(kPlanThreads) validate_plan_kernel(PlanPair pp) {
   __shared__ PlanSmem sh;
   const PlanArgs& a0 = pp.map[0];
+  const int* cu = stage_cu(a0.cu, a0.B, sh);  // every map is built from the same boundaries
   int bad = 0;
   for (int b = threadIdx.x; b < a0.B; b += blockDim.x) {
-    const int x = a0.cu[b], y = a0.cu[b + 1];
+    const int x = cu[b], y = cu[b + 1];
     if (y <= x || y - x > pp.max_seqlen) bad = 1;
   }
-  if (threadIdx.x == 0 && (a0.cu[0] != 0 || a0.cu[a0.B] != pp.T)) bad = 1;
+  if (threadIdx.x == 0 && (cu[0] != 0 || cu[a0.B] != pp.T)) bad = 1;
   bad = __syncthreads_or(bad);
   if (bad) {
     if (threadIdx.x == 0) {
@@ -170,7 +188,8 @@ __global__ void __launch_bounds__(kPlanThreads) validate_plan_kernel(PlanPair pp
     return;
   }
   if (threadIdx.x == 0) *a0.status = VA_OK;
-  for (int i = 0; i < pp.nmaps; ++i) plan_body(pp.map[i], sh);
+  for (int i = 0; i < pp.nmaps; ++i)
+    plan_body(pp.map[i], sh, cu, a0.B + 1 > kSmemSegs ? pp.map[i].seg_off : sh.off);
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
