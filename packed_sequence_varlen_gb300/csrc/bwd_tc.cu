@@ -20,7 +20,8 @@
 //                     dQ += dS K                           (TS)
 // Layout of both (384 threads, one CTA per SM, persistent over the tile map):
 //   warp 0 TMA producer, which also pulls work items from the map's counter and
-//   publishes them (sched.cuh); warp 1 MMA issuer + TMEM owner; warp 2 (dK/dV only) stages
+//   publishes them (sched.cuh); warp 1 MMA issuer (whole warp, one elected lane issues) +
+//   TMEM owner; warp 2 (dK/dV only) stages
 //   lse and D of each step in shared memory; warps 4-7 and 8-11 two
 //   softmax warpgroups that take alternate steps, each with its own TMEM S/dP
 //   buffer, so the tensor core computes step i+1 while step i is exponentiated.
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::B_DR), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_IF + b), 1);
-      mbar_init(bar(C::B_IE + b), 1 + 256 + 32);  // MMA thread, softmax warpgroups, lse/D warp
+      mbar_init(bar(C::B_IE + b), 32 + 256 + 32);  // MMA warp, softmax warpgroups, lse/D warp
     }
     for (int b = 0; b < C::LDS; ++b) {
       mbar_init(bar(C::B_LF + b), 32);
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     regs_dec<kRegsCtl>();
-    if (lane == 0) {
+    {  // the whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idG = idesc_bf16(128, D, false, true);
       int qit = 0, item_cnt = 0;
@@ -237,64 +238,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4, oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + x * 64, kd + okv, qd + oq, idS, kk > 0);
+          mma_ss_w(tmem + x * 64, kd + okv, qd + oq, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4, oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + 128 + x * 64, vd + okv, dd + oq, idS, kk > 0);
+          mma_ss_w(tmem + 128 + x * 64, vd + okv, dd + oq, idS, kk > 0);
         }
-        mma_commit(bar(C::B_SF + x));
+        mma_commit_w(bar(C::B_SF + x));
       };
       for (;; ++item_cnt) {
         KvItem I;
-        if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
+        const bool got_ = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        if (!all_ok) ok = false;
+        if (!all_ok || !got_) break;
         kb = item_cnt & 1;
-        ok = mbar_wait(bar(C::B_KVF + kb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 23);
+        ok = wwait(bar(C::B_KVF + kb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 23);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.steps; ++j) {
           const int s = (qit + j) % C::QST;
-          ok = mbar_wait(bar(C::B_QF + s), ((qit + j) / C::QST) & 1, abort_flag, p.hdr, 24);
+          ok = wwait(bar(C::B_QF + s), ((qit + j) / C::QST) & 1, abort_flag, p.hdr, 24);
           if (!ok) break;
           fence_after_sync();
           issue_SdP(j, s);
         }
         if (!ok) break;
-        if (I.steps <= 2) mma_commit(bar(C::B_KVE + kb));
+        if (I.steps <= 2) mma_commit_w(bar(C::B_KVE + kb));
         for (int i = 0; ok && i < I.steps; ++i) {
           const int x = i & 1, s = (qit + i) % C::QST;
-          ok = mbar_wait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 25);
+          ok = wwait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 25);
           if (!ok) break;
           if (x) ++pf1;
           else ++pf0;
           if (i == 0) {  // the accumulators must have been read out by the previous epilogue
-            ok = mbar_wait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 26);
+            ok = wwait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 26);
             if (!ok) break;
           }
           fence_after_sync();
           const uint32_t qm = ringM0 + ((s * 2 * C::TQ) >> 4), dm = qm + (C::TQ >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts_lo(tmem + 256, tmem + x * 64 + kk * 8, dm + kk * (2048 >> 4), idG, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tmem + 256, tmem + x * 64 + kk * 8, dm + kk * (2048 >> 4), idG, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts_lo(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, qm + kk * (2048 >> 4), idG,
+            mma_ts_w(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, qm + kk * (2048 >> 4), idG,
                       (i > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(C::B_QE + s));
+          mma_commit_w(bar(C::B_QE + s));
           if (i + 2 < I.steps) {
             const int s2 = (qit + i + 2) % C::QST;
-            ok = mbar_wait(bar(C::B_QF + s2), ((qit + i + 2) / C::QST) & 1, abort_flag, p.hdr, 27);
+            ok = wwait(bar(C::B_QF + s2), ((qit + i + 2) / C::QST) & 1, abort_flag, p.hdr, 27);
             if (!ok) break;
             fence_after_sync();
             issue_SdP(x, s2);
-            if (i + 2 == I.steps - 1) mma_commit(bar(C::B_KVE + kb));
+            if (i + 2 == I.steps - 1) mma_commit_w(bar(C::B_KVE + kb));
           }
         }
         if (!ok) break;
-        mma_commit(bar(C::B_AF));
+        mma_commit_w(bar(C::B_AF));
         qit += I.steps;
       }
-      mma_commit(bar(C::B_DR));
+      mma_commit_w(bar(C::B_DR));
       drain_wait_b(bar(C::B_DR), 0);
     }
   } else if (warp == 2) {
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::B_DR), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_IF + b), 1);
-      mbar_init(bar(C::B_IE + b), 1 + 256);  // MMA thread + both softmax warpgroups
+      mbar_init(bar(C::B_IE + b), 32 + 256);  // MMA warp + both softmax warpgroups
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     regs_dec<kRegsCtl>();
-    if (lane == 0) {
+    {  // the whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idG = idesc_bf16(128, D, false, true);
       int kit = 0, item_cnt = 0;
@@ -628,61 +632,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4, ok_ = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + x * 64, qd + oq, kd + ok_, idS, kk > 0);
+          mma_ss_w(tmem + x * 64, qd + oq, kd + ok_, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4, ok_ = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + 128 + x * 64, dd + oq, vd + ok_, idS, kk > 0);
+          mma_ss_w(tmem + 128 + x * 64, dd + oq, vd + ok_, idS, kk > 0);
         }
-        mma_commit(bar(C::B_SF + x));
+        mma_commit_w(bar(C::B_SF + x));
       };
       for (;; ++item_cnt) {
         QItem I;
-        if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
+        const bool got_ = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        if (!all_ok) ok = false;
+        if (!all_ok || !got_) break;
         qb = item_cnt & 1;
-        ok = mbar_wait(bar(C::B_QDF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 33);
+        ok = wwait(bar(C::B_QDF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 33);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.nb; ++j) {
           const int s = (kit + j) % C::KST;
-          ok = mbar_wait(bar(C::B_KF + s), ((kit + j) / C::KST) & 1, abort_flag, p.hdr, 34);
+          ok = wwait(bar(C::B_KF + s), ((kit + j) / C::KST) & 1, abort_flag, p.hdr, 34);
           if (!ok) break;
           fence_after_sync();
           issue_SdP(j, s);
         }
         if (!ok) break;
-        if (I.nb <= 2) mma_commit(bar(C::B_QDE + qb));
+        if (I.nb <= 2) mma_commit_w(bar(C::B_QDE + qb));
         for (int n = 0; ok && n < I.nb; ++n) {
           const int x = n & 1, s = (kit + n) % C::KST;
-          ok = mbar_wait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 35);
+          ok = wwait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 35);
           if (!ok) break;
           if (x) ++pf1;
           else ++pf0;
           if (n == 0) {
-            ok = mbar_wait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 36);
+            ok = wwait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 36);
             if (!ok) break;
           }
           fence_after_sync();
           const uint32_t km = ringM0 + ((s * 2 * C::TKV) >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::KB / 16; ++kk)
-            mma_ts_lo(tmem + 256, tmem + 128 + x * 64 + kk * 8, km + kk * (2048 >> 4), idG,
+            mma_ts_w(tmem + 256, tmem + 128 + x * 64 + kk * 8, km + kk * (2048 >> 4), idG,
                       (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(C::B_KE + s));
+          mma_commit_w(bar(C::B_KE + s));
           if (n + 2 < I.nb) {
             const int s2 = (kit + n + 2) % C::KST;
-            ok = mbar_wait(bar(C::B_KF + s2), ((kit + n + 2) / C::KST) & 1, abort_flag, p.hdr, 37);
+            ok = wwait(bar(C::B_KF + s2), ((kit + n + 2) / C::KST) & 1, abort_flag, p.hdr, 37);
             if (!ok) break;
             fence_after_sync();
             issue_SdP(x, s2);
-            if (n + 2 == I.nb - 1) mma_commit(bar(C::B_QDE + qb));
+            if (n + 2 == I.nb - 1) mma_commit_w(bar(C::B_QDE + qb));
           }
         }
         if (!ok) break;
-        mma_commit(bar(C::B_AF));
+        mma_commit_w(bar(C::B_AF));
         kit += I.nb;
       }
-      mma_commit(bar(C::B_DR));
+      mma_commit_w(bar(C::B_DR));
       drain_wait_b(bar(C::B_DR), 0);
     }
   } else if (warp < 4) {

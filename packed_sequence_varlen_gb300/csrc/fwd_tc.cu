@@ -12,7 +12,8 @@
 // CTA layout (384 threads, one CTA per SM, persistent over the tile map):
 //   warp 0      TMA producer: pulls work items from the map's counter and publishes them
 //               (sched.cuh); Q tiles once per item, K/V tiles into an NST-slot ring
-//   warp 1      MMA issuer (one thread): S_t = Q_t K^T (SS), O_t += P_t V (TS, P in TMEM);
+//   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues):
+//               S_t = Q_t K^T (SS), O_t += P_t V (TS, P in TMEM);
 //               also owns the TMEM allocation
 //   warps 4-7   softmax + epilogue for q tile 0 (rows 0..127 of the block; thread = row)
 //   warps 8-11  softmax + epilogue for q tile 1 (rows 128..255)
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar(C::B_DR), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_IF + b), 1);
-      mbar_init(bar(C::B_IE + b), 1 + 256);  // MMA thread + both softmax warpgroups
+      mbar_init(bar(C::B_IE + b), 32 + 256);  // MMA warp + both softmax warpgroups
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     regs_dec<kRegsCtl>();
-    if (lane == 0) {
+    {  // the whole warp runs the loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = idesc_bf16(128, kTcBN, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
       int kv_it = 0, item_cnt = 0;
@@ -255,52 +256,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::PANEL + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + t * 128, qd + off, kd + off, idS, kk > 0);
+          mma_ss_w(tmem + t * 128, qd + off, kd + off, idS, kk > 0);
         }
-        mma_commit(bar(C::B_SF + t));
+        mma_commit_w(bar(C::B_SF + t));
       };
       auto issue_PV = [&](int t, int slot, bool acc) {
         const uint32_t vd = vlo0 + ((slot * C::TILE) >> 4);
         const uint32_t d_tm = tmem + 256 + t * C::OCOLS, p_tm = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kTcBN / 16; ++kk)
-          mma_ts_lo(d_tm, p_tm + kk * 8, vd + kk * (2048 >> 4), idPV, (acc || kk > 0) ? 1u : 0u);
-        mma_commit(bar(C::B_OF + t));
+          mma_ts_w(d_tm, p_tm + kk * 8, vd + kk * (2048 >> 4), idPV, (acc || kk > 0) ? 1u : 0u);
+        mma_commit_w(bar(C::B_OF + t));
       };
       for (;; ++item_cnt) {
         Item I;
-        if (!queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok)) break;
-        ok = mbar_wait(bar(C::B_QF + 0), qcnt[0] & 1, abort_flag, p.hdr, 3);
+        const bool got_ = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        if (!all_ok) ok = false;
+        if (!all_ok || !got_) break;
+        ok = wwait(bar(C::B_QF + 0), qcnt[0] & 1, abort_flag, p.hdr, 3);
         if (!ok) break;
         if (I.t1) {
-          ok = mbar_wait(bar(C::B_QF + 1), qcnt[1] & 1, abort_flag, p.hdr, 3);
+          ok = wwait(bar(C::B_QF + 1), qcnt[1] & 1, abort_flag, p.hdr, 3);
           if (!ok) break;
         }
         int ks = kv_it % C::NST;
-        ok = mbar_wait(bar(C::B_KVF + ks), (kv_it / C::NST) & 1, abort_flag, p.hdr, 4);
+        ok = wwait(bar(C::B_KVF + ks), (kv_it / C::NST) & 1, abort_flag, p.hdr, 4);
         if (!ok) break;
         fence_after_sync();
         ++kv_it;
         issue_S(0, ks);
         if (I.nb0 == 1) {
-          mma_commit(bar(C::B_QE + 0));  // last S_0 of the item: Q tile 0 may be reloaded
+          mma_commit_w(bar(C::B_QE + 0));  // last S_0 of the item: Q tile 0 may be reloaded
           ++qcnt[0];
         }
         if (I.t1) {
           issue_S(1, ks);
           if (I.nb == 1) {
-            mma_commit(bar(C::B_QE + 1));
+            mma_commit_w(bar(C::B_QE + 1));
             ++qcnt[1];
           }
         }
-        mma_commit(bar(C::B_KVE + ks));
+        mma_commit_w(bar(C::B_KVE + ks));
         for (int n = 0; ok && n < I.nb; ++n) {
           const int vs = kv_it % C::NST;
-          ok = mbar_wait(bar(C::B_KVF + vs), (kv_it / C::NST) & 1, abort_flag, p.hdr, 5);
+          ok = wwait(bar(C::B_KVF + vs), (kv_it / C::NST) & 1, abort_flag, p.hdr, 5);
           if (!ok) break;
           ++kv_it;
           if (n < I.nb0) {
-            ok = mbar_wait(bar(C::B_PF + 0), pf[0] & 1, abort_flag, p.hdr, 6);
+            ok = wwait(bar(C::B_PF + 0), pf[0] & 1, abort_flag, p.hdr, 6);
             if (!ok) break;
             ++pf[0];
             fence_after_sync();
@@ -309,40 +313,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           int ks2 = -1;
           if (n + 1 < I.nb) {
             ks2 = kv_it % C::NST;
-            ok = mbar_wait(bar(C::B_KVF + ks2), (kv_it / C::NST) & 1, abort_flag, p.hdr, 7);
+            ok = wwait(bar(C::B_KVF + ks2), (kv_it / C::NST) & 1, abort_flag, p.hdr, 7);
             if (!ok) break;
             ++kv_it;
             fence_after_sync();
             if (n + 1 < I.nb0) {
               issue_S(0, ks2);
               if (n + 1 == I.nb0 - 1) {
-                mma_commit(bar(C::B_QE + 0));
+                mma_commit_w(bar(C::B_QE + 0));
                 ++qcnt[0];
               }
             }
           }
           if (I.t1) {
-            ok = mbar_wait(bar(C::B_PF + 1), pf[1] & 1, abort_flag, p.hdr, 8);
+            ok = wwait(bar(C::B_PF + 1), pf[1] & 1, abort_flag, p.hdr, 8);
             if (!ok) break;
             ++pf[1];
             fence_after_sync();
             issue_PV(1, vs, n > 0);
           }
-          mma_commit(bar(C::B_KVE + vs));
+          mma_commit_w(bar(C::B_KVE + vs));
           if (ks2 >= 0) {
             if (I.t1) {
               issue_S(1, ks2);
               if (n + 1 == I.nb - 1) {
-                mma_commit(bar(C::B_QE + 1));
+                mma_commit_w(bar(C::B_QE + 1));
                 ++qcnt[1];
               }
             }
-            mma_commit(bar(C::B_KVE + ks2));
+            mma_commit_w(bar(C::B_KVE + ks2));
           }
         }
       }
       // every MMA this thread issued must finish before TMEM is released
-      mma_commit(bar(C::B_DR));
+      mma_commit_w(bar(C::B_DR));
       drain_wait(bar(C::B_DR), 0);
     }
   } else if (warp < 4) {

@@ -63,6 +63,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait run by a whole warp, with a warp-uniform result so the warp stays converged
+// for the elect.sync-issued instructions that follow.
+__device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile int* abort_flag, WsHeader* hdr,
+                                      int where) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, hdr, where));
+}
+
 // Warpgroup register re-balancing (all 4 warps of a warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
@@ -231,6 +238,35 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
       " mov.b64 db, {%2, %5};\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi)
+      : "memory");
+}
+
+// Warp-collective forms: every lane of the issuing warp executes them with the same
+// operands and one lane, chosen by elect.sync, issues the instruction.  Keeping the whole
+// warp on the issuing path lets the compiler hold the operands in uniform registers, which
+// issues MMAs markedly faster than a loop run by a single lane.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n .reg .b64 da, db;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %4, 0;\n mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n .reg .b64 db;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %4, 0;\n mov.b64 db, {%2, %5};\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHi)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
       : "memory");
 }
 
