@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
-    if (lane == 0) {
+    {  // the whole warp runs the loop; elect.sync picks the issuing lane
       int qit = 0, item_cnt = 0, kv_issued = 0;  // kv_issued: items whose K/V load went out
       bool ok = true;
       KvItem nxt;
@@ -170,23 +170,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // with it
       auto load_kv = [&](const KvItem& J, int j) -> bool {
         const int kb = j & 1;
-        if (!mbar_wait(bar(C::B_KVE + kb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
-        mbar_expect_tx(bar(C::B_KVF + kb), 2 * C::TKV);
+        if (!wwait(bar(C::B_KVE + kb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
+        mbar_expect_tx_w(bar(C::B_KVF + kb), 2 * C::TKV);
         for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, J.hk,
+          tma_load_3d_w(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, J.hk,
                       J.s0 + J.n * 128);
-          tma_load_3d(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
+          tma_load_3d_w(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
                       J.hk, J.s0 + J.n * 128);
         }
         kv_issued = j + 1;
         return true;
       };
-      bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
+      bool more = queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
                                 abort_flag, p.hdr, ok);
       if (ok && more) ok = load_kv(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const KvItem I = nxt;  // publish the next record first: its decode overlaps this one
-        more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items,
+        more = queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items,
                              dec, nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
         // the next item's K/V goes out right after this item's first two Q/dO steps, a whole
@@ -200,13 +200,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (i == I.steps) break;
           const int m = I.m_start + i / p.g, h = I.hk * p.g + i % p.g;
           const int s = qit % C::QST;
-          ok = mbar_wait(bar(C::B_QE + s), ((qit / C::QST) & 1) ^ 1, abort_flag, p.hdr, 22);
+          ok = wwait(bar(C::B_QE + s), ((qit / C::QST) & 1) ^ 1, abort_flag, p.hdr, 22);
           if (!ok) break;
-          mbar_expect_tx(bar(C::B_QF + s), 2 * C::TQ);
+          mbar_expect_tx_w(bar(C::B_QF + s), 2 * C::TQ);
           const uint32_t dst = base + C::RING_OFF + s * 2 * C::TQ;
           for (int pn = 0; pn < D / 64; ++pn) {
-            tma_load_3d(dst + pn * C::PQ, &tq, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
-            tma_load_3d(dst + C::TQ + pn * C::PQ, &tdo, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
+            tma_load_3d_w(dst + pn * C::PQ, &tq, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
+            tma_load_3d_w(dst + C::TQ + pn * C::PQ, &tdo, bar(C::B_QF + s), pn * 64, h, I.s0 + m * 64);
           }
           ++qit;
         }
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
-    if (lane == 0) {
+    {  // the whole warp runs the loop; elect.sync picks the issuing lane
       int kit = 0, item_cnt = 0, qd_issued = 0;  // qd_issued: items whose Q/dO load went out
       bool ok = true;
       QItem nxt;
@@ -566,23 +566,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // with it
       auto load_qd = [&](const QItem& J, int j) -> bool {
         const int qb = j & 1;
-        if (!mbar_wait(bar(C::B_QDE + qb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 31)) return false;
-        mbar_expect_tx(bar(C::B_QDF + qb), 2 * C::TQ);
+        if (!wwait(bar(C::B_QDE + qb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 31)) return false;
+        mbar_expect_tx_w(bar(C::B_QDF + qb), 2 * C::TQ);
         for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(base + C::qd_off(qb) + pn * C::PQ, &tq, bar(C::B_QDF + qb), pn * 64, J.h,
+          tma_load_3d_w(base + C::qd_off(qb) + pn * C::PQ, &tq, bar(C::B_QDF + qb), pn * 64, J.h,
                       J.s0 + J.m * 128);
-          tma_load_3d(base + C::qd_off(qb) + C::TQ + pn * C::PQ, &tdo, bar(C::B_QDF + qb), pn * 64, J.h,
+          tma_load_3d_w(base + C::qd_off(qb) + C::TQ + pn * C::PQ, &tdo, bar(C::B_QDF + qb), pn * 64, J.h,
                       J.s0 + J.m * 128);
         }
         qd_issued = j + 1;
         return true;
       };
-      bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
+      bool more = queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
                                 abort_flag, p.hdr, ok);
       if (ok && more) ok = load_qd(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const QItem I = nxt;  // publish the next record first: its decode overlaps this one
-        more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items,
+        more = queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items,
                              dec, nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
         // the next item's Q/dO goes out right after this item's first two K/V steps
@@ -594,13 +594,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (n == I.nb) break;
           const int s = kit % C::KST;
-          ok = mbar_wait(bar(C::B_KE + s), ((kit / C::KST) & 1) ^ 1, abort_flag, p.hdr, 32);
+          ok = wwait(bar(C::B_KE + s), ((kit / C::KST) & 1) ^ 1, abort_flag, p.hdr, 32);
           if (!ok) break;
-          mbar_expect_tx(bar(C::B_KF + s), 2 * C::TKV);
+          mbar_expect_tx_w(bar(C::B_KF + s), 2 * C::TKV);
           const uint32_t dst = base + C::RING_OFF + s * 2 * C::TKV;
           for (int pn = 0; pn < D / 64; ++pn) {
-            tma_load_3d(dst + pn * C::PKV, &tk, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
-            tma_load_3d(dst + C::TKV + pn * C::PKV, &tv, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
+            tma_load_3d_w(dst + pn * C::PKV, &tk, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
+            tma_load_3d_w(dst + C::TKV + pn * C::PKV, &tv, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
           }
           ++kit;
         }

@@ -10,7 +10,8 @@
 // lse = ln sum_j exp(scale q.k_j).
 //
 // CTA layout (384 threads, one CTA per SM, persistent over the tile map):
-//   warp 0      TMA producer: pulls work items from the map's counter and publishes them
+//   warp 0      TMA producer (whole warp, one elected lane issues): pulls work items from
+//               the map's counter and publishes them
 //               (sched.cuh); Q tiles once per item, K/V tiles into an NST-slot ring
 //   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues):
 //               S_t = Q_t K^T (SS), O_t += P_t V (TS, P in TMEM);
@@ -195,24 +196,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
-    if (lane == 0) {
+    {  // the whole warp runs the loop; elect.sync picks the issuing lane
       int kv_it = 0, item_cnt = 0, qcnt[2] = {0, 0};
       bool ok = true;
       Item nxt;
-      bool more = queue_publish(0, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items, dec, nxt,
+      bool more = queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items, dec, nxt,
                                 abort_flag, p.hdr, ok);
       for (; ok && more; ++item_cnt) {
         const Item I = nxt;  // publish the next record first: its decode overlaps this one
-        more = queue_publish(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items,
+        more = queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items,
                              dec, nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
         // Q tile t is released by the item's last S_t MMA (tile 0 one key tile before tile 1)
         for (int t = 0; ok && t < (I.t1 ? 2 : 1); ++t) {
-          ok = mbar_wait(bar(C::B_QE + t), (qcnt[t] & 1) ^ 1, abort_flag, p.hdr, 1);
+          ok = wwait(bar(C::B_QE + t), (qcnt[t] & 1) ^ 1, abort_flag, p.hdr, 1);
           if (!ok) break;
-          mbar_expect_tx(bar(C::B_QF + t), C::TILE);
+          mbar_expect_tx_w(bar(C::B_QF + t), C::TILE);
           for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(base + C::Q_OFF + t * C::TILE + pn * C::PANEL, &tq, bar(C::B_QF + t), pn * 64,
+            tma_load_3d_w(base + C::Q_OFF + t * C::TILE + pn * C::PANEL, &tq, bar(C::B_QF + t), pn * 64,
                         I.h, I.s0 + I.m * kTcBM + t * 128);
           ++qcnt[t];
         }
@@ -220,11 +221,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int n = 0; ok && n < I.nb; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
             const int s = kv_it % C::NST;
-            ok = mbar_wait(bar(C::B_KVE + s), ((kv_it / C::NST) & 1) ^ 1, abort_flag, p.hdr, 2);
+            ok = wwait(bar(C::B_KVE + s), ((kv_it / C::NST) & 1) ^ 1, abort_flag, p.hdr, 2);
             if (!ok) break;
-            mbar_expect_tx(bar(C::B_KVF + s), C::TILE);
+            mbar_expect_tx_w(bar(C::B_KVF + s), C::TILE);
             for (int pn = 0; pn < D / 64; ++pn)
-              tma_load_3d(base + C::KV_OFF + s * C::TILE + pn * C::PANEL, kv ? &tv : &tk,
+              tma_load_3d_w(base + C::KV_OFF + s * C::TILE + pn * C::PANEL, kv ? &tv : &tk,
                           bar(C::B_KVF + s), pn * 64, I.hk, I.s0 + n * kTcBN);
             ++kv_it;
           }

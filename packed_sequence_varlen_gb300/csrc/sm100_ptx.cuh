@@ -70,6 +70,23 @@ __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile in
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, hdr, where));
 }
 
+// Warp-collective forms of the producer's instructions (one elected lane issues).
+__device__ __forceinline__ void mbar_expect_tx_w(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+      " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                              int c2) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n"
+      " @e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5}], [%2];\n}\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // Warpgroup register re-balancing (all 4 warps of a warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
