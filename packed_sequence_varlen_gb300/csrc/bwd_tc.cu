@@ -61,7 +61,7 @@ struct KvCfg {
   // two K/V buffers (items alternate): buffer b holds K at KV_OFF(b), V right after
   static constexpr int RING_OFF = 4 * TKV;
   static constexpr int LDS = 4;                            // lse/D ring slots (one step each)
-  static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [LDS][lse*log2e 64 | D 64] fp32
+  static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [LDS][-lse*log2e 64 | -D 64] fp32
   static constexpr int BAR_OFF = LD_OFF + LDS * 2 * 64 * 4;
   static constexpr int B_KVF = 0, B_KVE = 2, B_QF = 4, B_QE = 4 + QST, B_SF = 4 + 2 * QST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
@@ -303,9 +303,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ lse / D loader
-    // For every step, in the order the softmax warpgroups take them: lse * log2(e) and
-    // D of the step's 64 q rows into a shared-memory ring (out-of-segment rows get
-    // +inf / 0, so their P is 0).
+    // For every step, in the order the softmax warpgroups take them: -lse * log2(e) and
+    // -D of the step's 64 q rows into a shared-memory ring, negated so the softmax only
+    // adds them (out-of-segment rows get -inf / 0, so their P is 0).
     regs_dec<kRegsCtl>();
     int g = 0;  // steps of this CTA so far
     bool ok = true;
@@ -325,8 +325,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int qr = m * 64 + c;
           const int64_t at = static_cast<int64_t>(h) * p.T + I.s0 + qr;
           const bool in = qr < I.l;
-          dst[c] = in ? p.lse[at] * kLog2e : INFINITY;
-          dst[64 + c] = in ? p.dsum[at] : 0.f;
+          dst[c] = in ? p.lse[at] * -kLog2e : -INFINITY;
+          dst[64 + c] = in ? -p.dsum[at] : 0.f;
         }
         mbar_arrive(bar(C::B_LF + slot));  // release: this lane's values are visible
       }
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t s_addr = tmem + lane_off + x * 64;
     const uint32_t dp_addr = tmem + lane_off + 128 + x * 64;
     const uint32_t acc_addr = tmem + lane_off + 256 + x * D;
-    const float* ldring = reinterpret_cast<const float*>(sm + C::LD_OFF);  // [slot][lse 64 | D 64]
+    const float* ldring = reinterpret_cast<const float*>(sm + C::LD_OFF);  // [slot][-lse2 64 | -D 64]
     const float sl2 = p.scale_log2;
     uint32_t sf = 0;
     int item_cnt = 0;
@@ -392,17 +392,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int j = c + e;
-            const float la = e ? l4.z : l4.x, lb = e ? l4.w : l4.y;
-            const float da = e ? d4.z : d4.x, db = e ? d4.w : d4.y;
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), sl2, sl2, -la, -lb);
+            const float la = e ? l4.z : l4.x, lb = e ? l4.w : l4.y;  // -lse * log2(e)
+            const float da = e ? d4.z : d4.x, db = e ? d4.w : d4.y;  // -D
+            // scalar FMAs: the packed forms measured slower here (operand pairing moves)
+            const float x0 = fmaf(__uint_as_float(sv[j]), sl2, la), x1 = fmaf(__uint_as_float(sv[j + 1]), sl2, lb);
             float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             if (need_mask) {
               if (j < lim) p0 = 0.f;
               if (j + 1 < lim) p1 = 0.f;
             }
-            float t0, t1;
-            fadd2(t0, t1, __uint_as_float(dpv[j]), __uint_as_float(dpv[j + 1]), -da, -db);
+            const float t0 = __uint_as_float(dpv[j]) + da, t1 = __uint_as_float(dpv[j + 1]) + db;
             sv[j >> 1] = pack_bf16(p0, p1);
             dpv[j >> 1] = pack_bf16(p0 * t0, p1 * t1);
           }
