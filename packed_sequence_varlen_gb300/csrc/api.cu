@@ -19,7 +19,7 @@ cudaError_t launch_plan(const PlanArgs&, cudaStream_t);
 cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, cudaStream_t);
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
-cudaError_t launch_bwd_rowsum(const BwdParams&, int, cudaStream_t);
+cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, cudaStream_t);
 cudaError_t launch_bwd_dkdv_tc(const BwdParams&, int, int, cudaStream_t);
 cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, cudaStream_t);
 void bwd_tc_tiles(int*, int*, int*, int*);
@@ -30,12 +30,12 @@ void set_error(const char* msg) { g_error = msg; }
 
 // ------------------------------------------------------------ launch accounting
 enum KernelId {
-  K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_ROWSUM, K_BWD_DKDV, K_BWD_DQ,
+  K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_PREP, K_BWD_DKDV, K_BWD_DQ,
   K_VALIDATE_PLAN, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan", "fwd",
-    "bwd_rowsum",          "bwd_dkdv",      "bwd_dq",        "validate_plan"};
+    "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan"};
 
 struct Profiler {
   std::vector<cudaEvent_t> start, stop;
@@ -334,10 +334,6 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
        &hdr->n_items[1], segoff, &hdr->counter[1]},
       {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, qmap, static_cast<int>(L.cap_q), &hdr->status,
        &hdr->n_items[2], segoff, &hdr->counter[2]}};
-  cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
-    return launch_validate_plan(pa, 2, s->T, s->max_seqlen, cs);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "bwd plan");
   BwdParams p{};
   p.q = static_cast<const bf16*>(q);
   p.k = static_cast<const bf16*>(k);
@@ -372,7 +368,8 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
-  e = launch(K_BWD_ROWSUM, cs, [&] { return launch_bwd_rowsum(p, s->d, cs); });
+  // one launch validates, plans both maps and computes D = rowsum(dO * O)
+  cudaError_t e = launch(K_BWD_PREP, cs, [&] { return launch_bwd_prep(p, pa, 2, s->T, s->max_seqlen, s->d, cs); });
   if (e == cudaSuccess)
     e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv_tc(p, s->d, static_cast<int>(L.cap_kv), cs); });
   if (e == cudaSuccess)

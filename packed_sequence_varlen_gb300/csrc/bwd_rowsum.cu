@@ -1,26 +1,29 @@
-// Backward preprocessing: D_i = dO_i . O_i for every (token, q head), fp32 [Hq, T].
-// It is the row term of dS_ij = P_ij (dP_ij - D_i) in the analytic gradient of the
-// forward ("Packing与 FlashAttention Varlen", section 5 names the training branch).
-// HBM-bound: 16-byte loads, several rows in flight per warp.
+// Backward preparation, one launch: D_i = dO_i . O_i for every (token, q head), fp32
+// [Hq, T] -- the row term of dS_ij = P_ij (dP_ij - D_i) in the analytic gradient of the
+// forward ("Packing与 FlashAttention Varlen", section 5 names the training branch) --
+// while one extra CTA validates cu_seqlens and builds the dK/dV and dQ tile maps
+// (plan_body.cuh).  D does not depend on the boundaries, so the two run side by side.
+// HBM-bound: 16-byte streaming loads, several rows in flight per warp.
 #include <algorithm>
 
 #include "attn_params.cuh"
+#include "plan_body.cuh"
 
 namespace va {
 
 // D[h, t] = sum_c dO[t,h,c] * O[t,h,c].  Each thread reads 8 consecutive elements of
 // O and dO (16-byte loads); D/8 lanes share a row and reduce with shuffles; each warp
 // keeps 4 row groups in flight per iteration.
+// Blocks 0..nblk-1 of the D computation.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_rowsum_kernel(const BwdParams p) {
+__device__ __forceinline__ void rowsum_body(const BwdParams& p, int blk, int nblk) {
   constexpr int LPR = D / 8;            // lanes per row
   constexpr int RPW = 32 / LPR;         // rows per warp per group
   constexpr int UNR = 4;                // row groups in flight
-  if (p.hdr->status != VA_OK) return;
   const int lane = threadIdx.x & 31, sub = lane % LPR, slot = lane / LPR;
   const int rows = p.T * p.Hq;  // < 2^31 for every shape the library accepts
-  const int warp0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  const int warp0 = static_cast<int>((blk * blockDim.x + threadIdx.x) >> 5);
+  const int nwarps = static_cast<int>((nblk * blockDim.x) >> 5);
   for (int r0 = warp0 * RPW * UNR; r0 < rows; r0 += nwarps * RPW * UNR) {
     uint4 a[UNR], b[UNR];
 #pragma unroll
@@ -29,8 +32,9 @@ __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const BwdParams p) {
       if (r < rows) {
         const int t = r / p.Hq, h = r - t * p.Hq;
         const int64_t off = static_cast<int64_t>(t) * p.o_rs + static_cast<int64_t>(h) * p.o_hs + sub * 8;
-        a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + off));
-        b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + off));
+        // streaming loads (evict-first): O and dO are read once here
+        a[u] = __ldcs(reinterpret_cast<const uint4*>(p.o + off));
+        b[u] = __ldcs(reinterpret_cast<const uint4*>(p.dout + off));
       } else {
         a[u] = b[u] = make_uint4(0, 0, 0, 0);
       }
@@ -56,14 +60,32 @@ __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const BwdParams p) {
   }
 }
 
-cudaError_t launch_bwd_rowsum(const BwdParams& p, int d, cudaStream_t st) {
+// Block 0 validates and plans (the status word it writes gates the attention kernels that
+// follow, not this launch); blocks 1.. compute D.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p, const PlanPair pp) {
+  __shared__ PlanSmem sh;
+  if (blockIdx.x == 0) {
+    validate_plan_body(pp, sh);
+    return;
+  }
+  rowsum_body<D>(p, blockIdx.x - 1, gridDim.x - 1);
+}
+
+cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps, int T, int max_seqlen, int d,
+                            cudaStream_t st) {
+  PlanPair pp{};
+  for (int i = 0; i < nmaps && i < 2; ++i) pp.map[i] = maps[i];
+  pp.nmaps = nmaps;
+  pp.T = T;
+  pp.max_seqlen = max_seqlen;
   const int64_t rows = static_cast<int64_t>(p.T) * p.Hq;
   const int rpb = (256 / 32) * (32 / (d / 8)) * 4;   // rows per block per iteration
-  const int rb = static_cast<int>(std::min<int64_t>(152 * 8, (rows + rpb - 1) / rpb));
-  if (rb <= 0) return cudaSuccess;
-  if (d == 64) bwd_rowsum_kernel<64><<<rb, 256, 0, st>>>(p);
-  else bwd_rowsum_kernel<128><<<rb, 256, 0, st>>>(p);
+  const int rb = static_cast<int>(std::min<int64_t>(152 * 16, (rows + rpb - 1) / rpb));
+  if (d == 64) bwd_prep_kernel<64><<<rb + 1, 256, 0, st>>>(p, pp);
+  else bwd_prep_kernel<128><<<rb + 1, 256, 0, st>>>(p, pp);
   return cudaGetLastError();
 }
+
 
 }  // namespace va
