@@ -465,8 +465,8 @@ struct QCfg {
   static constexpr int RING_OFF = 4 * TQ;
   static constexpr int BAR_OFF = RING_OFF + KST * 2 * TKV;
   static constexpr int B_QDF = 0, B_QDE = 2, B_KF = 4, B_KE = 4 + KST, B_SF = 4 + 2 * KST,
-                       B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
-                       B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;
+                       B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 2, B_DR = B_AE + 2,
+                       B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;  // AF/AE: per dQ buffer
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
   static constexpr int MISC_OFF = QUEUE_OFF + 2 * 32;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
@@ -529,8 +529,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::B_SF + x), 1);
       mbar_init(bar(C::B_PF + x), 128);
     }
-    mbar_init(bar(C::B_AF), 1);
-    mbar_init(bar(C::B_AE), 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_AF + b), 1);
+      mbar_init(bar(C::B_AE + b), 256);
+    }
     mbar_init(bar(C::B_DR), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_IF + b), 1);
@@ -664,15 +666,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           if (x) ++pf1;
           else ++pf0;
-          if (n == 0) {
-            ok = wwait(bar(C::B_AE), (item_cnt & 1) ^ 1, abort_flag, p.hdr, 36);
+          if (n == 0) {  // this item's dQ buffer must have been read out two items ago
+            ok = wwait(bar(C::B_AE + (item_cnt & 1)), ((item_cnt >> 1) & 1) ^ 1, abort_flag, p.hdr, 36);
             if (!ok) break;
           }
           fence_after_sync();
           const uint32_t km = ringM0 + ((s * 2 * C::TKV) >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::KB / 16; ++kk)
-            mma_ts_w(tmem + 256, tmem + 128 + x * 64 + kk * 8, km + kk * (2048 >> 4), idG,
+            mma_ts_w(tmem + 256 + (item_cnt & 1) * D, tmem + 128 + x * 64 + kk * 8, km + kk * (2048 >> 4), idG,
                       (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(bar(C::B_KE + s));
           if (n + 2 < I.nb) {
@@ -685,7 +687,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit_w(bar(C::B_AF));
+        mma_commit_w(bar(C::B_AF + (item_cnt & 1)));
         kit += I.nb;
       }
       mma_commit_w(bar(C::B_DR));
@@ -707,6 +709,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t sf = 0;
     int item_cnt = 0;
     bool ok = true;
+    // The dQ accumulator is double-buffered (item k uses buffer k & 1), so item k's
+    // epilogue waits until this warpgroup has handed in its first step of item k + 1:
+    // the tensor core starts the next item meanwhile.
+    int pend = -1;          // item whose epilogue is pending, or -1
+    bf16* pend_out = nullptr;
+    bool pend_store = false;
+    auto epilogue = [&]() -> bool {
+      const int k = pend;
+      pend = -1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_AF + (k & 1)), (k >> 1) & 1, abort_flag, p.hdr, 39)))
+        return false;
+      fence_after_sync();
+      constexpr int HC = D / 2;  // this warpgroup's columns [x HC, (x + 1) HC), one round trip
+      uint32_t o[HC];
+#pragma unroll
+      for (int c = 0; c < HC / 32; ++c) tmem_ld32(acc_addr + (k & 1) * D + x * HC + c * 32, o + c * 32);
+      tmem_wait_ld();
+      fence_before_sync();
+      mbar_arrive(bar(C::B_AE + (k & 1)));  // the buffer is free once its values are in registers
+#pragma unroll
+      for (int j = 0; j < HC / 2; ++j)
+        o[j] = pack_bf16(__uint_as_float(o[2 * j]) * p.scale, __uint_as_float(o[2 * j + 1]) * p.scale);
+      if constexpr (HC % 64 == 0) {
+        uint4 ov[HC / 8];
+#pragma unroll
+        for (int j = 0; j < HC / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        store_rows_coalesced(ov, pend_out + x * HC, p.o_rs, pend_store);
+      } else if (pend_store) {
+        uint4* dst = reinterpret_cast<uint4*>(pend_out + x * HC);
+#pragma unroll
+        for (int j = 0; j < HC / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+      }
+      return true;
+    };
     for (;; ++item_cnt) {
       QItem I;
       const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
@@ -761,42 +797,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_st();
         fence_before_sync();
         mbar_arrive(bar(C::B_PF + x));
+        if (pend >= 0 && !epilogue()) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
-      // epilogue: this warpgroup's half of the dQ columns
-      ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 39);
-      if (!__all_sync(0xffffffffu, ok)) {
+      if (pend >= 0 && !epilogue()) {  // this warpgroup had no step in the item
         ok = false;
         break;
       }
-      fence_after_sync();
-      const bool store = qrow < I.l;
-      bf16* out = p.dq + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
-      {
-        constexpr int HC = D / 2;  // this warpgroup's columns [x HC, (x + 1) HC), one round trip
-        uint32_t o[HC];
-#pragma unroll
-        for (int c = 0; c < HC / 32; ++c) tmem_ld32(acc_addr + x * HC + c * 32, o + c * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < HC / 2; ++j)
-          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * p.scale, __uint_as_float(o[2 * j + 1]) * p.scale);
-        if constexpr (HC % 64 == 0) {
-          uint4 ov[HC / 8];
-#pragma unroll
-          for (int j = 0; j < HC / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          store_rows_coalesced(ov, out + x * HC, p.o_rs, store);
-        } else if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(out + x * HC);
-#pragma unroll
-          for (int j = 0; j < HC / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
-      }
-      fence_before_sync();
-      mbar_arrive(bar(C::B_AE));
+      pend = item_cnt;
+      pend_out = p.dq + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
+      pend_store = qrow < I.l;
     }
+    if (ok && pend >= 0) ok = epilogue();
   }
-
   fence_before_sync();
   __syncthreads();
   if (warp == 1) {
