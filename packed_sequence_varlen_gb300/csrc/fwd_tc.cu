@@ -452,13 +452,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int j = 0; j < D / 2; ++j)
           o[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-        // direct row stores: here they drain while the warps move on to the next tile, which
-        // measured faster than the shuffle-coalesced stores the backward kernels use
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
+        uint4 ov[D / 8];
 #pragma unroll
-          for (int j = 0; j < D / 8; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
+        for (int j = 0; j < D / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        store_rows_coalesced(ov, orow, p.o_rs, store);
       }
       if (store)
         p.lse[static_cast<int64_t>(I.h) * p.T + I.s0 + qrow] = (m_ref + __log2f(lsum)) * kLn2;
