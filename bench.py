@@ -41,6 +41,21 @@ WORKLOAD = "sft8k"
 PACKS_PER_STEP = 16        # --packs changes it (small cases for profiling)
 
 
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu record, or None
+    when there is none or the kernel's source changed since it was captured."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_sft8k.json")
+    try:
+        rec = json.load(open(path))["kernels"][kernel]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha1(src).hexdigest() != rec["source_sha1"]:
+        return None
+    return rec["bytes"] if WORKLOAD == "sft8k" else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -249,7 +264,7 @@ def run_ours(args, rank, world, local_rank):
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": round(ach / peaks["bf16_tflops_sustained"], 4),
                 "peak_kind": f"bf16 sustained, {peaks['source']}",
-                "traffic": None,
+                "traffic": kernel_traffic(dom),
                 "launches": per_kernel[dom][1],
                 "avg_launch_us": round(per_kernel[dom][0] / per_kernel[dom][1] * 1e3, 2)}
     kernel_table = {k: {"launches": c, "total_ms": round(t, 3),
@@ -285,7 +300,9 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier):
     """Same step through the public API from pinned HOST buffers: H2D of every pack's q/k/v/dO
-    and lengths, the step, D2H of dq/dk/dv, all inside the timed region."""
+    and lengths, the step, D2H of dq/dk/dv, all inside the timed region.  Copies run on their
+    own streams with two device buffer sets, so pack p+1 uploads and pack p-1 downloads while
+    pack p computes (H2D and D2H use opposite link directions)."""
     import torch
     d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to
     host_in = []
@@ -294,31 +311,52 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier):
         host_in.append(tuple(x.pin_memory() for x in (q, k, v, do)))
     host_len = [torch.tensor(p, dtype=torch.int32).pin_memory() for p in packs]
     host_out = tuple(torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory() for H in (Hq, Hkv, Hkv))
-    dev_in = [torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv, Hq)]
-    lens_dev = torch.empty(max(len(p) for p in packs), dtype=torch.int32, device=dev)
+    nbuf = 2
+    dev_in = [[torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv, Hq)]
+              for _ in range(nbuf)]
+    lens_dev = [torch.empty(max(len(p) for p in packs), dtype=torch.int32, device=dev) for _ in range(nbuf)]
     o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
-    g = [torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv)]
+    g = [[torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv)] for _ in range(nbuf)]
     all_docs = [L for p in packs for L in p]
     h2d = sum(x.numel() * x.element_size() for t in host_in for x in t) + sum(x.numel() * 4 for x in host_len)
     d2h = len(packs) * sum(x.numel() * x.element_size() for x in host_out)
+    s_up, s_cmp, s_dn = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n = len(packs)
 
     def step():
         va.pack_next_fit(all_docs, w.capacity)
-        for p in range(len(packs)):
-            for dst, src in zip(dev_in, host_in[p]):
-                dst.copy_(src, non_blocking=True)
-            n = len(packs[p])
-            lens_dev[:n].copy_(host_len[p], non_blocking=True)
-            cu, _, _, mx, _ = va.build_metadata(lens_dev[:n], pad_to=T, T_capacity=T)
-            Bp = n + (1 if sum(packs[p]) < T else 0)
-            mxs = max(packs[p] + ([T - sum(packs[p])] if sum(packs[p]) < T else []))
-            cu = cu[:Bp + 1]
-            q, k, v, do = dev_in
-            va.varlen_attn_fwd(q, k, v, cu, mxs, None, True, out=o, lse=lse)
-            va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs, None, True, dq=g[0], dk=g[1], dv=g[2])
-            for dst, src in zip(host_out, g):
-                dst.copy_(src, non_blocking=True)
+        up = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        down = [torch.cuda.Event() for _ in range(n)]
+        for p in range(n):
+            b = p % nbuf
+            with torch.cuda.stream(s_up):
+                if p >= nbuf:
+                    s_up.wait_event(done[p - nbuf])  # buffer set b is free once pack p-2 computed
+                for dst, src in zip(dev_in[b], host_in[p]):
+                    dst.copy_(src, non_blocking=True)
+                lens_dev[b][:len(packs[p])].copy_(host_len[p], non_blocking=True)
+                up[p].record(s_up)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(up[p])
+                if p >= nbuf:
+                    s_cmp.wait_event(down[p - nbuf])  # gradient set b is free once downloaded
+                k_ = len(packs[p])
+                cu, _, _, _, _ = va.build_metadata(lens_dev[b][:k_], pad_to=T, T_capacity=T)
+                Bp = k_ + (1 if sum(packs[p]) < T else 0)
+                mxs = max(packs[p] + ([T - sum(packs[p])] if sum(packs[p]) < T else []))
+                cu = cu[:Bp + 1]
+                q, k, v, do = dev_in[b]
+                va.varlen_attn_fwd(q, k, v, cu, mxs, None, True, out=o, lse=lse)
+                va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs, None, True, dq=g[b][0], dk=g[b][1], dv=g[b][2])
+                done[p].record(s_cmp)
+            with torch.cuda.stream(s_dn):
+                s_dn.wait_event(done[p])
+                for dst, src in zip(host_out, g[b]):
+                    dst.copy_(src, non_blocking=True)
+                down[p].record(s_dn)
+        torch.cuda.current_stream(dev).wait_stream(s_dn)
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -334,7 +372,8 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier):
         dt = float(t.item())
     world = dist.get_world_size() if dist is not None else 1
     return {"value": round(step_flops * args.steps * world / dt / 1e12, 3), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "overlap": "H2D, compute and D2H on three streams, two device buffer sets"}
 
 
 # ------------------------------------------------------------------ oracle timing
