@@ -65,6 +65,7 @@ __device__ __forceinline__ void rowsum_body(const BwdParams& p, int blk, int nbl
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p, const PlanPair pp) {
   __shared__ PlanSmem sh;
+  griddep_begin();  // O comes from the forward, and the workspace may be the forward's
   if (blockIdx.x == 0) {
     validate_plan_body(pp, sh);
     return;
@@ -82,9 +83,8 @@ cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps,
   const int64_t rows = static_cast<int64_t>(p.T) * p.Hq;
   const int rpb = (256 / 32) * (32 / (d / 8)) * 4;   // rows per block per iteration
   const int rb = static_cast<int>(std::min<int64_t>(152 * 16, (rows + rpb - 1) / rpb));
-  if (d == 64) bwd_prep_kernel<64><<<rb + 1, 256, 0, st>>>(p, pp);
-  else bwd_prep_kernel<128><<<rb + 1, 256, 0, st>>>(p, pp);
-  return cudaGetLastError();
+  if (d == 64) return launch_pdl(bwd_prep_kernel<64>, dim3(rb + 1), dim3(256), 0, st, p, pp);
+  return launch_pdl(bwd_prep_kernel<128>, dim3(rb + 1), dim3(256), 0, st, p, pp);
 }
 
 

@@ -116,8 +116,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // Launched as a programmatic dependent of the preparation kernel: its maps, D and status
   // are read only after the wait.  The dQ kernel, which reads the same products but none
   // of this kernel's, may then start on SMs as this kernel's CTAs finish.
-  griddep_wait();
-  griddep_launch_dependents();
+  griddep_begin();
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.kv_slot];
   if (static_cast<int>(blockIdx.x) >= n_items) return;
@@ -828,25 +827,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-// Launch with programmatic stream serialization: the kernel may be scheduled while the
-// previous kernel in the stream is still running; it orders itself with griddep_wait().
-template <class K>
-static cudaError_t launch_pdl(K kernel, int grid, int smem, cudaStream_t st, const CUtensorMap& tq,
-                              const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                              const BwdParams& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kBwdThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, p);
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
 
 template <int D>
 static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
@@ -869,7 +849,7 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dkdv_tc_kernel<D>, grid, C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dkdv_tc_kernel<D>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
 template <int D>
@@ -893,7 +873,7 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dq_tc_kernel<D>, grid, C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dq_tc_kernel<D>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
 cudaError_t launch_bwd_dkdv_tc(const BwdParams& p, int d, int cap, cudaStream_t st) {

@@ -161,4 +161,37 @@ __device__ __forceinline__ void store_rows_coalesced(uint4 (&a)[W], T* row, int6
   }
 }
 
+// Programmatic dependent launch.  Every kernel of the library starts with griddep_begin():
+// it waits until the grids it depends on have completed and their writes are visible
+// (at once when launched without the attribute), then lets the next grid in the stream
+// be scheduled.  That next grid's CTAs take SMs only after all of this grid's CTAs have
+// started, and wait in their own griddep_begin(), so launch latency and prologues overlap
+// the previous kernel without any read or write reordering.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_begin() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
+// Launches `kernel` with programmatic stream serialization allowed (see griddep_begin).
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace va

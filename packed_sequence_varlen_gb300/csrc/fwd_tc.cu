@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
   auto dec = [&](int idx) { return decode(p, idx); };
 
+  griddep_begin();  // the tile map and status come from the planning launch just before
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.slot];
   if (static_cast<int>(blockIdx.x) >= n_items) return;
@@ -492,8 +493,7 @@ static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  fwd_tc_kernel<D><<<grid, kTcThreads, C::SMEM, st>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(fwd_tc_kernel<D>, dim3(grid), dim3(kTcThreads), C::SMEM, st, tq, tk, tv, p);
 }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, int cap, cudaStream_t st) {

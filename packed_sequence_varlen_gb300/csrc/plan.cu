@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 // word (OK or VA_ERR_BAD_SEQLENS), and only if it holds builds the call's maps.
 __global__ void __launch_bounds__(kPlanThreads) validate_plan_kernel(PlanPair pp) {
   __shared__ PlanSmem sh;
+  griddep_begin();  // cu_seqlens may come from the metadata kernels just before
   validate_plan_body(pp, sh);
 }
 
@@ -35,8 +36,7 @@ cudaError_t launch_validate_plan(const PlanArgs* maps, int nmaps, int T, int max
   pp.nmaps = nmaps;
   pp.T = T;
   pp.max_seqlen = max_seqlen;
-  validate_plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
-  return cudaGetLastError();
+  return launch_pdl(validate_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp);
 }
 
 }  // namespace va

@@ -87,12 +87,6 @@ __device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const CUtensorMap* m
       : "memory");
 }
 
-// Programmatic dependent launch: wait until the grids this one depends on have completed
-// and their writes are visible (returns at once when launched without the attribute), and
-// let the grids that depend on this one be scheduled.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 // Warpgroup register re-balancing (all 4 warps of a warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
