@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kScanThreads)
                          int32_t* __restrict__ status) {
   __shared__ int warp_sums[32];
   __shared__ int carry, mx, bad;
+  griddep_begin();  // the lengths may come from the kernel just before
   if (threadIdx.x == 0) {
     carry = 0;
     mx = 0;
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(kScanThreads)
 __global__ void metadata_fill_kernel(const int32_t* __restrict__ cu, int n, int T_capacity,
                                      int32_t* __restrict__ pos, int32_t* __restrict__ seg,
                                      const int32_t* __restrict__ status) {
+  griddep_begin();  // cu and the status word come from the scan just before
   if (*status != VA_OK) return;
   const int T = cu[n + 1];
   const int nseg = (cu[n + 1] > cu[n]) ? n + 1 : n;
@@ -100,6 +102,7 @@ __global__ void metadata_fill_kernel(const int32_t* __restrict__ cu, int n, int 
 __global__ void __launch_bounds__(kScanThreads)
     validate_cu_kernel(const int32_t* __restrict__ cu, int B, int T, int max_seqlen,
                        int32_t* __restrict__ status, int overwrite) {
+  griddep_begin();
   int bad = 0;
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int a = cu[b], c = cu[b + 1];
@@ -115,22 +118,20 @@ __global__ void __launch_bounds__(kScanThreads)
 
 cudaError_t launch_metadata_scan(const int32_t* lengths, int n, int pad_to, int T_capacity,
                                  int32_t* cu, int32_t* max_out, int32_t* status, cudaStream_t st) {
-  metadata_scan_kernel<<<1, kScanThreads, 0, st>>>(lengths, n, pad_to, T_capacity, cu, max_out,
-                                                    status);
-  return cudaGetLastError();
+  return launch_pdl(metadata_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, lengths, n, pad_to, T_capacity, cu,
+                    max_out, status);
 }
 
 cudaError_t launch_metadata_fill(const int32_t* cu, int n, int T_capacity, int32_t* pos,
                                  int32_t* seg, const int32_t* status, cudaStream_t st) {
   const int blocks = min(1216, max(1, (T_capacity + 255) / 256));
-  metadata_fill_kernel<<<blocks, 256, 0, st>>>(cu, n, T_capacity, pos, seg, status);
-  return cudaGetLastError();
+  return launch_pdl(metadata_fill_kernel, dim3(blocks), dim3(256), 0, st, cu, n, T_capacity, pos, seg, status);
 }
 
 cudaError_t launch_validate(const int32_t* cu, int B, int T, int max_seqlen, int32_t* status,
                             int overwrite, cudaStream_t st) {
-  validate_cu_kernel<<<1, kScanThreads, 0, st>>>(cu, B, T, max_seqlen, status, overwrite);
-  return cudaGetLastError();
+  return launch_pdl(validate_cu_kernel, dim3(1), dim3(kScanThreads), 0, st, cu, B, T, max_seqlen, status,
+                    overwrite);
 }
 
 }  // namespace va
