@@ -70,6 +70,23 @@ __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile in
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, hdr, where));
 }
 
+// Shared -> global tile store through a tensor map, tracked by the issuing thread's bulk
+// groups.  The writers of the tile fence (fence_proxy_async_smem) and synchronise first.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Returns once every committed store of this thread has finished reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Returns once every committed store of this thread has completed.
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Warp-collective forms of the producer's instructions (one elected lane issues).
 __device__ __forceinline__ void mbar_expect_tx_w(uint32_t bar, uint32_t bytes) {
   asm volatile(
