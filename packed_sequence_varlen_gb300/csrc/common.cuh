@@ -161,6 +161,60 @@ __device__ __forceinline__ void store_rows_coalesced(uint4 (&a)[W], T* row, int6
   }
 }
 
+// Same contract as store_rows_coalesced, with 32-byte stores: within each group of 4 lanes
+// a 4 x 4 transpose of 32-byte chunks (two xor-shuffle stages) leaves lane j with chunk j
+// of each of the group's 4 rows, and every store instruction writes 128 contiguous bytes
+// per group with half the instructions.
+template <int W, class T>
+__device__ __forceinline__ void store_rows_coalesced32(uint4 (&a)[W], T* row, int64_t stride, bool valid) {
+  static_assert(W % 8 == 0, "rows must be a multiple of 128 bytes");
+  const int lane = threadIdx.x & 31, j = lane & 3;
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+  for (int b = 0; b < W / 8; ++b) {
+    uint4* c = a + 8 * b;  // four 32-byte chunks: (c[0], c[1]), (c[2], c[3]), ...
+#pragma unroll
+    for (int d = 2; d >= 1; d >>= 1) {
+      const bool hi = (j & d) != 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i & d) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 send = hi ? c[2 * i + h] : c[2 * (i + d) + h];
+          uint4 recv;
+          recv.x = __shfl_xor_sync(0xffffffffu, send.x, d);
+          recv.y = __shfl_xor_sync(0xffffffffu, send.y, d);
+          recv.z = __shfl_xor_sync(0xffffffffu, send.z, d);
+          recv.w = __shfl_xor_sync(0xffffffffu, send.w, d);
+          if (hi) c[2 * i + h] = recv;
+          else c[2 * (i + d) + h] = recv;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if ((vmask >> ((lane & ~3) + k)) & 1u) {
+        char* dst = reinterpret_cast<char*>(row + static_cast<int64_t>(k - j) * stride) + 128 * b + 32 * j;
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(c[2 * k].x),
+                     "r"(c[2 * k].y), "r"(c[2 * k].z), "r"(c[2 * k].w), "r"(c[2 * k + 1].x), "r"(c[2 * k + 1].y),
+                     "r"(c[2 * k + 1].z), "r"(c[2 * k + 1].w)
+                     : "memory");
+      }
+    }
+  }
+}
+
+// store_rows_coalesced32 when every row of the warp starts on a 32-byte boundary (the
+// 256-bit stores need it), store_rows_coalesced otherwise.
+template <int W, class T>
+__device__ __forceinline__ void store_rows_fast(uint4 (&a)[W], T* row, int64_t stride, bool valid) {
+  if (__all_sync(0xffffffffu, (reinterpret_cast<uintptr_t>(row) & 31u) == 0))
+    store_rows_coalesced32(a, row, stride, valid);
+  else
+    store_rows_coalesced(a, row, stride, valid);
+}
+
 // Programmatic dependent launch.  Every kernel of the library starts with griddep_begin():
 // it waits until the grids it depends on have completed and their writes are visible
 // (at once when launched without the attribute), then lets the next grid in the stream
