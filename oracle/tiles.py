@@ -25,6 +25,19 @@ The backward map lists kv blocks: for kv block n of BN rows the q blocks of BM
 rows run from m_start = floor(n * BN / BM) (causal; 0 otherwise) to
 ceil(l / BM) - 1; with C_b = sum over kv blocks of n_q its order is
 (-class_b, b, h_kv, -n_q, n).
+
+Token tiles (forward, causal, ``short > 0``).  A segment of l <= short tokens
+would fill a q block of BM rows only l rows deep.  Maximal runs of consecutive
+short segments are instead cut into row tiles of BM consecutive tokens that
+may hold many segments; row i of such a tile sees the keys
+[segment_start(i), i] -- the permission rule of "Pack sequences without joining
+their contexts" ("Permission depends on the example": same segment and key not
+later than the query) in its range form ("What the permission symbols mean").
+A run [r0, r1) gives the tiles t0 = r0, r0 + BM, ... with rows = min(BM, r1 - t0)
+rows; the keys a tile needs are [cu[f], t0 + rows) where f is the segment that
+holds row t0.  Its record is (-1 - f, t0, h, rows), and the token records follow
+every segment record, ordered by (t0, h).  Segments covered by token tiles have
+no segment records.
 """
 from __future__ import annotations
 
@@ -39,11 +52,16 @@ def _cost_class(c: int) -> int:
     return c.bit_length() - 1          # floor(log2(c)) for c >= 1
 
 
-def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True):
-    """Items (b, m, h, n_blocks) as an int32 array [N, 4], in the order above."""
+def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, short: int = 0):
+    """Items as an int32 array [N, 4], in the order above: segment records
+    (b, m, h, n_blocks), then (causal, short > 0) token records (-1 - f, t0, h, rows)."""
     cu = [int(x) for x in cu_seqlens]
+    B = len(cu) - 1
+    tok = [causal and short > 0 and cu[b + 1] - cu[b] <= short for b in range(B)]
     items = []
-    for b in range(len(cu) - 1):
+    for b in range(B):
+        if tok[b]:
+            continue
         l = cu[b + 1] - cu[b]
         blocks = []
         for m in range(_ceil(l, BM)):
@@ -54,7 +72,22 @@ def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True):
             for m, nb in blocks:
                 items.append(((-cls, b, h, -nb, m), (b, m, h, nb)))
     items.sort(key=lambda t: t[0])
-    return np.asarray([r for _, r in items], dtype=np.int32).reshape(-1, 4)
+    out = [r for _, r in items]
+    b = 0
+    while b < B:
+        if not tok[b]:
+            b += 1
+            continue
+        e = b
+        while e < B and tok[e]:
+            e += 1
+        r0, r1 = cu[b], cu[e]                     # one run of short segments
+        for t0 in range(r0, r1, BM):
+            f = max(x for x in range(b, e) if cu[x] <= t0)
+            for h in range(Hq):
+                out.append((-1 - f, t0, h, min(BM, r1 - t0)))
+        b = e
+    return np.asarray(out, dtype=np.int32).reshape(-1, 4)
 
 
 def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True):
@@ -79,8 +112,18 @@ def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True):
 def fwd_item_edges(cu_seqlens, item, BM: int, BN: int):
     """(query, key) token pairs a forward item's tiles cover, in global indices."""
     b, m, _h, nb = (int(x) for x in item)
+    if b < 0:                                     # token record (-1 - f, t0, h, rows)
+        t0, rows = m, nb
+        kb = int(cu_seqlens[-1 - b])
+        return [(i, j) for i in range(t0, t0 + rows) for j in range(kb, t0 + rows)]
     s = int(cu_seqlens[b])
     l = int(cu_seqlens[b + 1]) - s
     rows = range(s + m * BM, s + min(l, (m + 1) * BM))
     cols = range(s, s + min(l, nb * BN))
     return [(i, j) for i in rows for j in cols]
+
+
+def token_item_key_blocks(cu_seqlens, item, BN: int):
+    """Key blocks of BN columns from cu[f] that a token record's rows need."""
+    f, t0, _h, rows = (int(x) for x in item)
+    return _ceil(t0 + rows - int(cu_seqlens[-1 - f]), BN)

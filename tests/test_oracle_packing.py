@@ -171,13 +171,19 @@ def _allowed_edges(cu):
 
 @pytest.mark.parametrize("BM,BN", [(2, 2), (4, 2), (2, 4), (128, 128), (256, 128)])
 @pytest.mark.parametrize("seed", range(4))
-def test_fwd_tile_map_covers_each_allowed_edge_once(BM, BN, seed):
-    """Course 'History': tile traversal visits the same permitted edges as query order."""
+@pytest.mark.parametrize("short_div", [0, 2, 1])
+def test_fwd_tile_map_covers_each_allowed_edge_once(BM, BN, seed, short_div):
+    """Course 'History': tile traversal visits the same permitted edges as query order.
+
+    short_div > 0 turns on token tiles for segments of at most BN / short_div tokens."""
     rng = np.random.default_rng(seed)
+    short = BN // short_div if short_div else 0
     lengths = rng.integers(1, 3 * max(BM, BN) // 2 + 2, size=5).tolist()
+    if short:  # a run of short segments in the middle and one at the end
+        lengths = lengths[:2] + rng.integers(1, short + 1, size=7).tolist() + lengths[2:] + [short, 1]
     cu, _, _, _ = op.build_metadata(lengths)
     H = 2
-    tm = ot.fwd_tile_map(cu, H, BM, BN)
+    tm = ot.fwd_tile_map(cu, H, BM, BN, True, short)
     allowed = _allowed_edges(cu.tolist())
     for h in range(H):
         seen = []
@@ -186,22 +192,58 @@ def test_fwd_tile_map_covers_each_allowed_edge_once(BM, BN, seed):
             hit = [e for e in cover if e in allowed]
             assert hit, "a listed tile has no permitted edge"
             seen.extend(hit)
-            b, m, _, nb = it
+            b, m, _, nb = (int(x) for x in it)
+            if b < 0:      # token tile: rows [t0, t0 + rows) of short segments
+                t0, rows = m, nb
+                assert 1 <= rows <= BM
+                assert all(cu[x + 1] - cu[x] <= short for x in range(len(cu) - 1)
+                           if cu[x] < t0 + rows and cu[x + 1] > t0)
+                assert cu[-1 - b] <= t0 < cu[-b]          # f holds row t0
+                continue
             s, l = cu[b], cu[b + 1] - cu[b]
+            assert l > short
             last_row = s + min(l, (m + 1) * BM) - 1
             assert (last_row, s + (nb - 1) * BN) in allowed      # last kv tile is needed
         assert sorted(seen) == sorted(allowed)                  # each edge exactly once
+    seg = tm[tm[:, 0] >= 0]
+    tok = tm[tm[:, 0] < 0]
+    assert np.array_equal(tm, np.concatenate([seg, tok]))     # token records come last
     # order: segments by cost class (floor log2 of their total key tiles), then head,
     # then most key tiles first
     cost = {}
-    for b, m, h, nb in tm:
+    for b, m, h, nb in seg:
         if h == 0:
             cost[int(b)] = cost.get(int(b), 0) + int(nb)
-    keys = [(-(cost[int(r[0])].bit_length() - 1), r[0], r[2], -r[3], r[1]) for r in tm]
+    keys = [(-(cost[int(r[0])].bit_length() - 1), r[0], r[2], -r[3], r[1]) for r in seg]
     assert keys == sorted(keys)
     # records of one (segment, head) are contiguous
-    groups = [(r[0], r[2]) for r in tm]
+    groups = [(r[0], r[2]) for r in seg]
     assert len(set(groups)) == len([g for i, g in enumerate(groups) if i == 0 or g != groups[i - 1]])
+    # token records by (first row, head), every head of a tile
+    tkeys = [(r[1], r[2]) for r in tok]
+    assert tkeys == sorted(tkeys) and len(tok) % H == 0
+
+
+def test_token_tile_map_hand_example():
+    """Lengths 3, 2, 1, 300, 4, 60 with BM=256, BN=128, short=64, one head, worked by hand.
+
+    Segments 0-2 form the run [0, 6) (one tile of 6 rows, first segment 0); segment 3
+    (300 tokens) keeps its q blocks m=1 (3 key blocks) and m=0 (2 key blocks); segments
+    4-5 form the run [306, 370) (one tile of 64 rows starting in segment 4)."""
+    cu, _, _, _ = op.build_metadata([3, 2, 1, 300, 4, 60])
+    tm = ot.fwd_tile_map(cu, 1, 256, 128, True, 64)
+    assert tm.tolist() == [[3, 1, 0, 3], [3, 0, 0, 2], [-1, 0, 0, 6], [-5, 306, 0, 64]]
+    assert ot.token_item_key_blocks(cu, tm[2], 128) == 1
+    assert ot.token_item_key_blocks(cu, tm[3], 128) == 1
+    # a run longer than one tile, cut at 256 rows; the second tile starts inside a segment
+    lengths = [40] * 10
+    cu, _, _, _ = op.build_metadata(lengths)
+    tm = ot.fwd_tile_map(cu, 2, 256, 128, True, 64)
+    assert tm.tolist() == [[-1, 0, 0, 256], [-1, 0, 1, 256], [-7, 256, 0, 144], [-7, 256, 1, 144]]
+    assert ot.token_item_key_blocks(cu, tm[2], 128) == 2   # keys [240, 400)
+    # non-causal calls and short = 0 keep segment records only
+    assert (ot.fwd_tile_map(cu, 1, 256, 128, False, 64)[:, 0] >= 0).all()
+    assert (ot.fwd_tile_map(cu, 1, 256, 128, True, 0)[:, 0] >= 0).all()
 
 
 @pytest.mark.parametrize("BM,BN", [(2, 2), (2, 4), (4, 2), (128, 128), (64, 128)])
