@@ -18,7 +18,9 @@ cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaSt
 cudaError_t launch_plan(const PlanArgs&, cudaStream_t);
 cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, cudaStream_t);
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
+cudaError_t launch_fwd_tok(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
+int fwd_tc_token_short();
 cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, cudaStream_t);
 cudaError_t launch_bwd_dkdv_tc(const BwdParams&, int, int, cudaStream_t);
 cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, cudaStream_t);
@@ -31,11 +33,11 @@ void set_error(const char* msg) { g_error = msg; }
 // ------------------------------------------------------------ launch accounting
 enum KernelId {
   K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_PREP, K_BWD_DKDV, K_BWD_DQ,
-  K_VALIDATE_PLAN, K_COUNT
+  K_VALIDATE_PLAN, K_FWD_TOK, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
-    "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan", "fwd",
-    "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan"};
+    "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan",          "fwd",
+    "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan", "fwd_tok"};
 
 struct Profiler {
   std::vector<cudaEvent_t> start, stop;
@@ -235,7 +237,7 @@ va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kin
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const PlanArgs pa{cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
                     reinterpret_cast<TileItem*>(map_dev), capacity, nullptr, n_items_dev,
-                    scratch_dev + 4, scratch_dev};
+                    scratch_dev + 4, scratch_dev, kind == 0 && causal ? fwd_tc_token_short() : 0};
   cudaError_t e = launch(K_PLAN, cs, [&] { return launch_plan(pa, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "plan");
 }
@@ -266,7 +268,9 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   tiles(0, &BM, &BN);
   const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map, static_cast<int>(L.cap),
                     &hdr->status, &hdr->n_items[0],
-                    reinterpret_cast<int32_t*>(w + L.segoff), &hdr->counter[0]};
+                    reinterpret_cast<int32_t*>(w + L.segoff), &hdr->counter[0],
+                    causal ? fwd_tc_token_short() : 0, &hdr->n_items[kTokSlot],
+                    &hdr->counter[kTokSlot]};
   cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
     return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cs);
   });
@@ -279,6 +283,7 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   p.lse = lse;
   p.cu = cu;
   p.items = map;
+  p.B = s->B;
   p.hdr = hdr;
   p.slot = 0;
   p.counter = &hdr->counter[0];
@@ -296,8 +301,13 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   p.o_hs = s->o_head_stride;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
+  // segment records, then (as its programmatic dependent, filling its tail) token records
   e = launch(K_FWD, cs, [&] { return launch_fwd_tc(p, s->d, static_cast<int>(L.cap), cs); });
-  return e == cudaSuccess ? VA_OK : cuda_fail(e, "fwd kernel");
+  if (e != cudaSuccess) return cuda_fail(e, "fwd kernel");
+  FwdParams pt = p;
+  pt.counter = &hdr->counter[kTokSlot];
+  e = launch(K_FWD_TOK, cs, [&] { return launch_fwd_tok(pt, s->d, static_cast<int>(L.cap), cs); });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "fwd token kernel");
 }
 
 va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const void* out,

@@ -14,6 +14,7 @@ struct FwdParams {
   float* lse;  // [Hq, T]
   const int32_t* cu;
   const TileItem* items;
+  int B;  // segments (cu has B + 1 entries)
   WsHeader* hdr;
   int slot;
   int32_t* counter;  // work counter (records are pulled in list order)

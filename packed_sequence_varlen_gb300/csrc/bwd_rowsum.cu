@@ -60,10 +60,12 @@ __device__ __forceinline__ void rowsum_body(const BwdParams& p, int blk, int nbl
   }
 }
 
+constexpr int kPrepThreads = 1024;
+
 // Block 0 validates and plans (the status word it writes gates the attention kernels that
 // follow, not this launch); blocks 1.. compute D.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p, const PlanPair pp) {
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const BwdParams p, const PlanPair pp) {
   __shared__ PlanSmem sh;
   griddep_begin();  // O comes from the forward, and the workspace may be the forward's
   if (blockIdx.x == 0) {
@@ -81,10 +83,10 @@ cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps,
   pp.T = T;
   pp.max_seqlen = max_seqlen;
   const int64_t rows = static_cast<int64_t>(p.T) * p.Hq;
-  const int rpb = (256 / 32) * (32 / (d / 8)) * 4;   // rows per block per iteration
-  const int rb = static_cast<int>(std::min<int64_t>(152 * 16, (rows + rpb - 1) / rpb));
-  if (d == 64) return launch_pdl(bwd_prep_kernel<64>, dim3(rb + 1), dim3(256), 0, st, p, pp);
-  return launch_pdl(bwd_prep_kernel<128>, dim3(rb + 1), dim3(256), 0, st, p, pp);
+  const int rpb = (kPrepThreads / 32) * (32 / (d / 8)) * 4;   // rows per block per iteration
+  const int rb = static_cast<int>(std::min<int64_t>(152 * 4, (rows + rpb - 1) / rpb));
+  if (d == 64) return launch_pdl(bwd_prep_kernel<64>, dim3(rb + 1), dim3(kPrepThreads), 0, st, p, pp);
+  return launch_pdl(bwd_prep_kernel<128>, dim3(rb + 1), dim3(kPrepThreads), 0, st, p, pp);
 }
 
 

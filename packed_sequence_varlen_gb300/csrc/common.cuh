@@ -13,6 +13,10 @@ namespace va {
 //   int32 n_items[4]  -- record counts written by the plan kernels
 //   int32 where       -- diagnostic (which wait gave up)
 //   int32 counter[4]  -- work counters the attention kernels pull records from
+// Forward workspaces: n_items[0] counts all records of the map, n_items[kTokSlot] the
+// token records at its end; counter[kTokSlot] is the token kernel's work counter.
+constexpr int kTokSlot = 3;
+
 struct WsHeader {
   int32_t status;
   int32_t n_items[4];
@@ -40,6 +44,10 @@ struct PlanArgs {
   int32_t* n_items;  // out
   int32_t* seg_off;  // scratch [B]: first record of each segment
   int32_t* counter;  // work counter the attention kernel pulls items from; zeroed here
+  int short_len;      // kind 0, causal: segments of at most this many tokens go into token
+                      // tiles (records {-1 - f, t0, head, rows}); 0 = off
+  int32_t* n_tok;     // may be null: out, the number of token records (the map's last ones)
+  int32_t* tok_counter;  // may be null: the token kernel's work counter; zeroed here
 };
 
 __device__ __forceinline__ void set_status(WsHeader* h, int code) {

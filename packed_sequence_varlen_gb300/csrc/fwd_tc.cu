@@ -7,7 +7,8 @@
 // blocks run to ceil(min(l, (m+1)*256)/128) (causal) and the causal mask is
 // applied only on the one key block that crosses each 128-row tile's diagonal.
 // O is written at Q's offsets, rows past l are never stored, and
-// lse = ln sum_j exp(scale q.k_j).
+// lse = ln sum_j exp(scale q.k_j).  Runs of short segments are planned as token tiles and
+// computed by fwd_tok.cu's kernel, launched right after this one.
 //
 // CTA layout (384 threads, one CTA per SM, persistent over the tile map):
 //   warp 0      TMA producer (whole warp, one elected lane issues): pulls work items from
@@ -36,6 +37,7 @@ namespace {
 
 constexpr int kTcBM = 256;  // q rows per work item (two 128-row tiles)
 constexpr int kTcBN = 128;  // key rows per K/V tile
+static_assert((kTcBM & (kTcBM - 1)) == 0 && (kTcBN & (kTcBN - 1)) == 0, "the planner takes powers of two");
 constexpr int kTcThreads = 384;
 // setmaxnreg moves registers within what the CTA was launched with (168 per thread for
 // 384 threads); a split above that total would make the increase wait forever.
@@ -152,7 +154,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   griddep_begin();  // the tile map and status come from the planning launch just before
   if (p.hdr->status != VA_OK) return;
-  const int n_items = p.hdr->n_items[p.slot];
+  // segment records only: the token records at the map's end go to fwd_tok.cu's kernel
+  const int n_items = p.hdr->n_items[p.slot] - p.hdr->n_items[kTokSlot];
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (threadIdx.x == 0) {

@@ -95,8 +95,8 @@ def test_tile_maps_bit_exact(va, name, causal):
             tm, n = va.plan(cud, T, w.Hq, w.Hkv, w.d, mx, kind, causal)
             if kind == 1:
                 ref = ot.bwd_tile_map(cu, w.Hkv, BM, BN, causal)
-            else:
-                ref = ot.fwd_tile_map(cu, w.Hq, BM, BN, causal)
+            else:  # the forward map puts segments of at most BN/2 tokens in token tiles
+                ref = ot.fwd_tile_map(cu, w.Hq, BM, BN, causal, BN // 2 if kind == 0 else 0)
             assert n == len(ref)
             assert np.array_equal(tm.cpu().numpy(), ref)
 
@@ -214,6 +214,32 @@ def test_tiny4k_full(va):
     ro, rl, rg = run_oracle(q, k, v, do, cu)
     wl.assert_close_outputs(o, lse, ro, rl)
     wl.assert_close_grads(g, rg)
+
+
+# Runs of short segments: one of 300 single-token segments (more than 32 segment starts in
+# one token tile), runs cut at 256 rows inside a segment, a short segment alone between long
+# ones, 64 (the longest token-tiled length) next to 65, and a run that ends the stream.
+TOKEN_RUNS = [1] * 300 + [200] + [64] * 5 + [65, 3, 64, 1, 17, 700] + [33] * 20 + [2]
+
+
+@pytest.mark.parametrize("d,g", [(64, 1), (128, 2)])
+def test_token_tiles_mixed_runs(va, d, g):
+    cu, _, _, mx = op.build_metadata(TOKEN_RUNS)
+    T = int(cu[-1])
+    cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    BM, BN = va.tile_sizes(0, d)
+    tm, n = va.plan(cud, T, 2 * g, 2, d, mx, 0, True)
+    ref = ot.fwd_tile_map(cu, 2 * g, BM, BN, True, BN // 2)
+    assert (ref[:, 0] < 0).sum() > 0 and n == len(ref)
+    assert np.array_equal(tm.cpu().numpy(), ref)
+    q, k, v, do = si.tensors(T, 2 * g, 2, d, seed_offset=7 * d + g)
+    o, lse, gr = run_gpu(va, q, k, v, do, cud, mx)
+    ro, rl, rg = run_oracle(q, k, v, do, cu)
+    wl.assert_close_outputs(o, lse, ro, rl)
+    wl.assert_close_grads(gr, rg)
+    for s in cu[:-1]:  # a segment's first query sees only itself
+        for h in range(2 * g):
+            assert np.array_equal(o[s, h], si.to_f64(v[s, h // g]))
 
 
 # ------------------------------------------------------------------ properties
