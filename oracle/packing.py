@@ -116,6 +116,30 @@ def cu_seqlens_from_position_ids(position_ids, reset_at_min: bool = False):
     return cu, int(np.diff(cu).max())
 
 
+def boundary_plane_ok(position_ids, reset_at_min: bool = False, strict: bool = False) -> bool:
+    """Contract check of a position plane used as the boundary carrier.
+
+    The page (blog section 3) states the contract on the compiled array: int32,
+    first value 0, last value T, strictly increasing.  Reset indices are
+    distinct and below T, so the only way a plane breaks it is a first token
+    that is not a reset point (cu[0] would not be 0), or an empty plane.
+    ``strict`` adds the reading taken here for the repeated-values lesson of
+    the mRoPE section (a plane that repeats coordinates inside a sample cannot
+    carry boundaries): between resets the positions must count up by one.
+    """
+    p = np.asarray(position_ids).reshape(-1)
+    if p.size == 0:
+        return False
+    sentinel = p.min() if reset_at_min else 0
+    if p[0] != sentinel:
+        return False
+    if strict:
+        for i in range(1, p.size):
+            if p[i] != sentinel and p[i] != p[i - 1] + 1:
+                return False
+    return True
+
+
 def packed_storage_rows(inputs, targets, capacity: int):
     """Course storage rows for next-fit placement of (input, target) pair lists.
 

@@ -30,6 +30,26 @@ def test_three_sample_metadata(golden_dir):
     assert cu3.tolist() == fx["cu_seqlens"]
 
 
+def test_boundary_plane_check():
+    """Blog section 3: the compiled array must start at 0; the strict reading rejects a
+    plane whose positions repeat inside a sample (mRoPE's visual coordinates)."""
+    page = [0, 1, 2, 3, 4, 0, 1, 2, 0, 1, 2, 3]
+    assert op.boundary_plane_ok(page) and op.boundary_plane_ok(page, strict=True)
+    assert op.boundary_plane_ok(page, reset_at_min=True, strict=True)
+    shifted = [p + 1 for p in page]
+    assert not op.boundary_plane_ok(shifted)                     # no position 0 at index 0
+    assert op.boundary_plane_ok(shifted, reset_at_min=True, strict=True)
+    assert not op.boundary_plane_ok([1, 0, 1, 2])                # first token not a reset
+    repeated = [0, 0, 0, 1, 1, 1, 2, 2, 0, 1]                    # a plane with repeated values
+    assert op.boundary_plane_ok(repeated) and not op.boundary_plane_ok(repeated, strict=True)
+    assert not op.boundary_plane_ok([0, 1, 3], strict=True)      # a gap inside a sample
+    assert not op.boundary_plane_ok([])
+    # one-token samples are valid in the strict reading
+    assert op.boundary_plane_ok([0, 0, 0], strict=True)
+    cu, mx = op.cu_seqlens_from_position_ids([0, 0, 0])
+    assert cu.tolist() == [0, 1, 2, 3] and mx == 1
+
+
 def test_tail_pad_segment():
     cu, pos, seg, mx = op.build_metadata([3, 2], pad_to=8)
     assert cu.tolist() == [0, 3, 5, 8]
