@@ -132,6 +132,29 @@ va_status varlen_validate_cu_seqlens(const int32_t* cu_seqlens_dev, int32_t B, i
                                      int32_t max_seqlen, int32_t* status_dev,
                                      va_stream_t stream);
 
+/* Boundary compiler ("Packing与 FlashAttention Varlen", section 3): sample-local
+ * position_ids -> cu_seqlens.  Every index whose position equals the reset
+ * sentinel starts a sample -- the sentinel is 0, or with reset_at_min the
+ * plane's minimum (for position schemes that do not start at 0); the reset
+ * indices followed by T form cu_seqlens and max_seqlen is its largest
+ * difference.  The first token must be a reset point (the compiled array must
+ * start at 0).  With strict, positions between resets must count up by one, so a
+ * plane that repeats coordinates inside a sample is rejected.
+ *   position_ids_dev  int32 [T] device in, T >= 1
+ *   cu_seqlens_dev    int32 [capacity] device out: cu[0..B] (capacity >= B + 1;
+ *                     T + 1 always suffices)
+ *   B_dev, max_seqlen_dev   int32 [1] device out (0 on error)
+ *   status_dev        int32 [1] device out: VA_OK, VA_ERR_BAD_SEQLENS (first token
+ *                     not a reset, or a strict violation), VA_ERR_WORKSPACE
+ *                     (capacity < B + 1); cu_seqlens is left unwritten on error
+ * Host-detected: VA_ERR_INVALID_ARG (null pointer, T < 1, capacity < 2).
+ * Asynchronous. */
+va_status varlen_cu_seqlens_from_positions(const int32_t* position_ids_dev, int32_t T,
+                                           int32_t reset_at_min, int32_t strict,
+                                           int32_t* cu_seqlens_dev, int32_t capacity,
+                                           int32_t* B_dev, int32_t* max_seqlen_dev,
+                                           int32_t* status_dev, va_stream_t stream);
+
 /* ---------------------------------------------------------------- tile scheduler
  * Tile sizes the attention kernels use (BM query rows x BN key rows for
  * kind 0 = forward map; BM x BN for kind 1 = backward kv map; kind 2 = the

@@ -89,6 +89,23 @@ def validate_cu_seqlens(cu_seqlens: torch.Tensor, T: int, max_seqlen: int,
                                                  _stream(cu_seqlens.device)))
 
 
+def cu_seqlens_from_position_ids(position_ids: torch.Tensor, reset_at_min: bool = False,
+                                 strict: bool = False):
+    """Device position_ids (int32 [T]) -> (cu_seqlens[T + 1], B[1], max_seqlen[1], status[1]),
+    int32 device tensors; cu_seqlens[:B + 1] is the boundary array (unwritten on error)."""
+    assert position_ids.is_cuda and position_ids.dtype == torch.int32 and position_ids.is_contiguous()
+    T = position_ids.numel()
+    dev = position_ids.device
+    cu = torch.empty(T + 1, dtype=torch.int32, device=dev)
+    B = torch.empty(1, dtype=torch.int32, device=dev)
+    mx = torch.empty(1, dtype=torch.int32, device=dev)
+    st = torch.empty(1, dtype=torch.int32, device=dev)
+    check(_lib.load().varlen_cu_seqlens_from_positions(_ptr(position_ids), T, int(reset_at_min), int(strict),
+                                                       _ptr(cu), T + 1, _ptr(B), _ptr(mx), _ptr(st),
+                                                       _stream(dev)))
+    return cu, B, mx, st
+
+
 # ----------------------------------------------------------------- shapes, plans
 
 def make_shape(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, B: int, max_seqlen: int,

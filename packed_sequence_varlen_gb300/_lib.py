@@ -24,7 +24,7 @@ EXPORTS = (
     "varlen_attn_workspace_size", "varlen_attn_plan", "varlen_attn_fwd", "varlen_attn_bwd",
     "varlen_read_status", "varlen_clear_status", "varlen_last_error", "varlen_version",
     "varlen_profile_enable", "varlen_profile_read", "varlen_kernel_name", "varlen_launch_count",
-    "varlen_attn_fwd_noalloc",
+    "varlen_attn_fwd_noalloc", "varlen_cu_seqlens_from_positions",
 )
 
 
@@ -57,6 +57,8 @@ def _declare(lib):
                                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
         "varlen_validate_cu_seqlens": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p,
                                                  c_void_p]),
+        "varlen_cu_seqlens_from_positions": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p,
+                                                       c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
         "varlen_attn_tile_sizes": (c_int32, [c_int32, c_int32, i32p, i32p]),
         "varlen_attn_workspace_size": (c_size_t, [POINTER(VaShape), c_int32]),
         "varlen_attn_plan": (c_int32, [POINTER(VaShape), c_void_p, c_int32, c_int32, c_void_p,

@@ -15,6 +15,8 @@ cudaError_t launch_metadata_scan(const int32_t*, int, int, int, int32_t*, int32_
 cudaError_t launch_metadata_fill(const int32_t*, int, int, int32_t*, int32_t*, const int32_t*,
                                  cudaStream_t);
 cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaStream_t);
+cudaError_t launch_cu_from_positions(const int32_t*, int, int, int, int32_t*, int, int32_t*, int32_t*,
+                                     int32_t*, cudaStream_t);
 cudaError_t launch_plan(const PlanArgs&, cudaStream_t);
 cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, cudaStream_t);
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
@@ -33,11 +35,12 @@ void set_error(const char* msg) { g_error = msg; }
 // ------------------------------------------------------------ launch accounting
 enum KernelId {
   K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_PREP, K_BWD_DKDV, K_BWD_DQ,
-  K_VALIDATE_PLAN, K_FWD_TOK, K_COUNT
+  K_VALIDATE_PLAN, K_FWD_TOK, K_CU_FROM_POS, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan",          "fwd",
-    "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan", "fwd_tok"};
+    "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan", "fwd_tok",
+    "cu_from_positions"};
 
 struct Profiler {
   std::vector<cudaEvent_t> start, stop;
@@ -205,6 +208,22 @@ va_status varlen_validate_cu_seqlens(const int32_t* cu_dev, int32_t B, int32_t T
     return launch_validate(cu_dev, B, T, max_seqlen, status_dev, 0, cs);
   });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "validate");
+}
+
+va_status varlen_cu_seqlens_from_positions(const int32_t* position_ids_dev, int32_t T, int32_t reset_at_min,
+                                           int32_t strict, int32_t* cu_seqlens_dev, int32_t capacity,
+                                           int32_t* B_dev, int32_t* max_seqlen_dev, int32_t* status_dev,
+                                           va_stream_t stream) {
+  if (!position_ids_dev || !cu_seqlens_dev || !B_dev || !max_seqlen_dev || !status_dev)
+    return fail(VA_ERR_INVALID_ARG, "cu_seqlens_from_positions: null pointer");
+  if (T < 1 || capacity < 2)
+    return fail(VA_ERR_INVALID_ARG, "cu_seqlens_from_positions: T >= 1 and capacity >= 2");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(K_CU_FROM_POS, cs, [&] {
+    return launch_cu_from_positions(position_ids_dev, T, reset_at_min ? 1 : 0, strict ? 1 : 0, cu_seqlens_dev,
+                                    capacity, B_dev, max_seqlen_dev, status_dev, cs);
+  });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "cu_seqlens_from_positions");
 }
 
 va_status varlen_attn_tile_sizes(int32_t kind, int32_t d, int32_t* BM, int32_t* BN) {
