@@ -14,6 +14,8 @@ E = sum over real documents of l(l+1)/2 (the tail pad segment is computed but
 not credited), in TFLOP/s.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload sft8k|gqa16k|long64k|tiny4k] [--packs P]
+(--workload picks another configuration of seeded_inputs; sft8k is the benchmark.)
 For N > 1 launch with torch.distributed.run; each rank runs its own packs
 (independent replicas, no collective on the data path).
 """
@@ -73,17 +75,25 @@ def edges(lengths):
     return sum(l * (l + 1) // 2 for l in lengths)
 
 
-def batch_packs(rank: int, planner):
+def batch_packs(rank: int, planners):
     """Doc lengths (without pad) of this rank's packs, with the workload.
 
-    ``planner(lengths, capacity)`` returns packs as index lists: the library's
-    next-fit for our arm, the oracle's for the CPU legs.
+    ``planners = (next_fit, best_fit_decreasing)``, each ``(lengths, capacity)`` -> packs
+    as index lists: the library's for our arm, the oracle's for the CPU legs.
     """
     w = si.WORKLOADS[WORKLOAD]
     raw = si.raw_lengths(WORKLOAD).tolist()
-    packs = [[raw[i] for i in p] for p in planner(raw, w.capacity)]
+    planner = host_planner(w, planners)
+    packs = [raw] if planner is None else [[raw[i] for i in p] for p in planner(raw, w.capacity)]
     idx = [(rank * PACKS_PER_STEP + i) % len(packs) for i in range(PACKS_PER_STEP)]
     return [packs[i] for i in idx], idx, w
+
+
+def host_planner(w, planners):
+    """The workload's packing planner (None for a fixed segment list)."""
+    if w.strategy == "fixed":
+        return None
+    return planners[1] if w.strategy == "best_fit_decreasing" else planners[0]
 
 
 def flops_of(docs, pad_to, d, Hq):
@@ -166,8 +176,10 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     lib = _lib.load()
-    packs, idx, w = batch_packs(rank, va.pack_next_fit)
-    d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to
+    planners = (va.pack_next_fit, va.pack_best_fit_decreasing)
+    packs, idx, w = batch_packs(rank, planners)
+    plan_host = host_planner(w, planners)
+    d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to or sum(packs[0])
     fl = [flops_of(p, T, d, Hq) for p in packs]
     step_flops = sum(f["fwd"] + f["bwd"] for f in fl)
 
@@ -187,7 +199,8 @@ def run_ours(args, rank, world, local_rank):
 
     def step():
         # host planner over the batch's documents (its packs match the resident lengths)
-        va.pack_next_fit(all_docs, w.capacity)
+        if plan_host is not None:
+            plan_host(all_docs, w.capacity)
         for p in range(len(packs)):
             q, k, v, do = ins[p]
             o, lse, dq, dk, dv = outs[p]
@@ -273,17 +286,17 @@ def run_ours(args, rank, world, local_rank):
     fwd_t = per_kernel.get("fwd", (0.0, 1))[0]
     fwd_tflops = 4 * d * Hq * sum(f["e_doc"] for f in fl) * args.steps / (fwd_t * 1e-3) / 1e12 if fwd_t else None
 
-    e2e = run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier) if not args.no_e2e else None
+    e2e = run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host) if not args.no_e2e else None
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(max_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: first {PACKS_PER_STEP} next-fit packs of 8192 tokens "
-                               "(lengths U[32,2048], tail padded), Hq=Hkv=32, d=128, causal, fwd+bwd",
+        "config": {"workload": f"{WORKLOAD}: {PACKS_PER_STEP} pack(s) of {T} tokens per step ({w.description}), "
+                               "causal, fwd+bwd",
                    "tokens_per_step": PACKS_PER_STEP * T, "packs_per_step": PACKS_PER_STEP,
-                   "l2": "inputs larger than L2 (256 MB per pack)",
+                   "l2": f"inputs larger than L2 ({T * (2 * Hq + 2 * Hkv) * d * 2 // 2**20} MB per pack)",
                    "parallelism": f"replicas x{world}",
                    "pct_of_bf16_peak_burst": round(100 * value / world / peaks["bf16_tflops"], 2),
                    "fwd_kernel_tflops": round(fwd_tflops, 2) if fwd_tflops else None},
@@ -298,13 +311,13 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier):
+def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
     """Same step through the public API from pinned HOST buffers: H2D of every pack's q/k/v/dO
     and lengths, the step, D2H of dq/dk/dv, all inside the timed region.  Copies run on their
     own streams with two device buffer sets, so pack p+1 uploads and pack p-1 downloads while
     pack p computes (H2D and D2H use opposite link directions)."""
     import torch
-    d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to
+    d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to or sum(packs[0])
     host_in = []
     for pi in idx:
         q, k, v, do = si.tensors(T, Hq, Hkv, d, seed_offset=1000 * pi)
@@ -325,7 +338,8 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier):
     n = len(packs)
 
     def step():
-        va.pack_next_fit(all_docs, w.capacity)
+        if plan_host is not None:
+            plan_host(all_docs, w.capacity)
         up = [torch.cuda.Event() for _ in range(n)]
         done = [torch.cuda.Event() for _ in range(n)]
         down = [torch.cuda.Event() for _ in range(n)]
@@ -382,9 +396,9 @@ def cpu_baseline(budget_s: float = 12.0, steps: int | None = None):
     """The float64 CPU oracle as it stands, on sft8k pack 0, one kv head at a time, fwd+bwd."""
     from oracle import attention as oa
     from oracle import packing as op
-    packs, idx, w = batch_packs(0, op.next_fit)
+    packs, idx, w = batch_packs(0, (op.next_fit, op.best_fit_decreasing))
     docs = packs[0]
-    T = w.pad_to
+    T = w.pad_to or sum(docs)
     segs = docs + ([T - sum(docs)] if sum(docs) < T else [])
     cu = np.cumsum([0] + segs)
     q, k, v, do = si.tensors(T, w.Hq, w.Hkv, w.d, seed_offset=1000 * idx[0])
@@ -413,9 +427,9 @@ def run_reference(args, rank, world):
         return None
     from oracle import attention as oa
     from oracle import packing as op
-    packs, idx, w = batch_packs(0, op.next_fit)
+    packs, idx, w = batch_packs(0, (op.next_fit, op.best_fit_decreasing))
     docs = packs[0]
-    T = w.pad_to
+    T = w.pad_to or sum(docs)
     segs = docs + ([T - sum(docs)] if sum(docs) < T else [])
     cu = np.cumsum([0] + segs)
     q, k, v, do = si.tensors(T, w.Hq, w.Hkv, w.d, seed_offset=1000 * idx[0])
@@ -458,7 +472,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--packs", type=int, default=16,
                     help="packs per step (16 is the benchmark; fewer for profiling cases)")
+    ap.add_argument("--workload", choices=["sft8k", "gqa16k", "long64k", "tiny4k"], default="sft8k",
+                    help="configuration (sft8k is the benchmark; the others are for measurement)")
     args = ap.parse_args()
+    global WORKLOAD
+    WORKLOAD = args.workload
     PACKS_PER_STEP = args.packs
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
