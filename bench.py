@@ -283,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
     kernel_table = {k: {"launches": c, "total_ms": round(t, 3),
                         "share": round(t / max(sum(x[0] for x in per_kernel.values()), 1e-9), 4)}
                     for k, (t, c) in sorted(per_kernel.items(), key=lambda kv: -kv[1][0])}
-    fwd_t = per_kernel.get("fwd", (0.0, 1))[0]
+    fwd_t = per_kernel.get("fwd", (0.0, 1))[0] + per_kernel.get("fwd_tok", (0.0, 1))[0]
     fwd_tflops = 4 * d * Hq * sum(f["e_doc"] for f in fl) * args.steps / (fwd_t * 1e-3) / 1e12 if fwd_t else None
 
     e2e = run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host) if not args.no_e2e else None
