@@ -37,7 +37,8 @@ A run [r0, r1) gives the tiles t0 = r0, r0 + BM, ... with rows = min(BM, r1 - t0
 rows; the keys a tile needs are [cu[f], t0 + rows) where f is the segment that
 holds row t0.  Its record is (-1 - f, t0, h, rows), and the token records follow
 every segment record, ordered by (t0, h).  Segments covered by token tiles have
-no segment records.
+no segment records.  The dK/dV map cuts the same runs into BN-row tiles of key
+rows: key j of a tile is seen by the queries [j, end of its segment).
 """
 from __future__ import annotations
 
@@ -72,29 +73,21 @@ def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, sho
             for m, nb in blocks:
                 items.append(((-cls, b, h, -nb, m), (b, m, h, nb)))
     items.sort(key=lambda t: t[0])
-    out = [r for _, r in items]
-    b = 0
-    while b < B:
-        if not tok[b]:
-            b += 1
-            continue
-        e = b
-        while e < B and tok[e]:
-            e += 1
-        r0, r1 = cu[b], cu[e]                     # one run of short segments
-        for t0 in range(r0, r1, BM):
-            f = max(x for x in range(b, e) if cu[x] <= t0)
-            for h in range(Hq):
-                out.append((-1 - f, t0, h, min(BM, r1 - t0)))
-        b = e
+    out = [r for _, r in items] + _token_records(cu, tok, Hq, BM)
     return np.asarray(out, dtype=np.int32).reshape(-1, 4)
 
 
-def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True):
-    """Items (b, n, h_kv, n_q) as an int32 array [N, 4], in the order above."""
+def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True, short: int = 0):
+    """Items as an int32 array [N, 4], in the order above: segment records
+    (b, n, h_kv, n_q), then (causal, short > 0) token records (-1 - f, t0, h_kv, rows)
+    whose BN-row tiles hold the key rows [t0, t0 + rows) of a run of short segments."""
     cu = [int(x) for x in cu_seqlens]
+    B = len(cu) - 1
+    tok = [causal and short > 0 and cu[b + 1] - cu[b] <= short for b in range(B)]
     items = []
-    for b in range(len(cu) - 1):
+    for b in range(B):
+        if tok[b]:
+            continue
         l = cu[b + 1] - cu[b]
         Mq = _ceil(l, BM)
         blocks = []
@@ -106,7 +99,42 @@ def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True):
             for n, nq in blocks:
                 items.append(((-cls, b, h, -nq, n), (b, n, h, nq)))
     items.sort(key=lambda t: t[0])
-    return np.asarray([r for _, r in items], dtype=np.int32).reshape(-1, 4)
+    return np.asarray([r for _, r in items] + _token_records(cu, tok, Hkv, BN), dtype=np.int32).reshape(-1, 4)
+
+
+def _token_records(cu, tok, H, rows_per_tile):
+    """Token records of every maximal run of short segments, by (t0, head)."""
+    out, B, b = [], len(cu) - 1, 0
+    while b < B:
+        if not tok[b]:
+            b += 1
+            continue
+        e = b
+        while e < B and tok[e]:
+            e += 1
+        r0, r1 = cu[b], cu[e]
+        for t0 in range(r0, r1, rows_per_tile):
+            f = max(x for x in range(b, e) if cu[x] <= t0)
+            for h in range(H):
+                out.append((-1 - f, t0, h, min(rows_per_tile, r1 - t0)))
+        b = e
+    return out
+
+
+def bwd_item_edges(cu_seqlens, item, BM: int, BN: int):
+    """(query, key) token pairs a backward kv item's tiles cover, in global indices."""
+    b, n, _h, nq = (int(x) for x in item)
+    cu = [int(x) for x in cu_seqlens]
+    if b < 0:                                     # token record: key rows [t0, t0 + rows)
+        t0, rows = n, nq
+        last = t0 + rows - 1
+        end = min(cu[x + 1] for x in range(len(cu) - 1) if cu[x + 1] > last)
+        return [(i, j) for j in range(t0, t0 + rows) for i in range(t0, end)]
+    s, l = cu[b], cu[b + 1] - cu[b]
+    m0 = -(-l // BM) - nq
+    cols = range(s + n * BN, s + min(l, (n + 1) * BN))
+    rows = range(s + m0 * BM, s + l)
+    return [(i, j) for i in rows for j in cols]
 
 
 def fwd_item_edges(cu_seqlens, item, BM: int, BN: int):

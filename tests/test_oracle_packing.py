@@ -267,23 +267,48 @@ def test_token_tile_map_hand_example():
 
 
 @pytest.mark.parametrize("BM,BN", [(2, 2), (2, 4), (4, 2), (128, 128), (64, 128)])
-def test_bwd_tile_map_covers_each_allowed_edge_once(BM, BN):
-    lengths = [5, 1, 9, 3, 260, 130]
+@pytest.mark.parametrize("short", [0, 1, 2, 64])
+def test_bwd_tile_map_covers_each_allowed_edge_once(BM, BN, short):
+    lengths = [5, 1, 9, 3, 260, 130, 2, 1, 1, 64, 3]
     cu, _, _, _ = op.build_metadata(lengths)
-    tm = ot.bwd_tile_map(cu, 1, BM, BN)
+    tm = ot.bwd_tile_map(cu, 1, BM, BN, True, short)
     allowed = _allowed_edges(cu.tolist())
     seen = []
-    for b, n, _h, nq in tm:
-        s, l = cu[b], cu[b + 1] - cu[b]
-        m0 = -(-l // BM) - nq
-        cols = range(s + n * BN, s + min(l, (n + 1) * BN))
-        rows = range(s + m0 * BM, s + l)
-        hit = [(i, j) for i in rows for j in cols if (i, j) in allowed]
+    for it in tm:
+        b, n, _h, nq = (int(x) for x in it)
+        hit = [e for e in ot.bwd_item_edges(cu, it, BM, BN) if e in allowed]
         assert hit
         seen.extend(hit)
+        if b < 0:   # token tile: BN-row tiles of a run of short segments
+            assert 1 <= nq <= BN and cu[-1 - b] <= n < cu[-b]
+            assert all(cu[x + 1] - cu[x] <= short for x in range(len(cu) - 1)
+                       if cu[x] < n + nq and cu[x + 1] > n)
+            continue
+        s, l = cu[b], cu[b + 1] - cu[b]
+        assert l > short
+        m0 = -(-l // BM) - nq
+        cols = range(s + n * BN, s + min(l, (n + 1) * BN))
         # rows before m0 * BM see none of these keys
         assert all((i, j) not in allowed for i in range(s, s + m0 * BM) for j in cols)
     assert sorted(seen) == sorted(allowed)
+    tok = tm[tm[:, 0] < 0]
+    assert np.array_equal(tm[len(tm) - len(tok):], tok)      # token records come last
+    assert [(r[1], r[2]) for r in tok] == sorted((r[1], r[2]) for r in tok)
+
+
+def test_bwd_token_map_hand_example():
+    """Lengths 3, 2, 1, 300, 4, 60 with BM=64, BN=128, short=64: segment 3's kv blocks
+    n = 0, 1, 2 see 5, 3, 1 q blocks (m_start = 2n); the runs [0, 6) and [306, 370) are one
+    key tile each."""
+    cu, _, _, _ = op.build_metadata([3, 2, 1, 300, 4, 60])
+    tm = ot.bwd_tile_map(cu, 1, 64, 128, True, 64)
+    assert tm.tolist() == [[3, 0, 0, 5], [3, 1, 0, 3], [3, 2, 0, 1], [-1, 0, 0, 6], [-5, 306, 0, 64]]
+    # key 305 (last of segment 3) is not in a token tile; key 309 (last of segment 4) is seen
+    # by queries 309 only; key 306 by 306..309
+    edges = ot.bwd_item_edges(cu, tm[4], 64, 128)
+    assert (309, 306) in edges and (310, 306) in edges     # covered; (310, 306) not permitted
+    allowed = _allowed_edges(cu.tolist())
+    assert (310, 306) not in allowed and (309, 306) in allowed
 
 
 def test_tile_map_noncausal_counts():
