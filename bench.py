@@ -96,12 +96,31 @@ def host_planner(w, planners):
     return planners[1] if w.strategy == "best_fit_decreasing" else planners[0]
 
 
+# Causal packs whose mean segment length is below TOKEN_MEAN run their segments of at most
+# TOKEN_SHORT tokens as token tiles.
+TOKEN_SHORT, TOKEN_MEAN = 64, 256
+
+
 def flops_of(docs, pad_to, d, Hq):
     e_doc = edges(docs)
     pad = pad_to - sum(docs)
     e_all = e_doc + (edges([pad]) if pad > 0 else 0)
+    segs = list(docs) + ([pad] if pad > 0 else [])
+    tok = sum(segs) < TOKEN_MEAN * len(segs)
     return {"fwd": 4 * d * Hq * e_doc, "bwd": 10 * d * Hq * e_doc,
-            "e_doc": e_doc, "e_all": e_all}
+            "e_doc": e_doc, "e_all": e_all, "t_tok": sum(x for x in segs if x <= TOKEN_SHORT) if tok else 0}
+
+
+def kernel_bytes_of(t_all, t_tok, d, Hq, Hkv):
+    """Algorithmic HBM bytes per kernel: every input row read once and every output row
+    written once (bf16 rows of d per head, fp32 lse and D), over all t_all rows, or over the
+    t_tok rows of token-tiled segments for the token forward kernel."""
+    q, kv = 2 * d * Hq, 2 * d * Hkv
+    fwd_row = q + 2 * kv + q + 4 * Hq                # q, k, v -> o, lse
+    return {"fwd": t_all * fwd_row, "fwd_tok": t_tok * fwd_row,
+            "bwd_prep": t_all * (2 * q + 4 * Hq),    # o, dO -> D
+            "bwd_dkdv": t_all * (2 * q + 2 * kv + 8 * Hq + 2 * kv),  # q, dO, k, v, lse, D -> dk, dv
+            "bwd_dq": t_all * (2 * q + 2 * kv + 8 * Hq + q)}         # q, dO, k, v, lse, D -> dq
 
 
 class ClockSampler:
@@ -269,9 +288,22 @@ def run_ours(args, rank, world, local_rank):
     e_all = sum(f["e_all"] for f in fl) * args.steps
     kernel_flops = {"fwd": 4 * d * Hq * e_all, "bwd_dkdv": 8 * d * Hq * e_all,
                     "bwd_dq": 6 * d * Hq * e_all}
+    kernel_bytes = kernel_bytes_of(T * len(fl) * args.steps, sum(f["t_tok"] for f in fl) * args.steps,
+                                   d, Hq, Hkv)
     dom = max(per_kernel, key=lambda k: per_kernel[k][0])
     roof = None
-    if dom in kernel_flops:
+    # the kernel's bound: the larger of its ideal tensor time and its ideal HBM time
+    hbm_bound = dom in kernel_bytes and (dom not in kernel_flops or
+                                         kernel_bytes[dom] / (peaks["hbm_gbs"] * 1e9) >
+                                         kernel_flops[dom] / (peaks["bf16_tflops_sustained"] * 1e12))
+    if hbm_bound:
+        ach = kernel_bytes[dom] / (per_kernel[dom][0] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "peak_kind": f"HBM copy, {peaks['source']}", "traffic": kernel_traffic(dom),
+                "launches": per_kernel[dom][1],
+                "avg_launch_us": round(per_kernel[dom][0] / per_kernel[dom][1] * 1e3, 2)}
+    elif dom in kernel_flops:
         ach = kernel_flops[dom] / (per_kernel[dom][0] * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 2),
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",

@@ -172,17 +172,20 @@ size_t varlen_attn_workspace_size(const va_shape* shape, int32_t for_bwd);
  * same K/V tiles are adjacent and longer work goes first,
  *     key = (-floor(log2(C_b)), segment b, head, -count, block)
  * with C_b the segment's total tile count.
- *   kind 0: records {segment, q block, q head, n key blocks}; when causal,
- *           segments of at most BN/2 tokens get none: each maximal run of such
- *           segments [r0, r1) is cut into token tiles t0 = r0, r0 + BM, ... with
- *           records {-1 - f, t0, q head, rows = min(BM, r1 - t0)}, f the segment
- *           holding row t0; they follow all segment records, ordered by (t0, head).
- *           Row i of a token tile sees keys [start of its segment, i] ("Pack
- *           sequences without joining their contexts", "Permission depends on
- *           the example").
+ *   kind 0: records {segment, q block, q head, n key blocks}
  *   kind 1: records {segment, kv block, kv head, n q blocks} where the q blocks
  *           of a kv block n start at floor(n*BN/BM) (causal)
  *   kind 2: as kind 0 with the dQ kernel's tile sizes
+ * Token tiles: for causal calls whose mean segment length T / B is below 256
+ * tokens, segments of at most 64 tokens get no segment records.  Each maximal
+ * run of such segments [r0, r1) is cut into tiles of R rows t0 = r0, r0 + R, ...
+ * (R = BM, q rows, for kinds 0 and 2; R = BN, key rows, for kind 1) with records
+ * {-1 - f, t0, head, rows = min(R, r1 - t0)}, f the segment holding row t0; they
+ * follow all segment records, ordered by (t0, head).  Query i sees the keys
+ * [start of its segment, i], key j the queries [j, end of its segment) ("Pack
+ * sequences without joining their contexts", "Permission depends on the
+ * example").  The attention calls apply the same rule, so this builds the maps
+ * they use; the results do not depend on it.
  *   tile_map_dev    device out, int32 [capacity][4], 16-byte aligned
  *   n_items_dev     device out, int32
  *   scratch_dev     device scratch, int32 [B + 4]

@@ -23,9 +23,10 @@ cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
 cudaError_t launch_fwd_tok(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
 int fwd_tc_token_short();
+int bwd_tc_token_short();
 cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, cudaStream_t);
-cudaError_t launch_bwd_dkdv_tc(const BwdParams&, int, int, cudaStream_t);
-cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, cudaStream_t);
+cudaError_t launch_bwd_dkdv_tc(const BwdParams&, int, int, bool, cudaStream_t);
+cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, bool, cudaStream_t);
 void bwd_tc_tiles(int*, int*, int*, int*);
 
 static thread_local std::string g_error;
@@ -76,6 +77,16 @@ va_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Token tiles (runs of short segments planned as tiles of consecutive tokens) pay off when
+// short segments are common; they are used for causal calls whose mean segment length T / B
+// is below this many tokens.  Results do not depend on the choice: it only selects which
+// records cover the short segments and which kernel forms run.
+constexpr int64_t kTokenMeanLen = 256;
+
+bool token_tiles(const va_shape& s, int32_t causal) {
+  return causal && static_cast<int64_t>(s.T) < kTokenMeanLen * s.B;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -256,7 +267,8 @@ va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kin
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const PlanArgs pa{cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
                     reinterpret_cast<TileItem*>(map_dev), capacity, nullptr, n_items_dev,
-                    scratch_dev + 4, scratch_dev, kind == 0 && causal ? fwd_tc_token_short() : 0};
+                    scratch_dev + 4, scratch_dev,
+                    !token_tiles(*s, causal) ? 0 : kind == 0 ? fwd_tc_token_short() : bwd_tc_token_short()};
   cudaError_t e = launch(K_PLAN, cs, [&] { return launch_plan(pa, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "plan");
 }
@@ -285,10 +297,11 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   }
   int BM, BN;
   tiles(0, &BM, &BN);
+  const bool tok = token_tiles(*s, causal);
   const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map, static_cast<int>(L.cap),
                     &hdr->status, &hdr->n_items[0],
                     reinterpret_cast<int32_t*>(w + L.segoff), &hdr->counter[0],
-                    causal ? fwd_tc_token_short() : 0, &hdr->n_items[kTokSlot],
+                    tok ? fwd_tc_token_short() : 0, &hdr->n_items[kTokSlot],
                     &hdr->counter[kTokSlot]};
   cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
     return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cs);
@@ -323,6 +336,7 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   // segment records, then (as its programmatic dependent, filling its tail) token records
   e = launch(K_FWD, cs, [&] { return launch_fwd_tc(p, s->d, static_cast<int>(L.cap), cs); });
   if (e != cudaSuccess) return cuda_fail(e, "fwd kernel");
+  if (!tok) return VA_OK;
   FwdParams pt = p;
   pt.counter = &hdr->counter[kTokSlot];
   e = launch(K_FWD_TOK, cs, [&] { return launch_fwd_tok(pt, s->d, static_cast<int>(L.cap), cs); });
@@ -357,12 +371,15 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   int BM, BN, BM2, BN2;
   tiles(1, &BM, &BN);
   tiles(2, &BM2, &BN2);
+  const bool tok = token_tiles(*s, causal);
   int32_t* segoff = reinterpret_cast<int32_t*>(w + L.segoff);
   const PlanArgs pa[2] = {
       {cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, kvmap, static_cast<int>(L.cap_kv), &hdr->status,
-       &hdr->n_items[1], segoff, &hdr->counter[1]},
+       &hdr->n_items[1], segoff, &hdr->counter[1], tok ? bwd_tc_token_short() : 0,
+       &hdr->n_items[kKvTokSlot]},
       {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, qmap, static_cast<int>(L.cap_q), &hdr->status,
-       &hdr->n_items[2], segoff, &hdr->counter[2]}};
+       &hdr->n_items[2], segoff, &hdr->counter[2], tok ? bwd_tc_token_short() : 0,
+       &hdr->n_items[kQTokSlot]}};
   BwdParams p{};
   p.q = static_cast<const bf16*>(q);
   p.k = static_cast<const bf16*>(k);
@@ -375,11 +392,14 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   p.dk = static_cast<bf16*>(dk);
   p.dv = static_cast<bf16*>(dv);
   p.cu = cu;
+  p.B = s->B;
   p.kv_items = kvmap;
   p.q_items = qmap;
   p.hdr = hdr;
   p.kv_slot = 1;
   p.q_slot = 2;
+  p.kv_tok_slot = kKvTokSlot;
+  p.q_tok_slot = kQTokSlot;
   p.kv_counter = &hdr->counter[1];
   p.q_counter = &hdr->counter[2];
   p.T = s->T;
@@ -400,9 +420,9 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   // one launch validates, plans both maps and computes D = rowsum(dO * O)
   cudaError_t e = launch(K_BWD_PREP, cs, [&] { return launch_bwd_prep(p, pa, 2, s->T, s->max_seqlen, s->d, cs); });
   if (e == cudaSuccess)
-    e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv_tc(p, s->d, static_cast<int>(L.cap_kv), cs); });
+    e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv_tc(p, s->d, static_cast<int>(L.cap_kv), tok, cs); });
   if (e == cudaSuccess)
-    e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq_tc(p, s->d, static_cast<int>(L.cap_q), cs); });
+    e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq_tc(p, s->d, static_cast<int>(L.cap_q), tok, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd kernels");
 }
 

@@ -36,10 +36,12 @@ struct BwdParams {
   bf16* dk;
   bf16* dv;
   const int32_t* cu;
+  int B;  // segments (cu has B + 1 entries)
   const TileItem* kv_items;  // kv-block map
   const TileItem* q_items;   // q-block map (dQ pass)
   WsHeader* hdr;
-  int kv_slot, q_slot;
+  int kv_slot, q_slot;          // n_items[slot]: all records of the map
+  int kv_tok_slot, q_tok_slot;  // n_items[slot]: the token records at the map's end
   int32_t* kv_counter;
   int32_t* q_counter;
   int T, Hq, Hkv, g;

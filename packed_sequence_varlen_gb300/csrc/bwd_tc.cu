@@ -26,6 +26,19 @@
 //   softmax warpgroups that take alternate steps, each with its own TMEM S/dP
 //   buffer, so the tensor core computes step i+1 while step i is exponentiated.
 // TMEM: S_0 | S_1 | dP_0 | dP_1 (64 columns each) | accumulators.
+//
+// Token records (runs of segments of at most 64 tokens, at the end of both maps) take the
+// same pipeline.  A dK/dV token record {-1 - f, t0, kv head, rows} holds the key rows
+// [t0, t0 + rows) and the queries [t0, qend), qend the end of the last row's segment (at
+// most three 64-row steps); a dQ token record {-1 - f, t0, q head, rows} holds the query rows
+// [t0, t0 + rows) and the keys [cu[f], t0 + rows).  Query i sees the keys [start of its
+// segment, i], key j the queries [j, end of its segment): the permission rule of "Pack
+// sequences without joining their contexts" ("Permission depends on the example") in its
+// range form.  The producer decodes a token record into the item fields the producer, MMA
+// and lse/D roles already use, plus a per-row table next to the queue (the key row's segment
+// end, or the query row's position in its segment); only the softmax warpgroups treat token
+// items differently -- every step masked on both sides -- in a loop of their own that they
+// enter after their last segment item, so the segment loop is unchanged.
 #include "attn_params.cuh"
 #include "sched.cuh"
 #include "sm100_ptx.cuh"
@@ -68,14 +81,22 @@ struct KvCfg {
                        B_IF = B_DR + 1, B_IE = B_IF + 2, B_LF = B_IE + 2, B_LE = B_LF + LDS,
                        NBAR = B_LE + LDS;
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
-  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 32;
+  static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 32;   // four 128-byte row tables (item k & 3)
+  static constexpr int MISC_OFF = ROWS_OFF + 4 * KB;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
   __host__ __device__ static constexpr uint32_t kv_off(int b) { return static_cast<uint32_t>(b) * 2 * TKV; }
 };
+static_assert(KvCfg<128>::SMEM <= 232448 && KvCfg<64>::SMEM <= 232448, "dK/dV shared memory");
 
+// One dK/dV work item: key rows from s0 + 128 n of kv head hk; step i covers the 64 query rows
+// from s0 + 64 (m_start + i / g) of q head hk g + i % g; queries at or past s0 + l are outside
+// the item.  valid = 1: a segment record, the segment [s0, s0 + l).  valid = 2: a token record
+// (n = m_start = 0), key rows [s0, s0 + kvn), key row s0 + r seen only by the queries before
+// s0 + table[r].  valid = 0: the end of the list.
 struct KvItem {
   int s0, l, n, hk, m_start, steps;
   int valid;
+  int kvn;
 };
 
 __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
@@ -88,12 +109,62 @@ __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
   const int Mq = (r.l + 63) / 64;
   r.m_start = Mq - it.count;
   r.steps = it.count * p.g;
+  r.kvn = 0;
+  return r;
+}
+
+// Segments of at most this many tokens are planned as token records: a key then sees at most
+// 64 queries, an item's queries span at most three 64-row steps, and a row's segment end
+// (relative to the item's first row) fits the row table's byte.
+constexpr int kBwdTokenShort = 64;
+
+// Decodes dK/dV token record idx, {-1 - f, t0, kv head, rows} (whole warp, every lane gets the
+// same item), and writes its row table: the segment starts inside the rows come from
+// cu[f + 1], cu[f + 2], ... (32 per round) as a 128-bit map, and entry r is the next start
+// after row r, or, for the rows of the last segment, that segment's end (qend).
+__device__ __forceinline__ KvItem kv_token_decode_w(const BwdParams& p, int idx, uint8_t* table) {
+  const TileItem it = p.kv_items[idx];
+  const int lane = threadIdx.x & 31, f = -1 - it.seg, t0 = it.blk, rows = it.count;
+  uint32_t words[4] = {0u, 0u, 0u, 0u};
+  int qend = t0 + rows;  // the contract (cu[B] = T >= t0 + rows) always sets it below
+  for (int b0 = f + 1; b0 <= p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int x = b <= p.B ? p.cu[b] : INT_MAX;
+    const int rr = x - t0;  // >= 1: cu[f + 1] is past row t0
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      words[w] |= __reduce_or_sync(0xffffffffu, (rr < rows && (rr >> 5) == w) ? 1u << (rr & 31) : 0u);
+    const unsigned past = __ballot_sync(0xffffffffu, rr >= rows);  // the first one ends the last row's segment
+    if (past) {
+      qend = __shfl_sync(0xffffffffu, x, __ffs(past) - 1);
+      break;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int row = w * 32 + lane;
+    int e = qend - t0;
+    for (int w2 = 3; w2 > w; --w2)  // the nearest later word with a start wins
+      if (words[w2]) e = w2 * 32 + __ffs(words[w2]) - 1;
+    const uint32_t above = lane == 31 ? 0u : words[w] & (0xffffffffu << (lane + 1));
+    if (above) e = w * 32 + __ffs(above) - 1;
+    table[row] = static_cast<uint8_t>(row < rows ? e : 0);
+  }
+  __threadfence_block();
+  KvItem r;
+  r.s0 = t0;
+  r.l = qend - t0;
+  r.n = 0;
+  r.hk = it.head;
+  r.m_start = 0;
+  r.steps = (qend - t0 + 63) / 64 * p.g;
+  r.kvn = rows;
   return r;
 }
 
 }  // namespace
 
-template <int D>
+template <int D, bool TOK>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -112,6 +183,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
 
   KvItem* queue = reinterpret_cast<KvItem*>(sm + C::QUEUE_OFF);
+  uint8_t* row_tables = sm + C::ROWS_OFF;
   auto dec = [&](int idx) { return kv_decode(p, idx); };
   // Launched as a programmatic dependent of the preparation kernel: its maps, D and status
   // are read only after the wait.  The dQ kernel, which reads the same products but none
@@ -119,6 +191,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   griddep_begin();
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.kv_slot];
+  const int n_seg = n_items - p.hdr->n_items[p.kv_tok_slot];  // segment records, then token ones
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (threadIdx.x == 0) {
@@ -170,6 +243,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int qit = 0, item_cnt = 0, kv_issued = 0;  // kv_issued: items whose K/V load went out
       bool ok = true;
       KvItem nxt;
+      // Publishes this CTA's k-th item (the next record of the map): lane 0 pulls its index,
+      // the warp decodes it (a token record also fills row table k & 3) and lane 0 writes the
+      // slot and releases it.  Returns false at the end of the list or on abort (ok_ = false).
+      auto publish = [&](int k, KvItem& out, bool& ok_) -> bool {
+        const int s = k & 1;
+        ok_ = wwait(bar(C::B_IE + s), ((k >> 1) & 1) ^ 1, abort_flag, p.hdr, 40);
+        if (!ok_) return false;
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(p.kv_counter, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < n_seg) {
+          out = kv_decode(p, idx);
+          out.valid = 1;
+        } else if (idx < n_items) {
+          out = kv_token_decode_w(p, idx, row_tables + (k & 3) * C::KB);
+          out.valid = 2;
+        } else {
+          out = KvItem{};
+          out.valid = 0;
+        }
+        __syncwarp();  // every lane's table bytes before the release
+        if (lane == 0) {
+          queue[s] = out;
+          mbar_arrive(bar(C::B_IF + s));
+        }
+        __syncwarp();
+        return out.valid != 0;
+      };
       // K/V of this CTA's j-th item into buffer j & 1, once item j-2's S/dP MMAs are done
       // with it
       auto load_kv = [&](const KvItem& J, int j) -> bool {
@@ -185,13 +286,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         kv_issued = j + 1;
         return true;
       };
-      bool more = queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
-                                abort_flag, p.hdr, ok);
+      bool more = TOK ? publish(0, nxt, ok)
+                      : queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
+                                        abort_flag, p.hdr, ok);
       if (ok && more) ok = load_kv(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const KvItem I = nxt;  // publish the next record first: its decode overlaps this one
-        more = queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items,
-                             dec, nxt, abort_flag, p.hdr, ok);
+        more = TOK ? publish(item_cnt + 1, nxt, ok)
+                   : queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec,
+                                     nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
         // the next item's K/V goes out right after this item's first two Q/dO steps, a whole
         // item ahead of its use
@@ -354,6 +457,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int item_cnt = 0;
     bool ok = true;
     int g0 = 0;  // this CTA's steps before the current item (the lse/D ring index)
+    KvItem J;          // the first token item, once the segment loop has met it
+    bool tok = false;
     for (;; ++item_cnt) {
       KvItem I;
       const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
@@ -362,6 +467,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       if (!got) break;
+      if constexpr (TOK) {
+        if (I.valid == 2) {  // the token records follow: the loop below
+          J = I;
+          tok = true;
+          break;
+        }
+      }
       const int kvrow = I.n * 128 + r;
       for (int i = x; i < I.steps; i += 2) {
         const int gs = g0 + i, ls = gs % C::LDS;
@@ -446,6 +558,98 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_before_sync();
       mbar_arrive(bar(C::B_AE));
     }
+    // Token items (runs of short segments; all of them follow the segment items): every step
+    // masked on both sides per key row, rows past the item's keys not stored.
+    for (KvItem I = J; TOK && ok && tok;) {
+      const int kend = I.s0 + row_tables[(item_cnt & 3) * C::KB + r];  // end of this key's segment
+      for (int i = x; i < I.steps; i += 2) {
+        const int gs = g0 + i, ls = gs % C::LDS;
+        ok = mbar_wait(bar(C::B_LF + ls), (gs / C::LDS) & 1, abort_flag, p.hdr, 19);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 28);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++sf;
+        fence_after_sync();
+        const int q0 = I.s0 + (i / p.g) * 64;
+        // query columns c < lim (before the key) and c >= hi (past its segment) are masked
+        const int lim = I.s0 + r - q0, hi = kend - q0;
+        const float* L = ldring + ls * 128;
+        const float* Dd = L + 64;
+        // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(s_addr, sv);
+        tmem_ld32(s_addr + 32, sv + 32);
+        tmem_ld32(dp_addr, dpv);
+        tmem_ld32(dp_addr + 32, dpv + 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(L + c);
+          const float4 d4 = *reinterpret_cast<const float4*>(Dd + c);
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int j = c + e;
+            const float la = e ? l4.z : l4.x, lb = e ? l4.w : l4.y;  // -lse * log2(e)
+            const float da = e ? d4.z : d4.x, db = e ? d4.w : d4.y;  // -D
+            // scalar FMAs: the packed forms measured slower here (operand pairing moves)
+            const float x0 = fmaf(__uint_as_float(sv[j]), sl2, la), x1 = fmaf(__uint_as_float(sv[j + 1]), sl2, lb);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            if (j < lim || j >= hi) p0 = 0.f;
+            if (j + 1 < lim || j + 1 >= hi) p1 = 0.f;
+            const float t0 = __uint_as_float(dpv[j]) + da, t1 = __uint_as_float(dpv[j + 1]) + db;
+            sv[j >> 1] = pack_bf16(p0, p1);
+            dpv[j >> 1] = pack_bf16(p0 * t0, p1 * t1);
+          }
+        }
+        tmem_st32(s_addr, sv);
+        tmem_st32(dp_addr, dpv);
+        mbar_arrive(bar(C::B_LE + ls));  // this thread has read the slot's lse/D
+        tmem_wait_st();
+        fence_before_sync();
+        mbar_arrive(bar(C::B_PF + x));
+      }
+      if (!ok) break;
+      g0 += I.steps;
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+      ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 29);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const float mul = x == 0 ? 1.f : p.scale;
+      const bool store = r < I.kvn;
+      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>(I.s0 + r) * p.k_rs +
+                  static_cast<int64_t>(I.hk) * p.k_hs;
+      {
+        uint32_t o[D];  // the whole accumulator row in one TMEM round trip
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(acc_addr + c * 32, o + c * 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < D / 2; ++j)
+          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
+        uint4 ov[D / 8];
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        store_rows_coalesced(ov, out, p.k_rs, store);
+      }
+      fence_before_sync();
+      mbar_arrive(bar(C::B_AE));
+      ++item_cnt;
+      const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (!got) break;
+    }
   }
 
   fence_before_sync();
@@ -472,14 +676,22 @@ struct QCfg {
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 2, B_DR = B_AE + 2,
                        B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;  // AF/AE: per dQ buffer
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
-  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 32;
+  static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 32;   // four 128-byte row tables (item k & 3)
+  static constexpr int MISC_OFF = ROWS_OFF + 4 * QB;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
   __host__ __device__ static constexpr uint32_t qd_off(int b) { return static_cast<uint32_t>(b) * 2 * TQ; }
 };
+static_assert(QCfg<128>::SMEM <= 232448 && QCfg<64>::SMEM <= 232448, "dQ shared memory");
 
+// One dQ work item: query rows from s0 + 128 m of q head h (kv head hk), rows at or past
+// s0 + l outside it; step n covers the 64 key rows from kb + 64 n (nb steps).  valid = 1: a
+// segment record, the segment [s0, s0 + l) (kb = s0).  valid = 2: a token record (m = 0),
+// query row s0 + r seeing only the keys from s0 + r - table[r] (the start of its segment).
+// valid = 0: the end of the list.
 struct QItem {
   int s0, l, m, h, hk, nb;
   int valid;
+  int kb;
 };
 
 __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
@@ -491,12 +703,52 @@ __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
   r.h = it.head;
   r.hk = it.head / p.g;
   r.nb = it.count;
+  r.kb = r.s0;
+  return r;
+}
+
+// Decodes dQ token record idx, {-1 - f, t0, q head, rows} (whole warp, every lane gets the
+// same item), and writes its row table: the segment starts inside the rows come from
+// cu[f + 1], cu[f + 2], ... (32 per round) as a 128-bit map, and entry r is row r's position
+// in its segment.  Its keys start at cu[f].
+__device__ __forceinline__ QItem q_token_decode_w(const BwdParams& p, int idx, uint8_t* table) {
+  const TileItem it = p.q_items[idx];
+  const int lane = threadIdx.x & 31, f = -1 - it.seg, t0 = it.blk, rows = it.count;
+  const int kb = p.cu[f];
+  uint32_t words[4] = {0u, 0u, 0u, 0u};
+  for (int b0 = f + 1; b0 <= p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int x = b <= p.B ? p.cu[b] : INT_MAX;
+    const int rr = x - t0;  // >= 1: cu[f + 1] is past row t0
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      words[w] |= __reduce_or_sync(0xffffffffu, (rr < rows && (rr >> 5) == w) ? 1u << (rr & 31) : 0u);
+    if (__any_sync(0xffffffffu, rr >= rows)) break;  // a boundary past the rows was read
+  }
+  int last = kb - t0;  // start of the segment holding the rows before word w (<= 0)
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int row = w * 32 + lane;
+    const uint32_t mine = words[w] & (0xffffffffu >> (31 - lane));
+    const int st = mine ? w * 32 + 31 - __clz(mine) : last;
+    table[row] = static_cast<uint8_t>(row < rows ? row - st : 0);
+    if (words[w]) last = w * 32 + 31 - __clz(words[w]);
+  }
+  __threadfence_block();
+  QItem r;
+  r.s0 = t0;
+  r.l = rows;
+  r.m = 0;
+  r.h = it.head;
+  r.hk = it.head / p.g;
+  r.nb = (t0 + rows - kb + 63) / 64;
+  r.kb = kb;
   return r;
 }
 
 }  // namespace
 
-template <int D>
+template <int D, bool TOK>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -515,9 +767,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
 
   QItem* queue = reinterpret_cast<QItem*>(sm + C::QUEUE_OFF);
+  uint8_t* row_tables = sm + C::ROWS_OFF;
   auto dec = [&](int idx) { return q_decode(p, idx); };
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.q_slot];
+  const int n_seg = n_items - p.hdr->n_items[p.q_tok_slot];  // segment records, then token ones
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (threadIdx.x == 0) {
@@ -567,6 +821,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int kit = 0, item_cnt = 0, qd_issued = 0;  // qd_issued: items whose Q/dO load went out
       bool ok = true;
       QItem nxt;
+      // Publishes this CTA's k-th item (the next record of the map): lane 0 pulls its index,
+      // the warp decodes it (a token record also fills row table k & 3) and lane 0 writes the
+      // slot and releases it.  Returns false at the end of the list or on abort (ok_ = false).
+      auto publish = [&](int k, QItem& out, bool& ok_) -> bool {
+        const int s = k & 1;
+        ok_ = wwait(bar(C::B_IE + s), ((k >> 1) & 1) ^ 1, abort_flag, p.hdr, 40);
+        if (!ok_) return false;
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(p.q_counter, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < n_seg) {
+          out = q_decode(p, idx);
+          out.valid = 1;
+        } else if (idx < n_items) {
+          out = q_token_decode_w(p, idx, row_tables + (k & 3) * C::QB);
+          out.valid = 2;
+        } else {
+          out = QItem{};
+          out.valid = 0;
+        }
+        __syncwarp();  // every lane's table bytes before the release
+        if (lane == 0) {
+          queue[s] = out;
+          mbar_arrive(bar(C::B_IF + s));
+        }
+        __syncwarp();
+        return out.valid != 0;
+      };
       // Q/dO of this CTA's j-th item into buffer j & 1, once item j-2's S/dP MMAs are done
       // with it
       auto load_qd = [&](const QItem& J, int j) -> bool {
@@ -582,13 +864,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         qd_issued = j + 1;
         return true;
       };
-      bool more = queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
-                                abort_flag, p.hdr, ok);
+      bool more = TOK ? publish(0, nxt, ok)
+                      : queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
+                                        abort_flag, p.hdr, ok);
       if (ok && more) ok = load_qd(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const QItem I = nxt;  // publish the next record first: its decode overlaps this one
-        more = queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items,
-                             dec, nxt, abort_flag, p.hdr, ok);
+        more = TOK ? publish(item_cnt + 1, nxt, ok)
+                   : queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec,
+                                     nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
         // the next item's Q/dO goes out right after this item's first two K/V steps
         const int qd_at = I.nb < 2 ? I.nb : 2;
@@ -604,8 +888,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_expect_tx_w(bar(C::B_KF + s), 2 * C::TKV);
           const uint32_t dst = base + C::RING_OFF + s * 2 * C::TKV;
           for (int pn = 0; pn < D / 64; ++pn) {
-            tma_load_3d_w(dst + pn * C::PKV, &tk, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
-            tma_load_3d_w(dst + C::TKV + pn * C::PKV, &tv, bar(C::B_KF + s), pn * 64, I.hk, I.s0 + n * 64);
+            tma_load_3d_w(dst + pn * C::PKV, &tk, bar(C::B_KF + s), pn * 64, I.hk, I.kb + n * 64);
+            tma_load_3d_w(dst + C::TKV + pn * C::PKV, &tv, bar(C::B_KF + s), pn * 64, I.hk, I.kb + n * 64);
           }
           ++kit;
         }
@@ -747,14 +1031,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       return true;
     };
+    QItem I;
+    bool tok = false;  // the item in I is the first token item
     for (;; ++item_cnt) {
-      QItem I;
       const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       if (!got) break;
+      if constexpr (TOK) {
+        if (I.valid == 2) {  // the token records follow: the loop below
+          tok = true;
+          break;
+        }
+      }
       const int qrow = I.m * 128 + r;
       const int64_t at = static_cast<int64_t>(I.h) * p.T + I.s0 + qrow;
       // the row's lse and D: loads issued here, first used after the S wait below, so their
@@ -815,6 +1106,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       pend_out = p.dq + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
       pend_store = qrow < I.l;
     }
+    // Token items (runs of short segments; all of them follow the segment items): every step
+    // masked on both sides per query row.
+    while (TOK && ok && tok) {
+      const int qrow = r;  // m = 0
+      const int klo = I.s0 + r - row_tables[(item_cnt & 3) * C::QB + r];  // its segment's start
+      const int64_t at = static_cast<int64_t>(I.h) * p.T + I.s0 + qrow;
+      // the row's lse and D: loads issued here, first used after the S wait below, so their
+      // latency overlaps it
+      const bool qin = qrow < I.l;
+      float lse_raw = 0.f, dsum = 0.f;
+      if (qin) {
+        lse_raw = __ldg(p.lse + at);
+        dsum = __ldg(p.dsum + at);
+      }
+      for (int n = x; n < I.nb; n += 2) {
+        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 38);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++sf;
+        fence_after_sync();
+        const float lse2 = qin ? lse_raw * kLog2e : INFINITY;
+        // key columns c > lim (after the query) and c < lo (before its segment) are masked
+        const int k0 = I.kb + n * 64;
+        const int lim = I.s0 + r - k0, lo = klo - k0;
+        // one TMEM round trip: the step's 64 scores and 64 dP values of this q row
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(s_addr, sv);
+        tmem_ld32(s_addr + 32, sv + 32);
+        tmem_ld32(dp_addr, dpv);
+        tmem_ld32(dp_addr + 32, dpv + 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
+          float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          if (c > lim || c < lo) p0 = 0.f;
+          if (c + 1 > lim || c + 1 < lo) p1 = 0.f;
+          float t0, t1;
+          fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
+          dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
+        }
+        tmem_st32(dp_addr, dpv);
+        tmem_wait_st();
+        fence_before_sync();
+        mbar_arrive(bar(C::B_PF + x));
+        if (pend >= 0 && !epilogue()) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      if (pend >= 0 && !epilogue()) {  // this warpgroup had no step in the item
+        ok = false;
+        break;
+      }
+      pend = item_cnt;
+      pend_out = p.dq + static_cast<int64_t>(I.s0 + qrow) * p.o_rs + static_cast<int64_t>(I.h) * p.o_hs;
+      pend_store = qrow < I.l;
+      ++item_cnt;
+      const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (!got) break;
+    }
     if (ok && pend >= 0) ok = epilogue();
   }
   fence_before_sync();
@@ -828,7 +1188,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------- host side
 
 
-template <int D>
+template <int D, bool TOK>
 static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   using C = KvCfg<D>;
   CUtensorMap tq, tk, tv, tdo;
@@ -837,11 +1197,11 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
       !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
       !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D>);
+  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D, TOK>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -849,10 +1209,10 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dkdv_tc_kernel<D>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dkdv_tc_kernel<D, TOK>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
-template <int D>
+template <int D, bool TOK>
 static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   using C = QCfg<D>;
   CUtensorMap tq, tk, tv, tdo;
@@ -861,11 +1221,11 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
       !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 64) ||
       !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 64))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D>);
+  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D, TOK>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -873,16 +1233,23 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dq_tc_kernel<D>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dq_tc_kernel<D, TOK>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
-cudaError_t launch_bwd_dkdv_tc(const BwdParams& p, int d, int cap, cudaStream_t st) {
-  return d == 64 ? launch_dkdv_d<64>(p, cap, st) : launch_dkdv_d<128>(p, cap, st);
+// tok: the maps hold token records.  The two forms are compiled separately so that the
+// segment-only kernels keep their own code: the token branch in the softmax item loop
+// measured 15% slower on segment records.
+cudaError_t launch_bwd_dkdv_tc(const BwdParams& p, int d, int cap, bool tok, cudaStream_t st) {
+  if (tok) return d == 64 ? launch_dkdv_d<64, true>(p, cap, st) : launch_dkdv_d<128, true>(p, cap, st);
+  return d == 64 ? launch_dkdv_d<64, false>(p, cap, st) : launch_dkdv_d<128, false>(p, cap, st);
 }
 
-cudaError_t launch_bwd_dq_tc(const BwdParams& p, int d, int cap, cudaStream_t st) {
-  return d == 64 ? launch_dq_d<64>(p, cap, st) : launch_dq_d<128>(p, cap, st);
+cudaError_t launch_bwd_dq_tc(const BwdParams& p, int d, int cap, bool tok, cudaStream_t st) {
+  if (tok) return d == 64 ? launch_dq_d<64, true>(p, cap, st) : launch_dq_d<128, true>(p, cap, st);
+  return d == 64 ? launch_dq_d<64, false>(p, cap, st) : launch_dq_d<128, false>(p, cap, st);
 }
+
+int bwd_tc_token_short() { return kBwdTokenShort; }
 
 void bwd_tc_tiles(int* kvBM, int* kvBN, int* qBM, int* qBN) {
   *kvBM = 64;

@@ -15,7 +15,11 @@ namespace va {
 //   int32 counter[4]  -- work counters the attention kernels pull records from
 // Forward workspaces: n_items[0] counts all records of the map, n_items[kTokSlot] the
 // token records at its end; counter[kTokSlot] is the token kernel's work counter.
+// Backward workspaces: n_items[1] / n_items[2] count all records of the kv-block / q-block
+// maps, n_items[kKvTokSlot] / n_items[kQTokSlot] the token records at their ends;
+// counter[1] / counter[2] are the dK/dV and dQ kernels' work counters.
 constexpr int kTokSlot = 3;
+constexpr int kKvTokSlot = 0, kQTokSlot = 3;
 
 struct WsHeader {
   int32_t status;
@@ -44,8 +48,8 @@ struct PlanArgs {
   int32_t* n_items;  // out
   int32_t* seg_off;  // scratch [B]: first record of each segment
   int32_t* counter;  // work counter the attention kernel pulls items from; zeroed here
-  int short_len;      // kind 0, causal: segments of at most this many tokens go into token
-                      // tiles (records {-1 - f, t0, head, rows}); 0 = off
+  int short_len;      // causal: segments of at most this many tokens go into token tiles
+                      // (records {-1 - f, t0, head, rows}); 0 = off
   int32_t* n_tok;     // may be null: out, the number of token records (the map's last ones)
   int32_t* tok_counter;  // may be null: the token kernel's work counter; zeroed here
 };

@@ -26,14 +26,15 @@
 // not grow with the number of classes.  Tile sizes are powers of two (block counts are
 // shifts).
 //
-// Token tiles (forward map, causal, short_len > 0): segments of at most short_len tokens
-// get no segment records.  Each maximal run [r0, r1) of consecutive short segments is cut
-// into tiles of BM rows starting at r0, and each tile gets one record per head,
-//   {seg = -1 - f, blk = t0, head, count = rows = min(BM, r1 - t0)},
-// f being the segment that holds row t0.  Row i of a tile sees keys [start of its segment,
+// Token tiles (causal, short_len > 0): segments of at most short_len tokens get no segment
+// records.  Each maximal run [r0, r1) of consecutive short segments is cut into tiles of
+// R rows starting at r0 (R = BM, q rows, for the forward and dQ maps; R = BN, key rows, for
+// the dK/dV map), and each tile gets one record per head,
+//   {seg = -1 - f, blk = t0, head, count = rows = min(R, r1 - t0)},
+// f being the segment that holds row t0.  Query i of a run sees keys [start of its segment,
 // i] -- the permission rule of "Pack sequences without joining their contexts" ("Permission
-// depends on the example") in its range form.  Token records follow all segment records,
-// ordered by (t0, head).  Runs are found with block-wide scans over contiguous chunks of
+// depends on the example") in its range form; key j is seen by the queries [j, end of its
+// segment).  Token records follow all segment records, ordered by (t0, head).  Runs are found with block-wide scans over contiguous chunks of
 // segments per thread: the last long segment before a chunk (max scan), the first long
 // segment after it (min scan from the end), then the tile counts (sum scan).
 #pragma once
@@ -49,9 +50,7 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 __device__ __forceinline__ int ceil_p2(int a, int b) { return (a + b - 1) >> (__ffs(b) - 1); }
 __device__ __forceinline__ int div_p2(int a, int b) { return a >> (__ffs(b) - 1); }
 
-__device__ __forceinline__ bool token_mode(const PlanArgs& a) {
-  return a.kind == 0 && a.causal && a.short_len > 0;
-}
+__device__ __forceinline__ bool token_mode(const PlanArgs& a) { return a.causal && a.short_len > 0; }
 
 // What a map build is, fixed at compile time: the planner's time is mostly fetching its
 // own instructions (it runs once per call, on one SM), so each kind of map gets its own
@@ -155,8 +154,8 @@ struct TokenChunk {
   int lo, hi, ns_before, ns_after, first_tile, n_tiles;
 };
 
-__device__ __forceinline__ TokenChunk token_scan(const PlanArgs& a, const int* cu, int lo, int hi, int nth,
-                                                 int* tmp, int* n_tiles_total) {
+__device__ __forceinline__ TokenChunk token_scan(const PlanArgs& a, const int* cu, int tile, int lo, int hi,
+                                                 int nth, int* tmp, int* n_tiles_total) {
   TokenChunk c;
   c.lo = lo;
   c.hi = hi;
@@ -176,7 +175,7 @@ __device__ __forceinline__ TokenChunk token_scan(const PlanArgs& a, const int* c
       ns = b;
     } else {
       const int rs = cu[ns + 1];  // start of this segment's run
-      cnt += ceil_p2(y - rs, a.BM) - ceil_p2(x - rs, a.BM);
+      cnt += ceil_p2(y - rs, tile) - ceil_p2(x - rs, tile);
     }
   }
   c.n_tiles = cnt;
@@ -184,8 +183,9 @@ __device__ __forceinline__ TokenChunk token_scan(const PlanArgs& a, const int* c
   return c;
 }
 
-// Writes the token records of one chunk, from record index base.
-__device__ __forceinline__ void token_records(const PlanArgs& a, const int* cu, const TokenChunk& c, int base) {
+// Writes the token records of one chunk, from record index base; tiles of `tile` rows.
+__device__ __forceinline__ void token_records(const PlanArgs& a, const int* cu, int tile, const TokenChunk& c,
+                                              int base) {
   int ns = c.ns_before, g = c.first_tile;
   for (int b = c.lo; b < c.hi; ++b) {
     const int x = cu[b], y = cu[b + 1];
@@ -194,19 +194,19 @@ __device__ __forceinline__ void token_records(const PlanArgs& a, const int* cu, 
       continue;
     }
     const int rs = cu[ns + 1];
-    const int k0 = ceil_p2(x - rs, a.BM), k1 = ceil_p2(y - rs, a.BM);
+    const int k0 = ceil_p2(x - rs, tile), k1 = ceil_p2(y - rs, tile);
     if (k1 <= k0) continue;
     int nx = b + 1;  // first long segment after b: its start ends the run
     while (nx < c.hi && cu[nx + 1] - cu[nx] <= a.short_len) ++nx;
     const int re = cu[nx < c.hi ? nx : c.ns_after];
     for (int k = k0; k < k1; ++k, ++g) {
-      const int t0 = rs + k * a.BM;
+      const int t0 = rs + k * tile;
       for (int h = 0; h < a.heads; ++h) {
         TileItem t;
         t.seg = -1 - b;
         t.blk = t0;
         t.head = h;
-        t.count = min(a.BM, re - t0);
+        t.count = min(tile, re - t0);
         const int at = base + g * a.heads + h;
         if (at >= 0 && at < a.capacity) a.out[at] = t;  // boundaries that break the contract
                                                         // must not write outside the map
@@ -328,7 +328,7 @@ __device__ __forceinline__ void rank_and_write(const PlanArgs& a, PlanSmem& sh, 
   if (M::tokens) {
     const int per = ceil_div(a.B, nth);
     const int lo = min(a.B, tid * per), hi = min(a.B, lo + per);
-    tc = token_scan(a, cu, lo, hi, nth, sh.scan, &n_tiles);
+    tc = token_scan(a, cu, M::kv ? a.BN : a.BM, lo, hi, nth, sh.scan, &n_tiles);
   }
   plan_sync(nth);
   if (tid < 32) {  // class bases, largest class first
@@ -402,7 +402,7 @@ __device__ __forceinline__ void rank_and_write(const PlanArgs& a, PlanSmem& sh, 
     if (n > 0) seg_off[b] = sh.wtot[warp][c] + incl - n;
     plan_sync(nth);  // wtot is reused by the next round
   }
-  if (M::tokens) token_records(a, cu, tc, run);
+  if (M::tokens) token_records(a, cu, M::kv ? a.BN : a.BM, tc, run);
 }
 
 // Builds one map.  Every thread of the block (a multiple of 32, at most 1024) calls it.
@@ -431,8 +431,9 @@ __device__ __forceinline__ void plan_body_m(const PlanArgs& a, PlanSmem& sh, con
 
 __device__ __forceinline__ void plan_body(const PlanArgs& a, PlanSmem& sh, const int* cu, int* seg_off) {
   if (a.kind == 1) {
-    if (a.causal) plan_body_m<MapKind<true, true, false>>(a, sh, cu, seg_off);
-    else plan_body_m<MapKind<true, false, false>>(a, sh, cu, seg_off);
+    if (!a.causal) plan_body_m<MapKind<true, false, false>>(a, sh, cu, seg_off);
+    else if (token_mode(a)) plan_body_m<MapKind<true, true, true>>(a, sh, cu, seg_off);
+    else plan_body_m<MapKind<true, true, false>>(a, sh, cu, seg_off);
   } else if (a.causal) {
     if (token_mode(a)) plan_body_m<MapKind<false, true, true>>(a, sh, cu, seg_off);
     else plan_body_m<MapKind<false, true, false>>(a, sh, cu, seg_off);

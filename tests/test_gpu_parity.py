@@ -82,6 +82,23 @@ def test_metadata_page_layout_and_errors(va):
         assert int(st.item()) == 5
 
 
+# Causal calls whose mean segment length T / B is below TOKEN_MEAN put segments of at most
+# TOKEN_SHORT tokens in token tiles (every map); the results do not depend on the choice.
+TOKEN_SHORT = 64
+TOKEN_MEAN = 256
+
+
+def token_short(cu, causal):
+    return TOKEN_SHORT if causal and int(cu[-1]) < TOKEN_MEAN * (len(cu) - 1) else 0
+
+
+def oracle_map(va, kind, cu, Hq, Hkv, d, causal):
+    BM, BN = va.tile_sizes(kind, d)
+    if kind == 1:
+        return ot.bwd_tile_map(cu, Hkv, BM, BN, causal, token_short(cu, causal))
+    return ot.fwd_tile_map(cu, Hq, BM, BN, causal, token_short(cu, causal))
+
+
 @pytest.mark.parametrize("name", ["tiny", "sft8k", "gqa16k", "long64k", "tiny4k"])
 @pytest.mark.parametrize("causal", [True, False])
 def test_tile_maps_bit_exact(va, name, causal):
@@ -91,12 +108,8 @@ def test_tile_maps_bit_exact(va, name, causal):
         cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
         T = int(cu[-1])
         for kind in (0, 1, 2):
-            BM, BN = va.tile_sizes(kind, w.d)
             tm, n = va.plan(cud, T, w.Hq, w.Hkv, w.d, mx, kind, causal)
-            if kind == 1:
-                ref = ot.bwd_tile_map(cu, w.Hkv, BM, BN, causal)
-            else:  # the forward map puts segments of at most BN/2 tokens in token tiles
-                ref = ot.fwd_tile_map(cu, w.Hq, BM, BN, causal, BN // 2 if kind == 0 else 0)
+            ref = oracle_map(va, kind, cu, w.Hq, w.Hkv, w.d, causal)
             assert n == len(ref)
             assert np.array_equal(tm.cpu().numpy(), ref)
 
@@ -214,11 +227,13 @@ def test_tiny4k_full(va):
     ro, rl, rg = run_oracle(q, k, v, do, cu)
     wl.assert_close_outputs(o, lse, ro, rl)
     wl.assert_close_grads(g, rg)
+    wl.assert_close_grads_chunked(g, rg)
 
 
 # Runs of short segments: one of 300 single-token segments (more than 32 segment starts in
-# one token tile), runs cut at 256 rows inside a segment, a short segment alone between long
-# ones, 64 (the longest token-tiled length) next to 65, and a run that ends the stream.
+# one token tile), runs cut at 128 and 256 rows inside a segment, a short segment alone
+# between long ones, 64 (the longest token-tiled length) next to 65, and a run that ends the
+# stream.
 TOKEN_RUNS = [1] * 300 + [200] + [64] * 5 + [65, 3, 64, 1, 17, 700] + [33] * 20 + [2]
 
 
@@ -227,19 +242,45 @@ def test_token_tiles_mixed_runs(va, d, g):
     cu, _, _, mx = op.build_metadata(TOKEN_RUNS)
     T = int(cu[-1])
     cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
-    BM, BN = va.tile_sizes(0, d)
-    tm, n = va.plan(cud, T, 2 * g, 2, d, mx, 0, True)
-    ref = ot.fwd_tile_map(cu, 2 * g, BM, BN, True, BN // 2)
-    assert (ref[:, 0] < 0).sum() > 0 and n == len(ref)
-    assert np.array_equal(tm.cpu().numpy(), ref)
+    for kind in (0, 1, 2):  # forward, dK/dV and dQ maps: token records after segment ones
+        tm, n = va.plan(cud, T, 2 * g, 2, d, mx, kind, True)
+        ref = oracle_map(va, kind, cu, 2 * g, 2, d, True)
+        assert (ref[:, 0] < 0).sum() > 0 and n == len(ref)
+        assert np.array_equal(tm.cpu().numpy(), ref)
     q, k, v, do = si.tensors(T, 2 * g, 2, d, seed_offset=7 * d + g)
     o, lse, gr = run_gpu(va, q, k, v, do, cud, mx)
     ro, rl, rg = run_oracle(q, k, v, do, cu)
     wl.assert_close_outputs(o, lse, ro, rl)
     wl.assert_close_grads(gr, rg)
+    # the rows of token-tiled segments alone (whole-tensor norms could hide them)
+    short = np.repeat(np.diff(cu) <= TOKEN_SHORT, np.diff(cu))
+    wl.assert_close_grads(tuple(x[short] for x in gr), tuple(x[short] for x in rg))
+    wl.assert_close_grads_chunked(tuple(x[short] for x in gr), tuple(x[short] for x in rg))
     for s in cu[:-1]:  # a segment's first query sees only itself
         for h in range(2 * g):
             assert np.array_equal(o[s, h], si.to_f64(v[s, h // g]))
+
+
+def test_short_segments_among_long_ones(va):
+    """Mean segment length above the token-tile threshold: the short segments (1, 3, 64 tokens)
+    are covered by segment records, every map and gradient as the oracle gives them."""
+    lengths = [2000, 3, 1500, 64, 1, 1000]
+    cu, _, _, mx = op.build_metadata(lengths)
+    assert token_short(cu, True) == 0
+    T = int(cu[-1])
+    cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    for kind in (0, 1, 2):
+        tm, n = va.plan(cud, T, 4, 2, 128, mx, kind, True)
+        ref = oracle_map(va, kind, cu, 4, 2, 128, True)
+        assert (ref[:, 0] >= 0).all() and n == len(ref)
+        assert np.array_equal(tm.cpu().numpy(), ref)
+    q, k, v, do = si.tensors(T, 4, 2, 128, seed_offset=77)
+    o, lse, gr = run_gpu(va, q, k, v, do, cud, mx)
+    ro, rl, rg = run_oracle(q, k, v, do, cu)
+    wl.assert_close_outputs(o, lse, ro, rl)
+    wl.assert_close_grads(gr, rg)
+    short = np.repeat(np.diff(cu) <= TOKEN_SHORT, np.diff(cu))
+    wl.assert_close_grads(tuple(x[short] for x in gr), tuple(x[short] for x in rg))
 
 
 # ------------------------------------------------------------------ properties
