@@ -1,4 +1,5 @@
-"""Token-weighted objective and constructed-logit probe (test infrastructure only).
+"""Packed next-token targets, token-weighted objective and constructed-logit probe
+(test infrastructure only).
 
 "Pack sequences without joining their contexts", "Keep the same nine-target
 objective": the packed loss is the raw sum of the negative log likelihoods of
@@ -11,6 +12,24 @@ skipped before any arithmetic.
 from __future__ import annotations
 
 import numpy as np
+
+IGNORE_INDEX = -100
+
+
+def stream_targets(token_ids, cu_seqlens, ignore_index: int = IGNORE_INDEX):
+    """Next-token targets of a packed stream of whole documents, pairs formed inside each
+    document ("Form pairs inside each source range"): position t of segment [s, e) predicts
+    token t + 1 when t + 1 < e; the last position of every segment has no target
+    (``ignore_index``), so no pair crosses a boundary ("A's final input still predicts its
+    own EOS; it does not predict B's BOS")."""
+    ids = np.asarray(token_ids, dtype=np.int64).reshape(-1)
+    cu = np.asarray(cu_seqlens, dtype=np.int64).reshape(-1)
+    out = np.full(ids.size, ignore_index, dtype=np.int64)
+    for b in range(cu.size - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        for t in range(s, e - 1):
+            out[t] = ids[t + 1]
+    return out
 
 
 def constructed_logits(targets, eligible, q_of_cell, vocab: int):

@@ -94,6 +94,28 @@ def test_nine_target_permissions(golden_dir):
     assert [j for j in range(6) if allowed(c + 1, j)] == fx["b_second_query_allowed_keys"]
 
 
+def test_stream_targets_pairs_inside_documents(golden_dir):
+    """The three fixture documents as one packed stream: the targets are exactly the page's
+    nine (input, target) pairs, no pair crosses a document boundary, and they equal the
+    ms-swift layout (labels = ids with -100 at each sample's first label, shifted by one)."""
+    fx = json.load(open(os.path.join(golden_dir, "nine_target_fixture.json")))
+    docs = [i + t[-1:] for i, t in zip(fx["pair_inputs"], fx["pair_targets"])]
+    assert [len(d) for d in docs] == [4, 3, 5]
+    ids = sum(docs, [])
+    cu = np.cumsum([0] + [len(d) for d in docs])
+    tg = ol.stream_targets(ids, cu)
+    pairs = [(ids[t], int(tg[t])) for t in range(len(ids)) if tg[t] != ol.IGNORE_INDEX]
+    want = [(a, b) for i, t in zip(fx["pair_inputs"], fx["pair_targets"]) for a, b in zip(i, t)]
+    assert pairs == want and len(pairs) == fx["real_targets"]
+    assert [t for t in range(len(ids)) if tg[t] == ol.IGNORE_INDEX] == [3, 6, 11]  # each last token
+    labels = np.array(ids)
+    labels[cu[:-1]] = ol.IGNORE_INDEX                                          # sample-local -100
+    shifted = np.append(labels[1:], ol.IGNORE_INDEX)
+    assert np.array_equal(tg, shifted)
+    # a global shift of the concatenation would add the EOS -> BOS pairs at each join
+    assert {(1, 0)} & set(zip(ids[:-1], ids[1:])) and (1, 0) not in pairs
+
+
 def test_nine_target_loss_probe(golden_dir):
     """Token-weighted loss = 11 ln2 / 9 = 0.847180 (sum 7.624619); the row-mean and the
     document-mean weightings give 0.831777 and 0.924196 and must not be what we compute."""
