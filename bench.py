@@ -492,6 +492,89 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ packed loss
+
+def run_loss(args, rank, world, local_rank):
+    """Token-weighted cross entropy + logit gradient over the packed stream (the packed loss
+    layout): one step = targets formed inside each segment and the loss over `--packs` sft8k
+    packs of 8192 tokens with bf16 logits over `--vocab` classes.  HBM-bound: the algorithmic
+    bytes are the eligible rows' logits read once, every gradient row written once, targets."""
+    import torch
+    import packed_sequence_varlen_gb300 as va
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    planners = (va.pack_next_fit, va.pack_best_fit_decreasing)
+    global WORKLOAD
+    WORKLOAD = "sft8k"
+    packs, idx, w = batch_packs(rank, planners)
+    T1, V = w.pad_to, args.vocab
+    segs = [p + ([T1 - sum(p)] if sum(p) < T1 else []) for p in packs]
+    cu = [0]
+    for p in segs:
+        for x in p:
+            cu.append(cu[-1] + x)
+    T = cu[-1]
+    gen = torch.Generator().manual_seed(11 + rank)
+    ids = torch.randint(0, V, (T,), generator=gen, dtype=torch.int32).to(dev)
+    cud = torch.tensor(cu, dtype=torch.int32, device=dev)
+    dgen = torch.Generator(device=dev).manual_seed(12 + rank)  # seeded, drawn on the device
+    logits = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, T, 1024):  # N(0, 3^2), in slices
+        n = min(1024, T - r0)
+        logits[r0:r0 + n] = (3 * torch.randn(n, V, generator=dgen, device=dev)).to(torch.bfloat16)
+    grad = torch.empty_like(logits)
+    ws = torch.empty(va._lib.load().varlen_token_ce_workspace_size(T), dtype=torch.uint8, device=dev)
+    lib = va._lib.load()
+
+    def step():
+        tg = va.loss_targets(ids, cud)
+        return va.token_ce(logits, tg, grad=grad, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n_elig = int(step()[1].item())
+    l0 = lib.varlen_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = lib.varlen_launch_count() - l0
+    alg = n_elig * V * 2 + T * V * 2 + 3 * T * 4  # logits (eligible rows), grad, ids/targets
+    gbs = alg / (ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    res = {"metric": "packed token-weighted CE + logit gradient, algorithmic HBM GB/s", "value": round(gbs, 1),
+           "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"loss: {len(packs)} sft8k pack(s) of {T1} tokens (T={T}), V={V}, "
+                                  f"bf16 logits N(0, 9), targets formed inside each segment ({n_elig} eligible)",
+                      "l2": f"inputs larger than L2 ({T * V * 2 // 2**20} MB of logits)"},
+           "e2e": None, "gpu_launches": int(launches),
+           "roofline": {"bound": "hbm", "kernel": "token_ce", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "peak_kind": f"HBM copy, {peaks['source']}", "traffic": None},
+           "clocks": clocks.summary()}
+    if not args.no_cpu_baseline:
+        import time
+        from oracle import loss as ol
+        rows = 128  # bounded sample: the oracle on the first rows, scaled by bytes
+        z = logits[:rows].double().cpu().numpy()
+        tg = va.loss_targets(ids, cud)[:rows].cpu().numpy()
+        t0 = time.perf_counter()
+        ol.token_weighted_loss(z, tg, tg != -100)
+        dt = time.perf_counter() - t0
+        b = int((tg != -100).sum()) * V * 2 + rows * V * 2 + 3 * rows * 4
+        res["cpu_baseline"] = {"value": round(b / dt / 1e9, 3), "unit": "GB/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": f"first {rows} rows of the same logits, float64 numpy"}
+    return res
+
+
 def main():
     global PACKS_PER_STEP
     ap = argparse.ArgumentParser()
@@ -506,6 +589,9 @@ def main():
                     help="packs per step (16 is the benchmark; fewer for profiling cases)")
     ap.add_argument("--workload", choices=["sft8k", "gqa16k", "long64k", "tiny4k"], default="sft8k",
                     help="configuration (sft8k is the benchmark; the others are for measurement)")
+    ap.add_argument("--loss", action="store_true",
+                    help="measure the packed loss (targets + token-weighted CE + gradient) instead")
+    ap.add_argument("--vocab", type=int, default=32768, help="classes of the --loss logits")
     args = ap.parse_args()
     global WORKLOAD
     WORKLOAD = args.workload
@@ -526,7 +612,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    res = run_ours(args, rank, world, local_rank)
+    res = run_loss(args, rank, world, local_rank) if args.loss else run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

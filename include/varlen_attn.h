@@ -51,7 +51,8 @@ typedef enum {
   VA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   VA_ERR_BAD_SEQLENS = 5,  /* cu_seqlens breaks the contract (device-detected or host) */
   VA_ERR_TIMEOUT = 6,      /* a bounded device wait gave up (device-detected) */
-  VA_ERR_CAPACITY = 7      /* planner: a document longer than the pack capacity */
+  VA_ERR_CAPACITY = 7,     /* planner: a document longer than the pack capacity */
+  VA_ERR_BAD_TARGETS = 8   /* loss: an eligible target outside [0, V), or none eligible (device-detected) */
 } va_status;
 
 /* Shape and strides of one packed call.  Strides are in elements.
@@ -259,6 +260,47 @@ va_status varlen_read_status(const void* ws_dev, int32_t* status_host, va_stream
 
 /* Clears the workspace status word (asynchronous). */
 va_status varlen_clear_status(void* ws_dev, va_stream_t stream);
+
+/* ---------------------------------------------------------------- packed loss
+ * Next-token targets of a packed stream of whole documents.  Source: "Pack sequences
+ * without joining their contexts", "Form pairs inside each source range" (a document of L
+ * tokens gives L - 1 pairs, its final input predicts its own last token and never the next
+ * document's first) -- the same layout as sample-local -100 labels shifted by one
+ * ("Packing与 FlashAttention Varlen", section 2).  Position t of segment
+ * [cu[b], cu[b+1]) gets token_ids[t + 1] while t + 1 < cu[b+1], else ignore_index.
+ *   token_ids_dev  int32 [T] in;  cu_seqlens_dev int32 [B+1] in (the attention contract)
+ *   targets_dev    int32 [T] out
+ * Errors: VA_ERR_INVALID_ARG (null pointer, T < 0, B < 1).  Asynchronous. */
+va_status varlen_loss_targets(const int32_t* token_ids_dev, const int32_t* cu_seqlens_dev, int32_t B,
+                              int32_t T, int32_t ignore_index, int32_t* targets_dev, va_stream_t stream);
+
+/* Bytes of workspace varlen_token_ce needs for T rows: a 256-byte header (status word at
+ * byte 0) and one float per row. */
+size_t varlen_token_ce_workspace_size(int32_t T);
+
+/* Token-weighted cross entropy over the packed stream and its logit gradient.  Source: "Pack
+ * sequences without joining their contexts", "Keep the same nine-target objective": the
+ * loss is the raw sum of the negative log likelihoods of the eligible targets divided once by
+ * their count N (every eligible target has equal weight, whatever its row or document);
+ * d(mean)/d(z_ic) = (p_ic - [c == y_i]) / N on eligible rows; a row whose target is
+ * ignore_index is skipped before any arithmetic (its logits are never read, its gradient row
+ * is zero), so non-finite values there cannot leak in.
+ *   logits_dev   [T, V], row stride logits_row_stride elements; dtype 0 = fp32, 1 = bf16
+ *   targets_dev  int32 [T]: a class in [0, V), or ignore_index
+ *   loss_dev     double [2] out: {sum of NLL, sum / N}; NaN on a device-detected error
+ *   count_dev    int32 [1] out: N
+ *   grad_dev     [T, V] out (row stride grad_row_stride elements), the dtype of the logits,
+ *                or NULL for no gradient
+ *   ws_dev / ws_bytes  workspace (>= varlen_token_ce_workspace_size(T), 16-byte aligned)
+ * Arithmetic in fp32 per row (base-2 log-sum-exp), the sum over rows in fp64 in a fixed order
+ * (deterministic).  Errors: VA_ERR_INVALID_ARG, VA_ERR_WORKSPACE, VA_ERR_CUDA; the status
+ * word gets VA_ERR_BAD_TARGETS when an eligible target is outside [0, V) or no target is
+ * eligible (the mean would have no denominator), and then no row is computed.
+ * Asynchronous. */
+va_status varlen_token_ce(const void* logits_dev, int32_t dtype, int64_t logits_row_stride,
+                          const int32_t* targets_dev, int32_t T, int32_t V, int32_t ignore_index,
+                          double* loss_dev, int32_t* count_dev, void* grad_dev, int64_t grad_row_stride,
+                          void* ws_dev, size_t ws_bytes, va_stream_t stream);
 
 /* ---------------------------------------------------------------- tracing
  * Per-launch timing.  With capacity > 0, the library records a CUDA event pair

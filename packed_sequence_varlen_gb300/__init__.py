@@ -21,7 +21,8 @@ from ._lib import VarlenError, VaShape, check
 __all__ = [
     "pack_next_fit", "pack_best_fit_decreasing", "build_metadata", "validate_cu_seqlens",
     "tile_sizes", "workspace_size", "plan", "varlen_attn_fwd", "varlen_attn_bwd", "varlen_attn",
-    "read_status", "VarlenError", "make_shape", "library_path",
+    "read_status", "VarlenError", "make_shape", "library_path", "loss_targets", "token_ce",
+    "IGNORE_INDEX",
 ]
 
 
@@ -263,3 +264,54 @@ def varlen_attn(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None
                 causal: bool = True):
     """Differentiable packed attention: out [T, Hq, d]."""
     return _VarlenAttn.apply(q, k, v, cu_seqlens, max_seqlen, scale, causal)
+
+
+# ----------------------------------------------------------------- packed loss
+
+IGNORE_INDEX = -100
+
+
+def loss_targets(token_ids: torch.Tensor, cu_seqlens: torch.Tensor, ignore_index: int = IGNORE_INDEX):
+    """Next-token targets (int32 [T]) of a packed stream of whole documents: pairs formed
+    inside each segment, ``ignore_index`` at every segment's last position."""
+    if not token_ids.is_cuda or token_ids.dtype != torch.int32 or token_ids.dim() != 1:
+        raise ValueError("token_ids must be a CUDA int32 [T] tensor")
+    T = token_ids.numel()
+    out = torch.empty(T, dtype=torch.int32, device=token_ids.device)
+    check(_lib.load().varlen_loss_targets(_ptr(token_ids), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                          int(ignore_index), _ptr(out), _stream(token_ids.device)))
+    return out
+
+
+def token_ce(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = IGNORE_INDEX,
+             grad: bool | torch.Tensor = True, workspace=None, check_status=False):
+    """Token-weighted cross entropy of the packed stream: returns (loss [2] float64 device
+    tensor {sum, mean}, count [1] int32, grad or None).  ``logits`` is CUDA fp32 or bf16
+    [T, V] with a contiguous last dim; ``grad`` True allocates d(mean)/d(logits) like
+    ``logits``, a tensor receives it, False skips it."""
+    if not logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1 or \
+            logits.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("logits must be a CUDA fp32/bf16 [T, V] tensor with a contiguous last dim")
+    T, V = logits.shape
+    dev = logits.device
+    if grad is True:
+        g = torch.empty_like(logits, memory_format=torch.contiguous_format)
+    elif grad is False or grad is None:
+        g = None
+    else:
+        g = grad
+        if g.shape != logits.shape or g.dtype != logits.dtype or g.stride(1) != 1:
+            raise ValueError("grad must match logits in shape and dtype, with a contiguous last dim")
+    lib = _lib.load()
+    need = lib.varlen_token_ce_workspace_size(T)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    loss = torch.empty(2, dtype=torch.float64, device=dev)
+    count = torch.empty(1, dtype=torch.int32, device=dev)
+    check(lib.varlen_token_ce(_ptr(logits), 1 if logits.dtype == torch.bfloat16 else 0, logits.stride(0),
+                              _ptr(targets), T, V, int(ignore_index), _ptr(loss), _ptr(count), _ptr(g),
+                              g.stride(0) if g is not None else 0, _ptr(workspace), workspace.numel(),
+                              _stream(dev)))
+    if check_status:
+        _raise_status(workspace)
+    return loss, count, g

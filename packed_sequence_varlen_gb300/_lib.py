@@ -15,6 +15,7 @@ VA_OK = 0
 STATUS_NAMES = {
     0: "VA_OK", 1: "VA_ERR_INVALID_ARG", 2: "VA_ERR_UNSUPPORTED", 3: "VA_ERR_WORKSPACE",
     4: "VA_ERR_CUDA", 5: "VA_ERR_BAD_SEQLENS", 6: "VA_ERR_TIMEOUT", 7: "VA_ERR_CAPACITY",
+    8: "VA_ERR_BAD_TARGETS",
 }
 
 # every symbol include/varlen_attn.h declares
@@ -25,6 +26,7 @@ EXPORTS = (
     "varlen_read_status", "varlen_clear_status", "varlen_last_error", "varlen_version",
     "varlen_profile_enable", "varlen_profile_read", "varlen_kernel_name", "varlen_launch_count",
     "varlen_attn_fwd_noalloc", "varlen_cu_seqlens_from_positions",
+    "varlen_loss_targets", "varlen_token_ce_workspace_size", "varlen_token_ce",
 )
 
 
@@ -72,6 +74,12 @@ def _declare(lib):
         "varlen_attn_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                               POINTER(VaShape), c_float, c_int32, c_void_p,
                                               c_void_p, c_void_p]),
+        "varlen_loss_targets": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p,
+                                          c_void_p]),
+        "varlen_token_ce_workspace_size": (c_size_t, [c_int32]),
+        "varlen_token_ce": (c_int32, [c_void_p, c_int32, c_int64, c_void_p, c_int32, c_int32, c_int32,
+                                      c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_size_t,
+                                      c_void_p]),
         "varlen_read_status": (c_int32, [c_void_p, i32p, c_void_p]),
         "varlen_clear_status": (c_int32, [c_void_p, c_void_p]),
         "varlen_profile_enable": (c_int32, [c_int32]),

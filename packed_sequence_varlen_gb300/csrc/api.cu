@@ -25,6 +25,9 @@ void fwd_tc_tiles(int*, int*);
 int fwd_tc_token_short();
 int bwd_tc_token_short();
 cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, cudaStream_t);
+cudaError_t launch_loss_targets(const int32_t*, const int32_t*, int, int, int, int32_t*, cudaStream_t);
+cudaError_t launch_token_ce(int, const void*, int, int64_t, const int32_t*, int, int, int, void*, int64_t, float*,
+                            int32_t*, int32_t*, double*, cudaStream_t);
 cudaError_t launch_bwd_dkdv_tc(const BwdParams&, int, int, bool, cudaStream_t);
 cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, bool, cudaStream_t);
 void bwd_tc_tiles(int*, int*, int*, int*);
@@ -36,12 +39,12 @@ void set_error(const char* msg) { g_error = msg; }
 // ------------------------------------------------------------ launch accounting
 enum KernelId {
   K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_PREP, K_BWD_DKDV, K_BWD_DQ,
-  K_VALIDATE_PLAN, K_FWD_TOK, K_CU_FROM_POS, K_COUNT
+  K_VALIDATE_PLAN, K_FWD_TOK, K_CU_FROM_POS, K_LOSS_TARGETS, K_CE_COUNT, K_CE_ROWS, K_CE_REDUCE, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan",          "fwd",
     "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan", "fwd_tok",
-    "cu_from_positions"};
+    "cu_from_positions",   "loss_targets",  "ce_count",      "ce_rows",       "ce_reduce"};
 
 struct Profiler {
   std::vector<cudaEvent_t> start, stop;
@@ -424,6 +427,40 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   if (e == cudaSuccess)
     e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq_tc(p, s->d, static_cast<int>(L.cap_q), tok, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd kernels");
+}
+
+va_status varlen_loss_targets(const int32_t* ids, const int32_t* cu, int32_t B, int32_t T, int32_t ignore_index,
+                              int32_t* targets, va_stream_t stream) {
+  if (!ids || !cu || !targets || T < 0 || B < 1) return fail(VA_ERR_INVALID_ARG, "loss_targets: null pointer or bad size");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(K_LOSS_TARGETS, cs, [&] { return launch_loss_targets(ids, cu, B, T, ignore_index, targets, cs); });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "loss_targets");
+}
+
+size_t varlen_token_ce_workspace_size(int32_t T) {
+  return T < 0 ? 0 : align256(sizeof(WsHeader) + static_cast<size_t>(T) * sizeof(float));
+}
+
+va_status varlen_token_ce(const void* logits, int32_t dtype, int64_t l_rs, const int32_t* targets, int32_t T,
+                          int32_t V, int32_t ignore_index, double* loss, int32_t* count, void* grad, int64_t g_rs,
+                          void* ws, size_t ws_bytes, va_stream_t stream) {
+  if (!logits || !targets || !loss || !count || !ws) return fail(VA_ERR_INVALID_ARG, "token_ce: null pointer");
+  if (T < 1 || V < 1 || (dtype != 0 && dtype != 1)) return fail(VA_ERR_INVALID_ARG, "token_ce: T, V >= 1, dtype 0 or 1");
+  if (l_rs < V || (grad && g_rs < V)) return fail(VA_ERR_INVALID_ARG, "token_ce: row strides must be >= V");
+  if (!aligned16(ws)) return fail(VA_ERR_INVALID_ARG, "token_ce: workspace must be 16-byte aligned");
+  if (ws_bytes < varlen_token_ce_workspace_size(T)) return fail(VA_ERR_WORKSPACE, "token_ce: workspace too small");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  float* nll = reinterpret_cast<float*>(w + sizeof(WsHeader));
+  cudaError_t e = cudaSuccess;
+  const KernelId ids[3] = {K_CE_COUNT, K_CE_ROWS, K_CE_REDUCE};
+  for (int stage = 0; stage < 3 && e == cudaSuccess; ++stage)
+    e = launch(ids[stage], cs, [&] {
+      return launch_token_ce(stage, logits, dtype, l_rs, targets, T, V, ignore_index, grad, g_rs, nll, count,
+                             &hdr->status, loss, cs);
+    });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "token_ce");
 }
 
 va_status varlen_read_status(const void* ws, int32_t* out, va_stream_t stream) {

@@ -115,3 +115,21 @@ def test_host_side_argument_errors(va):
     s3 = va._lib.VaShape()
     lib.varlen_shape_contiguous(ctypes.byref(s3), 16, 1, 2, 2, 64, 17)
     assert lib.varlen_attn_workspace_size(ctypes.byref(s3), 0) == 0
+
+
+def test_loss_entry_points_reject_bad_arguments(va):
+    """The packed-loss entry points check their arguments on the host."""
+    lib = va._lib.load()
+    p = ctypes.c_void_p(16)
+    assert lib.varlen_token_ce_workspace_size(1000) == 256 + 4096  # header + 4 bytes a row, 256-aligned
+    assert lib.varlen_token_ce_workspace_size(-1) == 0
+    ws = lib.varlen_token_ce_workspace_size(8)
+    assert lib.varlen_loss_targets(None, p, 1, 8, -100, p, None) == 1
+    assert lib.varlen_loss_targets(p, p, 0, 8, -100, p, None) == 1
+    # null logits, bad dtype, stride below V, misaligned or small workspace
+    assert lib.varlen_token_ce(None, 1, 64, p, 8, 64, -100, p, p, None, 0, p, ws, None) == 1
+    assert lib.varlen_token_ce(p, 2, 64, p, 8, 64, -100, p, p, None, 0, p, ws, None) == 1
+    assert lib.varlen_token_ce(p, 1, 63, p, 8, 64, -100, p, p, None, 0, p, ws, None) == 1
+    assert lib.varlen_token_ce(p, 1, 64, p, 8, 64, -100, p, p, p, 32, p, ws, None) == 1
+    assert lib.varlen_token_ce(p, 1, 64, p, 8, 64, -100, p, p, None, 0, ctypes.c_void_p(24), ws, None) == 1
+    assert lib.varlen_token_ce(p, 1, 64, p, 8, 64, -100, p, p, None, 0, p, ws - 16, None) == 3
