@@ -22,6 +22,9 @@
 * ``packed_storage_rows`` -- the course's storage rows (inputs, targets,
   occurrence segments, local positions, validity) for next-fit placements
   ("Fill only the current row").
+* ``unpad_index`` / ``gather_rows`` -- the padded-batch bridge of blog section 4
+  (a 2-D attention mask: drop the padding, run the varlen kernel, scatter the output
+  back to the padded shape).
 """
 from __future__ import annotations
 
@@ -173,3 +176,40 @@ def packed_storage_rows(inputs, targets, capacity: int):
         rows["input_valid"].append(r_val)
         rows["target_valid"].append(list(r_val))
     return rows
+
+
+def unpad_index(mask):
+    """Padded batch -> packed stream (blog section 4, the padded-batch path).
+
+    ``mask`` [Bp, S]: nonzero marks a real token.  Each row's real tokens, in order, become
+    one segment; a row without a real token is an error (it would be an empty segment, and
+    cu_seqlens must be strictly increasing, blog section 3).  Returns (indices [Bp*S]:
+    flat positions r*S + s of the T real tokens in row-major order, then -1 for the padding
+    slots; inverse [Bp*S]: packed index of each position or -1; cu_seqlens [Bp+1]; T;
+    max_seqlen).
+    """
+    m = np.asarray(mask).astype(bool)
+    Bp, S = m.shape
+    lens = m.sum(axis=1)
+    if (lens == 0).any():
+        raise ValueError("a row without real tokens would be an empty segment")
+    real = [r * S + s for r in range(Bp) for s in range(S) if m[r, s]]
+    T = len(real)
+    indices = np.full(Bp * S, -1, dtype=np.int64)
+    indices[:T] = real
+    inverse = np.full(Bp * S, -1, dtype=np.int64)
+    for i, flat in enumerate(real):
+        inverse[flat] = i
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    return indices, inverse, cu, T, int(lens.max())
+
+
+def gather_rows(src, row_map):
+    """dst[i] = src[row_map[i]] for row_map[i] >= 0, else a zero row (unpad with the indices,
+    pad with the inverse map)."""
+    src = np.asarray(src)
+    dst = np.zeros((len(row_map),) + src.shape[1:], dtype=src.dtype)
+    for i, r in enumerate(row_map):
+        if r >= 0:
+            dst[i] = src[r]
+    return dst

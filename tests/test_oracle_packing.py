@@ -353,3 +353,41 @@ def test_tile_map_order_small_example():
     assert tb[:, 0].tolist() == [1] * 8 + [0] * 3
     assert tb[:8, 3].tolist() == [16, 14, 12, 10, 8, 6, 4, 2]
     assert tb[8:, 3].tolist() == [5, 3, 1]
+
+
+@pytest.mark.parametrize("layout", ["right", "left", "holes"])
+def test_unpad_pad_bridge(layout):
+    """Blog section 4's padded-batch path: per row the real tokens, in order, form one segment;
+    pad(unpad(x)) keeps the real tokens and zeroes the padding; and varlen attention over the
+    unpadded stream equals each row's attention over its own real tokens, whatever the padding
+    side (brute force per row)."""
+    from oracle import attention as oa
+    rng = np.random.default_rng({"right": 1, "left": 2, "holes": 3}[layout])
+    Bp, S, H, d = 4, 9, 2, 8
+    lens = [9, 3, 6, 1]
+    mask = np.zeros((Bp, S), dtype=np.int32)
+    for r, L in enumerate(lens):
+        if layout == "right":
+            mask[r, :L] = 1
+        elif layout == "left":
+            mask[r, S - L:] = 1
+        else:
+            mask[r, rng.choice(S, L, replace=False)] = 1
+    idx, inv, cu, T, mx = op.unpad_index(mask)
+    assert T == sum(lens) and list(cu) == [0, 9, 12, 18, 19] and mx == 9
+    assert (idx[T:] == -1).all() and sorted(idx[:T]) == list(idx[:T])
+    assert all(inv[f] == i for i, f in enumerate(idx[:T])) and (inv >= 0).sum() == T
+    x = rng.standard_normal((Bp * S, H, d))
+    packed = op.gather_rows(x, idx[:T])
+    back = op.gather_rows(packed, inv)
+    assert np.array_equal(back, x * mask.reshape(-1, 1, 1))
+    q, k, v = (rng.standard_normal((Bp, S, H, d)) for _ in range(3))
+    pq, pk, pv = (op.gather_rows(t.reshape(Bp * S, H, d), idx[:T]) for t in (q, k, v))
+    o, _ = oa.varlen_forward(pq, pk, pv, cu)
+    out = op.gather_rows(o, inv).reshape(Bp, S, H, d)
+    for r in range(Bp):
+        sel = mask[r].astype(bool)
+        ro, _ = oa.segment_forward(q[r, sel], k[r, sel], v[r, sel], 1 / np.sqrt(d))
+        assert np.allclose(out[r, sel], ro, atol=1e-12) and (out[r, ~sel] == 0).all()
+    with pytest.raises(ValueError):
+        op.unpad_index(np.array([[1, 0], [0, 0]]))
