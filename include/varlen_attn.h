@@ -261,6 +261,34 @@ va_status varlen_read_status(const void* ws_dev, int32_t* status_host, va_stream
 /* Clears the workspace status word (asynchronous). */
 va_status varlen_clear_status(void* ws_dev, va_stream_t stream);
 
+/* ---------------------------------------------------------------- padded-batch bridge
+ * A batch padded to [Bp, S] with a 2-D attention mask enters the varlen path by dropping its
+ * padding, and the packed output goes back to the padded shape.  Source: "Packing与
+ * FlashAttention Varlen", section 4 (the padded-batch branch: remove the padding, run the
+ * varlen kernel, scatter the output back).  Each row's real tokens, in order, form one
+ * segment, so left, right or scattered padding all work.
+ *   mask_dev        int32 [Bp, S] in: nonzero marks a real token
+ *   indices_dev     int32 [Bp*S] out: the flat positions r*S + s of the T real tokens in
+ *                   row-major order, then -1 for every padding cell (gather map of unpad)
+ *   inverse_dev     int32 [Bp*S] out: each flat position's packed index, or -1 (pad map)
+ *   cu_seqlens_dev  int32 [Bp+1] out; T_dev, max_seqlen_dev int32 [1] out
+ *   status_dev      int32 [1] out: VA_OK, or VA_ERR_BAD_SEQLENS when a row has no real
+ *                   token (it would be an empty segment)
+ * Errors: VA_ERR_INVALID_ARG (null pointer, Bp < 1, S < 1, Bp*S >= 2^31).  Asynchronous. */
+va_status varlen_unpad_index(const int32_t* mask_dev, int32_t Bp, int32_t S, int32_t* indices_dev,
+                             int32_t* inverse_dev, int32_t* cu_seqlens_dev, int32_t* T_dev,
+                             int32_t* max_seqlen_dev, int32_t* status_dev, va_stream_t stream);
+
+/* Row gather: dst row i = src row map[i], or a zero row where map[i] < 0, for i < n_rows.
+ * With varlen_unpad_index's indices it unpads ([Bp*S, row] -> [T, row]); with its inverse
+ * map it pads the packed output back ([T, row] -> [Bp*S, row], zeros in the padding).
+ *   row_bytes, src/dst_row_stride_bytes  positive multiples of 16 (strides >= row_bytes)
+ *   src_dev, dst_dev                     16-byte aligned; map_dev int32 [n_rows]
+ * Errors: VA_ERR_INVALID_ARG.  Asynchronous. */
+va_status varlen_gather_rows(const void* src_dev, int64_t src_row_stride_bytes, const int32_t* map_dev,
+                             int32_t n_rows, int64_t row_bytes, void* dst_dev, int64_t dst_row_stride_bytes,
+                             va_stream_t stream);
+
 /* ---------------------------------------------------------------- packed loss
  * Next-token targets of a packed stream of whole documents.  Source: "Pack sequences
  * without joining their contexts", "Form pairs inside each source range" (a document of L

@@ -22,7 +22,7 @@ __all__ = [
     "pack_next_fit", "pack_best_fit_decreasing", "build_metadata", "validate_cu_seqlens",
     "tile_sizes", "workspace_size", "plan", "varlen_attn_fwd", "varlen_attn_bwd", "varlen_attn",
     "read_status", "VarlenError", "make_shape", "library_path", "loss_targets", "token_ce",
-    "IGNORE_INDEX",
+    "IGNORE_INDEX", "unpad_index", "gather_rows", "unpad", "pad",
 ]
 
 
@@ -315,3 +315,52 @@ def token_ce(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = IG
     if check_status:
         _raise_status(workspace)
     return loss, count, g
+
+
+# ----------------------------------------------------------------- padded-batch bridge
+
+def unpad_index(mask: torch.Tensor):
+    """Padded batch -> packed stream.  ``mask`` CUDA [Bp, S] (nonzero = real token).  Returns
+    (indices [Bp*S], inverse [Bp*S], cu_seqlens [Bp+1] (int32 device tensors), T, max_seqlen);
+    T and max_seqlen are read back to the host (one synchronisation), as the attention calls
+    take them on the host.  A row without real tokens raises (status VA_ERR_BAD_SEQLENS)."""
+    if not mask.is_cuda or mask.dim() != 2:
+        raise ValueError("mask must be a CUDA [Bp, S] tensor")
+    m = mask.to(torch.int32).contiguous()
+    Bp, S = m.shape
+    dev = m.device
+    indices = torch.empty(Bp * S, dtype=torch.int32, device=dev)
+    inverse = torch.empty(Bp * S, dtype=torch.int32, device=dev)
+    cu = torch.empty(Bp + 1, dtype=torch.int32, device=dev)
+    small = torch.empty(3, dtype=torch.int32, device=dev)  # T, max_seqlen, status
+    check(_lib.load().varlen_unpad_index(_ptr(m), Bp, S, _ptr(indices), _ptr(inverse), _ptr(cu),
+                                         ctypes.c_void_p(small.data_ptr()),
+                                         ctypes.c_void_p(small.data_ptr() + 4),
+                                         ctypes.c_void_p(small.data_ptr() + 8), _stream(dev)))
+    T, mx, st = (int(x) for x in small.cpu())
+    if st != 0:
+        raise VarlenError(st, "unpad_index: a row has no real token")
+    return indices, inverse, cu, T, mx
+
+
+def gather_rows(src: torch.Tensor, row_map: torch.Tensor, n_rows: int) -> torch.Tensor:
+    """dst[i] = src[row_map[i]] (a zero row where row_map[i] < 0) for i < n_rows; rows are
+    src's trailing dims (contiguous, a multiple of 16 bytes)."""
+    if not src.is_cuda or src.dim() < 1 or not src[0].is_contiguous():
+        raise ValueError("src must be a CUDA tensor with contiguous rows")
+    row_bytes = src[0].numel() * src.element_size()
+    dst = torch.empty((n_rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    check(_lib.load().varlen_gather_rows(_ptr(src), src.stride(0) * src.element_size(), _ptr(row_map), n_rows,
+                                         row_bytes, _ptr(dst), dst.stride(0) * dst.element_size(),
+                                         _stream(src.device)))
+    return dst
+
+
+def unpad(x: torch.Tensor, indices: torch.Tensor, T: int) -> torch.Tensor:
+    """[Bp, S, ...] -> [T, ...]: the real tokens in row-major order."""
+    return gather_rows(x.reshape((-1,) + tuple(x.shape[2:])), indices, T)
+
+
+def pad(y: torch.Tensor, inverse: torch.Tensor, Bp: int, S: int) -> torch.Tensor:
+    """[T, ...] -> [Bp, S, ...]: each token back to its padded position, zeros in the padding."""
+    return gather_rows(y, inverse, Bp * S).reshape((Bp, S) + tuple(y.shape[1:]))

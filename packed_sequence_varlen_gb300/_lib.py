@@ -27,6 +27,7 @@ EXPORTS = (
     "varlen_profile_enable", "varlen_profile_read", "varlen_kernel_name", "varlen_launch_count",
     "varlen_attn_fwd_noalloc", "varlen_cu_seqlens_from_positions",
     "varlen_loss_targets", "varlen_token_ce_workspace_size", "varlen_token_ce",
+    "varlen_unpad_index", "varlen_gather_rows",
 )
 
 
@@ -74,6 +75,10 @@ def _declare(lib):
         "varlen_attn_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                               POINTER(VaShape), c_float, c_int32, c_void_p,
                                               c_void_p, c_void_p]),
+        "varlen_unpad_index": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p]),
+        "varlen_gather_rows": (c_int32, [c_void_p, c_int64, c_void_p, c_int32, c_int64, c_void_p, c_int64,
+                                         c_void_p]),
         "varlen_loss_targets": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p,
                                           c_void_p]),
         "varlen_token_ce_workspace_size": (c_size_t, [c_int32]),

@@ -25,6 +25,9 @@ void fwd_tc_tiles(int*, int*);
 int fwd_tc_token_short();
 int bwd_tc_token_short();
 cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, cudaStream_t);
+cudaError_t launch_unpad_index(int, const int32_t*, int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
+                               int32_t*, cudaStream_t);
+cudaError_t launch_gather_rows(const void*, int64_t, const int32_t*, int, int64_t, void*, int64_t, cudaStream_t);
 cudaError_t launch_loss_targets(const int32_t*, const int32_t*, int, int, int, int32_t*, cudaStream_t);
 cudaError_t launch_token_ce(int, const void*, int, int64_t, const int32_t*, int, int, int, void*, int64_t, float*,
                             int32_t*, int32_t*, double*, cudaStream_t);
@@ -39,12 +42,14 @@ void set_error(const char* msg) { g_error = msg; }
 // ------------------------------------------------------------ launch accounting
 enum KernelId {
   K_VALIDATE = 0, K_META_SCAN, K_META_FILL, K_PLAN, K_FWD, K_BWD_PREP, K_BWD_DKDV, K_BWD_DQ,
-  K_VALIDATE_PLAN, K_FWD_TOK, K_CU_FROM_POS, K_LOSS_TARGETS, K_CE_COUNT, K_CE_ROWS, K_CE_REDUCE, K_COUNT
+  K_VALIDATE_PLAN, K_FWD_TOK, K_CU_FROM_POS, K_LOSS_TARGETS, K_CE_COUNT, K_CE_ROWS, K_CE_REDUCE, K_PAD_COUNT,
+  K_PAD_SCAN, K_PAD_INDEX, K_GATHER_ROWS, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "validate_cu_seqlens", "metadata_scan", "metadata_fill", "plan",          "fwd",
     "bwd_prep",            "bwd_dkdv",      "bwd_dq",        "validate_plan", "fwd_tok",
-    "cu_from_positions",   "loss_targets",  "ce_count",      "ce_rows",       "ce_reduce"};
+    "cu_from_positions",   "loss_targets",  "ce_count",      "ce_rows",       "ce_reduce",
+    "pad_count",           "pad_scan",      "pad_index",     "gather_rows"};
 
 struct Profiler {
   std::vector<cudaEvent_t> start, stop;
@@ -427,6 +432,35 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   if (e == cudaSuccess)
     e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq_tc(p, s->d, static_cast<int>(L.cap_q), tok, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd kernels");
+}
+
+va_status varlen_unpad_index(const int32_t* mask, int32_t Bp, int32_t S, int32_t* indices, int32_t* inverse,
+                             int32_t* cu, int32_t* T_out, int32_t* max_out, int32_t* status, va_stream_t stream) {
+  if (!mask || !indices || !inverse || !cu || !T_out || !max_out || !status)
+    return fail(VA_ERR_INVALID_ARG, "unpad_index: null pointer");
+  if (Bp < 1 || S < 1 || static_cast<int64_t>(Bp) * S >= (int64_t(1) << 31))
+    return fail(VA_ERR_INVALID_ARG, "unpad_index: Bp >= 1, S >= 1 and Bp * S < 2^31");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const KernelId ids[3] = {K_PAD_COUNT, K_PAD_SCAN, K_PAD_INDEX};
+  cudaError_t e = cudaSuccess;
+  for (int stage = 0; stage < 3 && e == cudaSuccess; ++stage)
+    e = launch(ids[stage], cs, [&] {
+      return launch_unpad_index(stage, mask, Bp, S, indices, inverse, cu, T_out, max_out, status, cs);
+    });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "unpad_index");
+}
+
+va_status varlen_gather_rows(const void* src, int64_t src_stride, const int32_t* map, int32_t n_rows, int64_t row_bytes,
+                             void* dst, int64_t dst_stride, va_stream_t stream) {
+  if (!src || !map || !dst || n_rows < 0) return fail(VA_ERR_INVALID_ARG, "gather_rows: null pointer or n_rows < 0");
+  if (row_bytes <= 0 || row_bytes % 16 || src_stride % 16 || dst_stride % 16 || src_stride < row_bytes ||
+      dst_stride < row_bytes || !aligned16(src) || !aligned16(dst))
+    return fail(VA_ERR_INVALID_ARG, "gather_rows: rows, strides and pointers must be 16-byte multiples");
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch(K_GATHER_ROWS, cs, [&] {
+    return launch_gather_rows(src, src_stride, map, n_rows, row_bytes, dst, dst_stride, cs);
+  });
+  return e == cudaSuccess ? VA_OK : cuda_fail(e, "gather_rows");
 }
 
 va_status varlen_loss_targets(const int32_t* ids, const int32_t* cu, int32_t B, int32_t T, int32_t ignore_index,

@@ -133,3 +133,16 @@ def test_loss_entry_points_reject_bad_arguments(va):
     assert lib.varlen_token_ce(p, 1, 64, p, 8, 64, -100, p, p, p, 32, p, ws, None) == 1
     assert lib.varlen_token_ce(p, 1, 64, p, 8, 64, -100, p, p, None, 0, ctypes.c_void_p(24), ws, None) == 1
     assert lib.varlen_token_ce(p, 1, 64, p, 8, 64, -100, p, p, None, 0, p, ws - 16, None) == 3
+
+
+def test_bridge_entry_points_reject_bad_arguments(va):
+    """The padded-batch bridge checks its arguments on the host."""
+    lib = va._lib.load()
+    p = ctypes.c_void_p(16)
+    assert lib.varlen_unpad_index(None, 2, 8, p, p, p, p, p, p, None) == 1
+    assert lib.varlen_unpad_index(p, 0, 8, p, p, p, p, p, p, None) == 1
+    assert lib.varlen_unpad_index(p, 65536, 65536, p, p, p, p, p, p, None) == 1  # Bp * S >= 2^31
+    assert lib.varlen_gather_rows(p, 64, p, 4, 24, p, 64, None) == 1     # row not a multiple of 16
+    assert lib.varlen_gather_rows(p, 16, p, 4, 32, p, 64, None) == 1     # stride below the row
+    assert lib.varlen_gather_rows(ctypes.c_void_p(8), 64, p, 4, 32, p, 64, None) == 1  # misaligned
+    assert lib.varlen_gather_rows(p, 64, p, -1, 32, p, 64, None) == 1
