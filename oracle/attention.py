@@ -23,6 +23,11 @@ Backward, given dO (analytic gradient of the definition above):
 
 and dK, dV sum over the q heads that share a kv head.
 
+Local window ("Packing与 FlashAttention Varlen", section 5: a local window further
+narrows the key blocks a query block may see): with ``window = w`` (causal only),
+query i sees the keys i - w <= j <= i of its segment, i.e. itself and the w keys
+before it (FlashAttention's left window size; its right size is 0 under causality).
+
 The GQA head mapping h -> h // (Hq/Hkv) is not on the pages; it is the plainest
 reading (consecutive q heads share a kv head).  Rows of long segments are
 processed in blocks only to bound memory; each block computes full rows.
@@ -55,11 +60,27 @@ def _expand(x: np.ndarray, g: int) -> np.ndarray:
     return np.repeat(x, g, axis=1).transpose(1, 0, 2)
 
 
-def segment_forward(q, k, v, scale: float, causal: bool = True):
+def _visible(i, j, causal: bool, window):
+    """Permission of query rows i (column vector) on key columns j (row vector)."""
+    if not causal:
+        return np.ones(np.broadcast(i, j).shape, dtype=bool)
+    vis = j <= i
+    if window is not None:
+        vis = vis & (j >= i - window)
+    return vis
+
+
+def _check_window(causal: bool, window):
+    if window is not None and (not causal or window < 0):
+        raise ValueError("a local window needs causal attention and window >= 0")
+
+
+def segment_forward(q, k, v, scale: float, causal: bool = True, window=None):
     """One segment, all heads.  q [l,Hq,d], k/v [l,Hkv,d] (float64).
 
     Returns (o [l,Hq,d], lse [Hq,l]).
     """
+    _check_window(causal, window)
     l, Hq, d = q.shape
     g = Hq // k.shape[1]
     Q = q.transpose(1, 0, 2)
@@ -75,7 +96,7 @@ def segment_forward(q, k, v, scale: float, causal: bool = True):
         if causal:
             i = np.arange(r0, r1)[:, None]
             j = np.arange(kend)[None, :]
-            s = np.where(j <= i, s, -np.inf)
+            s = np.where(_visible(i, j, causal, window), s, -np.inf)
         mx = s.max(axis=2, keepdims=True)
         e = np.exp(s - mx)
         z = e.sum(axis=2, keepdims=True)
@@ -84,12 +105,13 @@ def segment_forward(q, k, v, scale: float, causal: bool = True):
     return o.transpose(1, 0, 2), lse
 
 
-def segment_backward(q, k, v, o, lse, do, scale: float, causal: bool = True):
+def segment_backward(q, k, v, o, lse, do, scale: float, causal: bool = True, window=None):
     """Analytic backward of ``segment_forward`` for one segment.
 
     ``o``/``lse`` are this oracle's own forward results.  Returns (dq, dk, dv)
     with the shapes of q, k, v.
     """
+    _check_window(causal, window)
     l, Hq, d = q.shape
     Hkv = k.shape[1]
     g = Hq // Hkv
@@ -110,7 +132,7 @@ def segment_backward(q, k, v, o, lse, do, scale: float, causal: bool = True):
         if causal:
             i = np.arange(r0, r1)[:, None]
             j = np.arange(kend)[None, :]
-            p = np.where(j <= i, p, 0.0)
+            p = np.where(_visible(i, j, causal, window), p, 0.0)
         dVx[:, :kend] += p.transpose(0, 2, 1) @ dO[:, r0:r1]
         dp = dO[:, r0:r1] @ V[:, :kend].transpose(0, 2, 1)
         ds = p * (dp - D[:, r0:r1, None])
@@ -129,7 +151,7 @@ def _head_slices(Hq: int, Hkv: int, kv_heads):
     return kv_heads, g
 
 
-def varlen_forward(q, k, v, cu_seqlens, scale=None, causal=True, kv_heads=None):
+def varlen_forward(q, k, v, cu_seqlens, scale=None, causal=True, kv_heads=None, window=None):
     """Packed forward: every segment of ``cu_seqlens`` is its own attention.
 
     q [T,Hq,d], k/v [T,Hkv,d] float64.  Returns (o [T,Hq,d], lse [Hq,T]).
@@ -150,14 +172,14 @@ def varlen_forward(q, k, v, cu_seqlens, scale=None, causal=True, kv_heads=None):
         for hk in kvh:
             hq = slice(hk * g, (hk + 1) * g)
             ob, lb = segment_forward(q[s:e, hq], k[s:e, hk:hk + 1], v[s:e, hk:hk + 1],
-                                     scale, causal)
+                                     scale, causal, window)
             o[s:e, hq] = ob
             lse[hq, s:e] = lb
     return o, lse
 
 
 def varlen_backward(q, k, v, o, lse, do, cu_seqlens, scale=None, causal=True,
-                    kv_heads=None):
+                    kv_heads=None, window=None):
     """Packed backward (dq, dk, dv); entries of heads outside ``kv_heads`` are NaN."""
     T, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -173,7 +195,7 @@ def varlen_backward(q, k, v, o, lse, do, cu_seqlens, scale=None, causal=True,
             hq = slice(hk * g, (hk + 1) * g)
             a, bk, c = segment_backward(q[s:e, hq], k[s:e, hk:hk + 1], v[s:e, hk:hk + 1],
                                         o[s:e, hq], lse[hq, s:e], do[s:e, hq],
-                                        scale, causal)
+                                        scale, causal, window)
             dq[s:e, hq] = a
             dk[s:e, hk:hk + 1] = bk
             dv[s:e, hk:hk + 1] = c

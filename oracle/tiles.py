@@ -39,6 +39,13 @@ holds row t0.  Its record is (-1 - f, t0, h, rows), and the token records follow
 every segment record, ordered by (t0, h).  Segments covered by token tiles have
 no segment records.  The dK/dV map cuts the same runs into BN-row tiles of key
 rows: key j of a tile is seen by the queries [j, end of its segment).
+
+Local window w (causal; section 5: "causal or local window further narrows
+n_block_min/max"): q block m's key blocks run from n_min = floor(max(0, m*BM - w) / BN)
+to its diagonal, count = n_max - n_min; kv block n's q blocks run from its diagonal
+floor(n*BN / BM) to floor((n*BN + BN - 1 + w) / BM) (capped by the segment).  Window
+maps have no token records and keep each segment's blocks in block order (q blocks
+descending, kv blocks ascending), which is the no-window order as well.
 """
 from __future__ import annotations
 
@@ -53,12 +60,23 @@ def _cost_class(c: int) -> int:
     return c.bit_length() - 1          # floor(log2(c)) for c >= 1
 
 
-def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, short: int = 0):
+def window_key_start(m: int, BM: int, BN: int, window) -> int:
+    """First key block of q block m under a local window (0 without one)."""
+    return 0 if window is None else max(0, m * BM - window) // BN
+
+
+def window_q_end(n: int, l: int, BM: int, BN: int, window) -> int:
+    """One past the last q block that sees kv block n (the segment's last block without a window)."""
+    Mq = _ceil(l, BM)
+    return Mq if window is None else min(Mq, (n * BN + BN - 1 + window) // BM + 1)
+
+
+def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, short: int = 0, window=None):
     """Items as an int32 array [N, 4], in the order above: segment records
     (b, m, h, n_blocks), then (causal, short > 0) token records (-1 - f, t0, h, rows)."""
     cu = [int(x) for x in cu_seqlens]
     B = len(cu) - 1
-    tok = [causal and short > 0 and cu[b + 1] - cu[b] <= short for b in range(B)]
+    tok = [causal and short > 0 and window is None and cu[b + 1] - cu[b] <= short for b in range(B)]
     items = []
     for b in range(B):
         if tok[b]:
@@ -67,23 +85,23 @@ def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, sho
         blocks = []
         for m in range(_ceil(l, BM)):
             nb = _ceil(min(l, (m + 1) * BM), BN) if causal else _ceil(l, BN)
-            blocks.append((m, nb))
+            blocks.append((m, nb - window_key_start(m, BM, BN, window)))
         cls = _cost_class(sum(nb for _, nb in blocks))
         for h in range(Hq):
             for m, nb in blocks:
-                items.append(((-cls, b, h, -nb, m), (b, m, h, nb)))
+                items.append(((-cls, b, h, -m if window is not None else -nb, m), (b, m, h, nb)))
     items.sort(key=lambda t: t[0])
     out = [r for _, r in items] + _token_records(cu, tok, Hq, BM)
     return np.asarray(out, dtype=np.int32).reshape(-1, 4)
 
 
-def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True, short: int = 0):
+def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True, short: int = 0, window=None):
     """Items as an int32 array [N, 4], in the order above: segment records
     (b, n, h_kv, n_q), then (causal, short > 0) token records (-1 - f, t0, h_kv, rows)
     whose BN-row tiles hold the key rows [t0, t0 + rows) of a run of short segments."""
     cu = [int(x) for x in cu_seqlens]
     B = len(cu) - 1
-    tok = [causal and short > 0 and cu[b + 1] - cu[b] <= short for b in range(B)]
+    tok = [causal and short > 0 and window is None and cu[b + 1] - cu[b] <= short for b in range(B)]
     items = []
     for b in range(B):
         if tok[b]:
@@ -93,11 +111,11 @@ def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True, sh
         blocks = []
         for n in range(_ceil(l, BN)):
             m_start = (n * BN) // BM if causal else 0
-            blocks.append((n, Mq - m_start))
+            blocks.append((n, window_q_end(n, l, BM, BN, window) - m_start))
         cls = _cost_class(sum(nq for _, nq in blocks))
         for h in range(Hkv):
             for n, nq in blocks:
-                items.append(((-cls, b, h, -nq, n), (b, n, h, nq)))
+                items.append(((-cls, b, h, n if window is not None else -nq, n), (b, n, h, nq)))
     items.sort(key=lambda t: t[0])
     return np.asarray([r for _, r in items] + _token_records(cu, tok, Hkv, BN), dtype=np.int32).reshape(-1, 4)
 
@@ -121,7 +139,7 @@ def _token_records(cu, tok, H, rows_per_tile):
     return out
 
 
-def bwd_item_edges(cu_seqlens, item, BM: int, BN: int):
+def bwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None):
     """(query, key) token pairs a backward kv item's tiles cover, in global indices."""
     b, n, _h, nq = (int(x) for x in item)
     cu = [int(x) for x in cu_seqlens]
@@ -131,13 +149,13 @@ def bwd_item_edges(cu_seqlens, item, BM: int, BN: int):
         end = min(cu[x + 1] for x in range(len(cu) - 1) if cu[x + 1] > last)
         return [(i, j) for j in range(t0, t0 + rows) for i in range(t0, end)]
     s, l = cu[b], cu[b + 1] - cu[b]
-    m0 = -(-l // BM) - nq
+    m0 = window_q_end(n, l, BM, BN, window) - nq
     cols = range(s + n * BN, s + min(l, (n + 1) * BN))
-    rows = range(s + m0 * BM, s + l)
+    rows = range(s + m0 * BM, s + min(l, (m0 + nq) * BM))
     return [(i, j) for i in rows for j in cols]
 
 
-def fwd_item_edges(cu_seqlens, item, BM: int, BN: int):
+def fwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None):
     """(query, key) token pairs a forward item's tiles cover, in global indices."""
     b, m, _h, nb = (int(x) for x in item)
     if b < 0:                                     # token record (-1 - f, t0, h, rows)
@@ -146,8 +164,9 @@ def fwd_item_edges(cu_seqlens, item, BM: int, BN: int):
         return [(i, j) for i in range(t0, t0 + rows) for j in range(kb, t0 + rows)]
     s = int(cu_seqlens[b])
     l = int(cu_seqlens[b + 1]) - s
+    n0 = window_key_start(m, BM, BN, window)
     rows = range(s + m * BM, s + min(l, (m + 1) * BM))
-    cols = range(s, s + min(l, nb * BN))
+    cols = range(s + n0 * BN, s + min(l, (n0 + nb) * BN))
     return [(i, j) for i in rows for j in cols]
 
 

@@ -327,3 +327,51 @@ def test_key_rows_sampler_matches_full_oracle(causal):
         rk, rv = oa.key_rows_backward(q, k, v, do, cu, toks, hk, 0.3, causal)
         assert close(rk, dk[toks, hk], 1e-12, 1e-10)
         assert close(rv, dv[toks, hk], 1e-12, 1e-10)
+
+
+@pytest.mark.parametrize("w", [0, 1, 3, 7])
+def test_local_window_against_banded_sdpa(w):
+    """Local window w: each segment equals torch's float64 SDPA under a band mask built from
+    two triangles (tril(0) minus tril(-(w+1))), forward and autograd backward."""
+    cu, pos, seg, q, k, v, do = random_pack(50 + w, T_max=60)
+    scale = 0.29
+    o, lse = oa.varlen_forward(q, k, v, cu, scale, window=w)
+    dq, dk, dv = oa.varlen_backward(q, k, v, o, lse, do, cu, scale, window=w)
+    for b in range(len(cu) - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        l = e - s
+        ones = torch.ones(l, l, dtype=torch.bool)
+        band = torch.tril(ones) & ~torch.tril(ones, diagonal=-(w + 1))
+        tq, tk, tv = (torch.tensor(x[s:e].transpose(1, 0, 2), requires_grad=True) for x in (q, k, v))
+        g = tq.shape[0] // tk.shape[0]
+        to = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk.repeat_interleave(g, 0), tv.repeat_interleave(g, 0), attn_mask=band, scale=scale)
+        (to * torch.tensor(do[s:e].transpose(1, 0, 2))).sum().backward()
+        assert close(o[s:e], to.detach().numpy().transpose(1, 0, 2), 1e-12, 1e-10)
+        assert close(dq[s:e], tq.grad.numpy().transpose(1, 0, 2), 1e-12, 1e-9)
+        assert close(dk[s:e], tk.grad.numpy().transpose(1, 0, 2), 1e-12, 1e-9)
+        assert close(dv[s:e], tv.grad.numpy().transpose(1, 0, 2), 1e-12, 1e-9)
+
+
+def test_local_window_closed_forms():
+    """w = 0: a query sees only itself (O = v, LSE = scale q.k); w >= the longest segment: no
+    window; w = 1 by hand: query 2 of a segment mixes v_1 and v_2 with weights
+    softmax(scale q_2.k_1, scale q_2.k_2)."""
+    cu, pos, seg, q, k, v, do = random_pack(77, T_max=50, Hq=2, Hkv=2)
+    scale = 0.5
+    o0, l0 = oa.varlen_forward(q, k, v, cu, scale, window=0)
+    assert close(o0, v, 1e-12, 1e-12)
+    assert close(l0, scale * np.einsum("thc,thc->ht", q, k), 1e-12, 1e-12)
+    big = int(np.diff(cu).max())
+    ow, lw = oa.varlen_forward(q, k, v, cu, scale, window=big)
+    on, ln = oa.varlen_forward(q, k, v, cu, scale)
+    assert np.array_equal(ow, on) and np.array_equal(lw, ln)
+    o1, _ = oa.varlen_forward(q, k, v, cu, scale, window=1)
+    b = int(np.argmax(np.diff(cu) >= 3))
+    t = int(cu[b]) + 2
+    for h in range(2):
+        a1, a2 = scale * q[t, h] @ k[t - 1, h], scale * q[t, h] @ k[t, h]
+        w1, w2 = np.exp(a1) / (np.exp(a1) + np.exp(a2)), np.exp(a2) / (np.exp(a1) + np.exp(a2))
+        assert close(o1[t, h], w1 * v[t - 1, h] + w2 * v[t, h], 1e-12, 1e-12)
+    with pytest.raises(ValueError):
+        oa.varlen_forward(q, k, v, cu, scale, causal=False, window=2)

@@ -391,3 +391,29 @@ def test_unpad_pad_bridge(layout):
         assert np.allclose(out[r, sel], ro, atol=1e-12) and (out[r, ~sel] == 0).all()
     with pytest.raises(ValueError):
         op.unpad_index(np.array([[1, 0], [0, 0]]))
+
+
+@pytest.mark.parametrize("BM,BN", [(2, 2), (4, 2), (2, 4), (256, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("w", [0, 1, 5, 100, 300])
+def test_window_tile_maps_cover_each_allowed_edge_once(BM, BN, w):
+    """Local window w (a query sees itself and the w keys before it): the forward (q-block)
+    and backward (kv-block) maps cover every permitted edge exactly once, every listed tile
+    holds a permitted edge, and a segment's blocks keep block order."""
+    lengths = [5, 1, 9, 3, 260, 130, 2, 700, 64, 3]
+    cu, _, _, _ = op.build_metadata(lengths)
+    cu = [int(x) for x in cu]
+    allowed = {(i, j) for (i, j) in _allowed_edges(cu)
+               if j >= i - w}
+    fm = ot.fwd_tile_map(cu, 1, BM, BN, True, 64, window=w)   # token tiles stay off
+    bm = ot.bwd_tile_map(cu, 1, BM, BN, True, 64, window=w)
+    assert (fm[:, 0] >= 0).all() and (bm[:, 0] >= 0).all()
+    for tm, edges in ((fm, ot.fwd_item_edges), (bm, ot.bwd_item_edges)):
+        seen = []
+        for it in tm:
+            hit = [e for e in edges(cu, it, BM, BN, window=w) if e in allowed]
+            assert hit, "a listed tile has no permitted edge"
+            seen.extend(hit)
+        assert sorted(seen) == sorted(allowed)
+        for b in set(int(x) for x in tm[:, 0]):
+            blk = [int(r[1]) for r in tm if r[0] == b]
+            assert blk == (sorted(blk, reverse=True) if tm is fm else sorted(blk))
