@@ -71,8 +71,19 @@ def load_peaks():
                 "source": "fallback"}
 
 
+WINDOW = None  # causal local window of the run (--window), None for none
+
+
 def edges(lengths):
-    return sum(l * (l + 1) // 2 for l in lengths)
+    """Causal in-segment edges: query i of a segment sees min(i, w) + 1 keys under a window w."""
+    if WINDOW is None:
+        return sum(l * (l + 1) // 2 for l in lengths)
+    w = WINDOW
+    tot = 0
+    for l in lengths:
+        m = min(l - 1, w)
+        tot += (m + 1) * (m + 2) // 2 + max(0, l - 1 - w) * (w + 1)
+    return tot
 
 
 def batch_packs(rank: int, planners):
@@ -225,8 +236,8 @@ def run_ours(args, rank, world, local_rank):
             o, lse, dq, dk, dv = outs[p]
             cu, _, _, _, _ = va.build_metadata(lens_dev[p], pad_to=T, T_capacity=T)
             cu = cu[:B[p] + 1]
-            va.varlen_attn_fwd(q, k, v, cu, mxs[p], None, True, out=o, lse=lse, workspace=ws_f)
-            va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs[p], None, True, dq=dq, dk=dk, dv=dv,
+            va.varlen_attn_fwd(q, k, v, cu, mxs[p], None, True, out=o, lse=lse, workspace=ws_f, window=WINDOW)
+            va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs[p], None, True, dq=dq, dk=dk, dv=dv, window=WINDOW,
                                workspace=ws_b)
 
     dist = None
@@ -326,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": round(max_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: {PACKS_PER_STEP} pack(s) of {T} tokens per step ({w.description}), "
-                               "causal, fwd+bwd",
+                               "causal" + (f", local window {WINDOW} (in-window FLOPs)" if WINDOW is not None else "")
+                               + ", fwd+bwd",
                    "tokens_per_step": PACKS_PER_STEP * T, "packs_per_step": PACKS_PER_STEP,
                    "l2": f"inputs larger than L2 ({T * (2 * Hq + 2 * Hkv) * d * 2 // 2**20} MB per pack)",
                    "parallelism": f"replicas x{world}",
@@ -394,8 +406,9 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
                 mxs = max(packs[p] + ([T - sum(packs[p])] if sum(packs[p]) < T else []))
                 cu = cu[:Bp + 1]
                 q, k, v, do = dev_in[b]
-                va.varlen_attn_fwd(q, k, v, cu, mxs, None, True, out=o, lse=lse)
-                va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs, None, True, dq=g[b][0], dk=g[b][1], dv=g[b][2])
+                va.varlen_attn_fwd(q, k, v, cu, mxs, None, True, out=o, lse=lse, window=WINDOW)
+                va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs, None, True, dq=g[b][0], dk=g[b][1], dv=g[b][2],
+                                   window=WINDOW)
                 done[p].record(s_cmp)
             with torch.cuda.stream(s_dn):
                 s_dn.wait_event(done[p])
@@ -440,8 +453,8 @@ def cpu_baseline(budget_s: float = 12.0, steps: int | None = None):
     while (steps is None and t_total < budget_s and heads < w.Hkv) or (steps is not None and heads < steps):
         h = heads % w.Hkv
         t0 = time.perf_counter()
-        o, lse = oa.varlen_forward(qq, kk, vv, cu, None, True, [h])
-        oa.varlen_backward(qq, kk, vv, o, lse, dd, cu, None, True, [h])
+        o, lse = oa.varlen_forward(qq, kk, vv, cu, None, True, [h], window=WINDOW)
+        oa.varlen_backward(qq, kk, vv, o, lse, dd, cu, None, True, [h], window=WINDOW)
         dt = time.perf_counter() - t0
         times.append(dt)
         t_total += dt
@@ -470,8 +483,8 @@ def run_reference(args, rank, world):
 
     def step(i):
         h = i % w.Hkv
-        o, lse = oa.varlen_forward(qq, kk, vv, cu, None, True, [h])
-        oa.varlen_backward(qq, kk, vv, o, lse, dd, cu, None, True, [h])
+        o, lse = oa.varlen_forward(qq, kk, vv, cu, None, True, [h], window=WINDOW)
+        oa.varlen_backward(qq, kk, vv, o, lse, dd, cu, None, True, [h], window=WINDOW)
 
     for i in range(args.warmup):
         step(i)
@@ -589,12 +602,15 @@ def main():
                     help="packs per step (16 is the benchmark; fewer for profiling cases)")
     ap.add_argument("--workload", choices=["sft8k", "gqa16k", "long64k", "tiny4k"], default="sft8k",
                     help="configuration (sft8k is the benchmark; the others are for measurement)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="causal local window (query i sees keys i-w..i); FLOPs count in-window edges")
     ap.add_argument("--loss", action="store_true",
                     help="measure the packed loss (targets + token-weighted CE + gradient) instead")
     ap.add_argument("--vocab", type=int, default=32768, help="classes of the --loss logits")
     args = ap.parse_args()
-    global WORKLOAD
+    global WORKLOAD, WINDOW
     WORKLOAD = args.workload
+    WINDOW = args.window
     PACKS_PER_STEP = args.packs
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -197,6 +197,19 @@ va_status varlen_attn_plan(const va_shape* shape, const int32_t* cu_seqlens_dev,
                            int32_t causal, int32_t* tile_map_dev, int32_t capacity,
                            int32_t* n_items_dev, int32_t* scratch_dev, va_stream_t stream);
 
+/* varlen_attn_plan for a causal local window of `window` keys (query i sees the keys
+ * i - window .. i of its segment; -1 = no window, as varlen_attn_plan).  Source:
+ * "Packing与 FlashAttention Varlen", section 5 (a local window narrows the key blocks a q
+ * block may enumerate, n_block_min/max).  q block m's key blocks start at
+ * floor(max(0, m*BM - window) / BN), count = blocks up to its diagonal; kv block n's q blocks
+ * stop after floor((n*BN + BN - 1 + window) / BM), count from its diagonal.  Window maps have
+ * no token records and keep each segment's blocks in block order (q blocks last-first, kv
+ * blocks first-first).  Errors as varlen_attn_plan, plus VA_ERR_INVALID_ARG for window < -1
+ * or a window without causal. */
+va_status varlen_attn_plan_window(const va_shape* shape, const int32_t* cu_seqlens_dev, int32_t kind,
+                                  int32_t causal, int32_t window, int32_t* tile_map_dev, int32_t capacity,
+                                  int32_t* n_items_dev, int32_t* scratch_dev, va_stream_t stream);
+
 /* ---------------------------------------------------------------- attention
  * Forward.  Source: "Packing与 FlashAttention Varlen", section 5 (each segment
  * b reads Q/K/V at offset cu[b]*row_stride with extent cu[b+1]-cu[b]; the
@@ -217,6 +230,17 @@ va_status varlen_attn_fwd(const void* q_dev, const void* k_dev, const void* v_de
                           int32_t causal, void* out_dev, float* lse_dev, void* ws_dev,
                           size_t ws_bytes, va_stream_t stream);
 
+/* varlen_attn_fwd with a causal local window: query i sees the keys i - window .. i of its
+ * segment (itself and the window keys before it; FlashAttention's left window size, its
+ * right size being 0 under causality); window = -1 is varlen_attn_fwd.  Source:
+ * "Packing与 FlashAttention Varlen", section 5 (causal or local window narrows the key
+ * blocks inside the segment's tile domain).  Workspace as varlen_attn_fwd.  Errors as
+ * varlen_attn_fwd, plus VA_ERR_INVALID_ARG for window < -1 or a window without causal. */
+va_status varlen_attn_fwd_window(const void* q_dev, const void* k_dev, const void* v_dev,
+                                 const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
+                                 int32_t causal, int32_t window, void* out_dev, float* lse_dev, void* ws_dev,
+                                 size_t ws_bytes, va_stream_t stream);
+
 /* Backward.  The analytic gradient of the forward definition, with P
  * recomputed from lse ("Packing与 FlashAttention Varlen", section 5 names the
  * training branch; the gradient itself is the plain derivative):
@@ -232,6 +256,14 @@ va_status varlen_attn_bwd(const void* q_dev, const void* k_dev, const void* v_de
                           const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
                           int32_t causal, void* dq_dev, void* dk_dev, void* dv_dev, void* ws_dev,
                           size_t ws_bytes, va_stream_t stream);
+
+/* varlen_attn_bwd for the causal local window of varlen_attn_fwd_window (the same window
+ * as the forward that produced out and lse); window = -1 is varlen_attn_bwd. */
+va_status varlen_attn_bwd_window(const void* q_dev, const void* k_dev, const void* v_dev,
+                                 const void* out_dev, const float* lse_dev, const void* dout_dev,
+                                 const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
+                                 int32_t causal, int32_t window, void* dq_dev, void* dk_dev, void* dv_dev,
+                                 void* ws_dev, size_t ws_bytes, va_stream_t stream);
 
 /* Forward without a workspace, for callers that cannot allocate device memory
  * where they run attention (a plugin inside a host runtime that owns all device

@@ -145,8 +145,9 @@ def workspace_size(T, B, Hq, Hkv, d, max_seqlen, for_bwd: bool) -> int:
 
 
 def plan(cu_seqlens: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, max_seqlen: int,
-         kind: int = 0, causal: bool = True):
-    """Tile map on the device: (records int32 [n, 4], n)."""
+         kind: int = 0, causal: bool = True, window: int | None = None):
+    """Tile map on the device: (records int32 [n, 4], n).  ``window``: causal local window
+    (query i sees keys i - window .. i), None for none."""
     B = cu_seqlens.numel() - 1
     s = _contig_shape(T, B, Hq, Hkv, d, max_seqlen)
     BM, BN = tile_sizes(kind, d)
@@ -156,9 +157,9 @@ def plan(cu_seqlens: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, max_seqlen
     tm = torch.empty((max(cap, 1), 4), dtype=torch.int32, device=cu_seqlens.device)
     n = torch.zeros(1, dtype=torch.int32, device=cu_seqlens.device)
     scratch = torch.empty(B + 4, dtype=torch.int32, device=cu_seqlens.device)
-    check(_lib.load().varlen_attn_plan(ctypes.byref(s), _ptr(cu_seqlens), kind, int(causal),
-                                       _ptr(tm), cap, _ptr(n), _ptr(scratch),
-                                       _stream(cu_seqlens.device)))
+    check(_lib.load().varlen_attn_plan_window(ctypes.byref(s), _ptr(cu_seqlens), kind, int(causal),
+                                              -1 if window is None else int(window), _ptr(tm), cap, _ptr(n),
+                                              _ptr(scratch), _stream(cu_seqlens.device)))
     k = int(n.item())
     return tm[:k], k
 
@@ -184,8 +185,11 @@ def _check_inputs(*ts):
 # ----------------------------------------------------------------- attention
 
 def varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,
-                    causal: bool = True, out=None, lse=None, workspace=None, check_status=False):
-    """Forward: returns (out [T,Hq,d] bf16, lse [Hq,T] fp32)."""
+                    causal: bool = True, out=None, lse=None, workspace=None, check_status=False,
+                    window: int | None = None):
+    """Forward: returns (out [T,Hq,d] bf16, lse [Hq,T] fp32).  ``window``: causal local window
+    (query i sees keys i - window .. i of its segment), None for none."""
+    win = -1 if window is None else int(window)
     _check_inputs(q, k, v)
     T, Hq, d = q.shape
     B = cu_seqlens.numel() - 1
@@ -198,14 +202,14 @@ def varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = 
     lib = _lib.load()
     need = lib.varlen_attn_workspace_size(ctypes.byref(s), 0)
     if need == 0:
-        check(lib.varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(s),
-                                  scale, int(causal), _ptr(out), _ptr(lse), _ptr(None), 0,
-                                  _stream(q.device)))
+        check(lib.varlen_attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(s),
+                                         scale, int(causal), win, _ptr(out), _ptr(lse), _ptr(None), 0,
+                                         _stream(q.device)))
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    check(lib.varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(s), scale,
-                              int(causal), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-                              _stream(q.device)))
+    check(lib.varlen_attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(s), scale,
+                                     int(causal), win, _ptr(out), _ptr(lse), _ptr(workspace),
+                                     workspace.numel(), _stream(q.device)))
     if check_status:
         _raise_status(workspace)
     return out, lse
@@ -213,8 +217,9 @@ def varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = 
 
 def varlen_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int,
                     scale: float | None = None, causal: bool = True, dq=None, dk=None, dv=None,
-                    workspace=None, check_status=False):
-    """Backward: returns (dq, dk, dv) bf16 with the shapes of q, k, v."""
+                    workspace=None, check_status=False, window: int | None = None):
+    """Backward: returns (dq, dk, dv) bf16 with the shapes of q, k, v (``window`` as in the
+    forward that produced out and lse)."""
     _check_inputs(q, k, v, out, dout)
     if out.stride() != dout.stride():
         raise ValueError("out and dout must share strides")
@@ -234,10 +239,10 @@ def varlen_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int,
     need = lib.varlen_attn_workspace_size(ctypes.byref(s), 1)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    check(lib.varlen_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                              _ptr(cu_seqlens), ctypes.byref(s), scale, int(causal), _ptr(dq),
-                              _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
-                              _stream(q.device)))
+    check(lib.varlen_attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                     _ptr(cu_seqlens), ctypes.byref(s), scale, int(causal),
+                                     -1 if window is None else int(window), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(workspace), workspace.numel(), _stream(q.device)))
     if check_status:
         _raise_status(workspace)
     return dq, dk, dv
@@ -245,10 +250,10 @@ def varlen_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int,
 
 class _VarlenAttn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, cu_seqlens, max_seqlen, scale, causal):
-        out, lse = varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen, scale, causal)
+    def forward(ctx, q, k, v, cu_seqlens, max_seqlen, scale, causal, window):
+        out, lse = varlen_attn_fwd(q, k, v, cu_seqlens, max_seqlen, scale, causal, window=window)
         ctx.save_for_backward(q, k, v, out, lse, cu_seqlens)
-        ctx.max_seqlen, ctx.scale, ctx.causal = max_seqlen, scale, causal
+        ctx.max_seqlen, ctx.scale, ctx.causal, ctx.window = max_seqlen, scale, causal, window
         return out
 
     @staticmethod
@@ -256,14 +261,14 @@ class _VarlenAttn(torch.autograd.Function):
         q, k, v, out, lse, cu = ctx.saved_tensors
         dout = dout.contiguous() if dout.stride() != out.stride() else dout
         dq, dk, dv = varlen_attn_bwd(q, k, v, out, lse, dout, cu, ctx.max_seqlen, ctx.scale,
-                                     ctx.causal)
-        return dq, dk, dv, None, None, None, None
+                                     ctx.causal, window=ctx.window)
+        return dq, dk, dv, None, None, None, None, None
 
 
 def varlen_attn(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,
-                causal: bool = True):
-    """Differentiable packed attention: out [T, Hq, d]."""
-    return _VarlenAttn.apply(q, k, v, cu_seqlens, max_seqlen, scale, causal)
+                causal: bool = True, window: int | None = None):
+    """Differentiable packed attention: out [T, Hq, d] (``window``: causal local window)."""
+    return _VarlenAttn.apply(q, k, v, cu_seqlens, max_seqlen, scale, causal, window)
 
 
 # ----------------------------------------------------------------- packed loss

@@ -28,6 +28,7 @@ EXPORTS = (
     "varlen_attn_fwd_noalloc", "varlen_cu_seqlens_from_positions",
     "varlen_loss_targets", "varlen_token_ce_workspace_size", "varlen_token_ce",
     "varlen_unpad_index", "varlen_gather_rows",
+    "varlen_attn_plan_window", "varlen_attn_fwd_window", "varlen_attn_bwd_window",
 )
 
 
@@ -72,6 +73,14 @@ def _declare(lib):
         "varlen_attn_bwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                       c_void_p, POINTER(VaShape), c_float, c_int32, c_void_p,
                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+        "varlen_attn_plan_window": (c_int32, [POINTER(VaShape), c_void_p, c_int32, c_int32, c_int32,
+                                              c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
+        "varlen_attn_fwd_window": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(VaShape),
+                                             c_float, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                             c_size_t, c_void_p]),
+        "varlen_attn_bwd_window": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, POINTER(VaShape), c_float, c_int32, c_int32,
+                                             c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
         "varlen_attn_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                               POINTER(VaShape), c_float, c_int32, c_void_p,
                                               c_void_p, c_void_p]),

@@ -92,8 +92,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // records cover the short segments and which kernel forms run.
 constexpr int64_t kTokenMeanLen = 256;
 
-bool token_tiles(const va_shape& s, int32_t causal) {
-  return causal && static_cast<int64_t>(s.T) < kTokenMeanLen * s.B;
+bool token_tiles(const va_shape& s, int32_t causal, int32_t window) {
+  return causal && window < 0 && static_cast<int64_t>(s.T) < kTokenMeanLen * s.B;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -263,8 +263,15 @@ size_t varlen_attn_workspace_size(const va_shape* s, int32_t for_bwd) {
 va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kind, int32_t causal,
                            int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
                            int32_t* scratch_dev, va_stream_t stream) {
+  return varlen_attn_plan_window(s, cu_dev, kind, causal, -1, map_dev, capacity, n_items_dev, scratch_dev, stream);
+}
+
+va_status varlen_attn_plan_window(const va_shape* s, const int32_t* cu_dev, int32_t kind, int32_t causal,
+                                  int32_t window, int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
+                                  int32_t* scratch_dev, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
+  if (window < -1 || (window >= 0 && !causal)) return fail(VA_ERR_INVALID_ARG, "plan: window needs causal and >= 0 (-1 = none)");
   if (kind < 0 || kind > 2 || !cu_dev || !map_dev || !n_items_dev || !scratch_dev || capacity < 0)
     return fail(VA_ERR_INVALID_ARG, "plan: bad kind or null pointer");
   if (!aligned16(map_dev)) return fail(VA_ERR_INVALID_ARG, "plan: tile map must be 16-byte aligned");
@@ -276,7 +283,8 @@ va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kin
   const PlanArgs pa{cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
                     reinterpret_cast<TileItem*>(map_dev), capacity, nullptr, n_items_dev,
                     scratch_dev + 4, scratch_dev,
-                    !token_tiles(*s, causal) ? 0 : kind == 0 ? fwd_tc_token_short() : bwd_tc_token_short()};
+                    !token_tiles(*s, causal, window) ? 0 : kind == 0 ? fwd_tc_token_short() : bwd_tc_token_short(),
+                    nullptr, nullptr, window};
   cudaError_t e = launch(K_PLAN, cs, [&] { return launch_plan(pa, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "plan");
 }
@@ -284,8 +292,15 @@ va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kin
 va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
                           const va_shape* s, float scale, int32_t causal, void* out, float* lse,
                           void* ws, size_t ws_bytes, va_stream_t stream) {
+  return varlen_attn_fwd_window(q, k, v, cu, s, scale, causal, -1, out, lse, ws, ws_bytes, stream);
+}
+
+va_status varlen_attn_fwd_window(const void* q, const void* k, const void* v, const int32_t* cu,
+                                 const va_shape* s, float scale, int32_t causal, int32_t window, void* out,
+                                 float* lse, void* ws, size_t ws_bytes, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
+  if (window < -1 || (window >= 0 && !causal)) return fail(VA_ERR_INVALID_ARG, "fwd: window needs causal and >= 0 (-1 = none)");
   if (!q || !k || !v || !cu || !out || !lse || !ws)
     return fail(VA_ERR_INVALID_ARG, "fwd: null pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws))
@@ -305,12 +320,12 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   }
   int BM, BN;
   tiles(0, &BM, &BN);
-  const bool tok = token_tiles(*s, causal);
+  const bool tok = token_tiles(*s, causal, window);
   const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map, static_cast<int>(L.cap),
                     &hdr->status, &hdr->n_items[0],
                     reinterpret_cast<int32_t*>(w + L.segoff), &hdr->counter[0],
                     tok ? fwd_tc_token_short() : 0, &hdr->n_items[kTokSlot],
-                    &hdr->counter[kTokSlot]};
+                    &hdr->counter[kTokSlot], window};
   cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
     return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cs);
   });
@@ -341,6 +356,7 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
   p.o_hs = s->o_head_stride;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
+  p.window = window;
   // segment records, then (as its programmatic dependent, filling its tail) token records
   e = launch(K_FWD, cs, [&] { return launch_fwd_tc(p, s->d, static_cast<int>(L.cap), cs); });
   if (e != cudaSuccess) return cuda_fail(e, "fwd kernel");
@@ -355,8 +371,17 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
                           const float* lse, const void* dout, const int32_t* cu, const va_shape* s,
                           float scale, int32_t causal, void* dq, void* dk, void* dv, void* ws,
                           size_t ws_bytes, va_stream_t stream) {
+  return varlen_attn_bwd_window(q, k, v, out, lse, dout, cu, s, scale, causal, -1, dq, dk, dv, ws, ws_bytes,
+                                stream);
+}
+
+va_status varlen_attn_bwd_window(const void* q, const void* k, const void* v, const void* out,
+                                 const float* lse, const void* dout, const int32_t* cu, const va_shape* s,
+                                 float scale, int32_t causal, int32_t window, void* dq, void* dk, void* dv,
+                                 void* ws, size_t ws_bytes, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
+  if (window < -1 || (window >= 0 && !causal)) return fail(VA_ERR_INVALID_ARG, "bwd: window needs causal and >= 0 (-1 = none)");
   if (!q || !k || !v || !out || !lse || !dout || !cu || !dq || !dk || !dv || !ws)
     return fail(VA_ERR_INVALID_ARG, "bwd: null pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
@@ -379,15 +404,15 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   int BM, BN, BM2, BN2;
   tiles(1, &BM, &BN);
   tiles(2, &BM2, &BN2);
-  const bool tok = token_tiles(*s, causal);
+  const bool tok = token_tiles(*s, causal, window);
   int32_t* segoff = reinterpret_cast<int32_t*>(w + L.segoff);
   const PlanArgs pa[2] = {
       {cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, kvmap, static_cast<int>(L.cap_kv), &hdr->status,
        &hdr->n_items[1], segoff, &hdr->counter[1], tok ? bwd_tc_token_short() : 0,
-       &hdr->n_items[kKvTokSlot]},
+       &hdr->n_items[kKvTokSlot], nullptr, window},
       {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, qmap, static_cast<int>(L.cap_q), &hdr->status,
        &hdr->n_items[2], segoff, &hdr->counter[2], tok ? bwd_tc_token_short() : 0,
-       &hdr->n_items[kQTokSlot]}};
+       &hdr->n_items[kQTokSlot], nullptr, window}};
   BwdParams p{};
   p.q = static_cast<const bf16*>(q);
   p.k = static_cast<const bf16*>(k);
@@ -425,6 +450,7 @@ va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const voi
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
+  p.window = window;
   // one launch validates, plans both maps and computes D = rowsum(dO * O)
   cudaError_t e = launch(K_BWD_PREP, cs, [&] { return launch_bwd_prep(p, pa, 2, s->T, s->max_seqlen, s->d, cs); });
   if (e == cudaSuccess)

@@ -22,6 +22,7 @@ struct FwdParams {
   int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs, o_rs, o_hs;
   float scale_log2;  // scale * log2(e)
   int causal;
+  int window = -1;   // causal local window: query i sees keys i-w..i; -1 = none
 };
 
 struct BwdParams {
@@ -49,6 +50,7 @@ struct BwdParams {
   float scale;
   float scale_log2;
   int causal;
+  int window = -1;   // causal local window: query i sees keys i-w..i; -1 = none
 };
 
 }  // namespace va

@@ -99,6 +99,7 @@ struct KvItem {
   int kvn;
 };
 
+template <bool WIN>
 __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
   const TileItem it = p.kv_items[idx];
   KvItem r;
@@ -107,7 +108,8 @@ __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
   r.n = it.blk;
   r.hk = it.head;
   const int Mq = (r.l + 63) / 64;
-  r.m_start = Mq - it.count;
+  // the q steps start at the diagonal; without a window they run to the segment's end
+  r.m_start = WIN ? it.blk * 2 : Mq - it.count;
   r.steps = it.count * p.g;
   r.kvn = 0;
   return r;
@@ -164,7 +166,9 @@ __device__ __forceinline__ KvItem kv_token_decode_w(const BwdParams& p, int idx,
 
 }  // namespace
 
-template <int D, bool TOK>
+// WIN: causal local window p.window: a kv block's q steps stop at the window of its last key
+// row, and steps that cross a key's window edge also mask the queries past key + w.
+template <int D, bool TOK, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   KvItem* queue = reinterpret_cast<KvItem*>(sm + C::QUEUE_OFF);
   uint8_t* row_tables = sm + C::ROWS_OFF;
-  auto dec = [&](int idx) { return kv_decode(p, idx); };
+  auto dec = [&](int idx) { return kv_decode<WIN>(p, idx); };
   // Launched as a programmatic dependent of the preparation kernel: its maps, D and status
   // are read only after the wait.  The dQ kernel, which reads the same products but none
   // of this kernel's, may then start on SMs as this kernel's CTAs finish.
@@ -254,7 +258,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) idx = atomicAdd(p.kv_counter, 1);
         idx = __shfl_sync(0xffffffffu, idx, 0);
         if (idx < n_seg) {
-          out = kv_decode(p, idx);
+          out = kv_decode<WIN>(p, idx);
           out.valid = 1;
         } else if (idx < n_items) {
           out = kv_token_decode_w(p, idx, row_tables + (k & 3) * C::KB);
@@ -491,7 +495,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_after_sync();
         const int q0 = (I.m_start + i / p.g) * 64;
         const int lim = kvrow - q0;  // query columns c < lim are masked (key after query)
-        const bool need_mask = p.causal && (I.n * 128 + 127 > q0);
+        // (window) query columns c >= hi are masked too: past the key's window
+        const int hi = WIN ? kvrow + p.window + 1 - q0 : 0;
+        const bool need_mask =
+            p.causal && (I.n * 128 + 127 > q0 || (WIN && q0 + 63 > I.n * 128 + p.window));
         const float* L = ldring + ls * 128;
         const float* Dd = L + 64;
         // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
@@ -514,8 +521,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float x0 = fmaf(__uint_as_float(sv[j]), sl2, la), x1 = fmaf(__uint_as_float(sv[j + 1]), sl2, lb);
             float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
             if (need_mask) {
-              if (j < lim) p0 = 0.f;
-              if (j + 1 < lim) p1 = 0.f;
+              if (j < lim || (WIN && j >= hi)) p0 = 0.f;
+              if (j + 1 < lim || (WIN && j + 1 >= hi)) p1 = 0.f;
             }
             const float t0 = __uint_as_float(dpv[j]) + da, t1 = __uint_as_float(dpv[j + 1]) + db;
             sv[j >> 1] = pack_bf16(p0, p1);
@@ -694,6 +701,7 @@ struct QItem {
   int kb;
 };
 
+template <bool WIN>
 __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
   const TileItem it = p.q_items[idx];
   QItem r;
@@ -703,7 +711,8 @@ __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
   r.h = it.head;
   r.hk = it.head / p.g;
   r.nb = it.count;
-  r.kb = r.s0;
+  // key steps from the segment start, or (window) from the window of the item's first row
+  r.kb = WIN ? r.s0 + max(0, it.blk * 128 - p.window) / 64 * 64 : r.s0;
   return r;
 }
 
@@ -748,7 +757,9 @@ __device__ __forceinline__ QItem q_token_decode_w(const BwdParams& p, int idx, u
 
 }  // namespace
 
-template <int D, bool TOK>
+// WIN: causal local window p.window: an item's key steps start at the window of its first
+// row, and steps that cross a query's window edge also mask the keys before query - w.
+template <int D, bool TOK, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -768,7 +779,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   QItem* queue = reinterpret_cast<QItem*>(sm + C::QUEUE_OFF);
   uint8_t* row_tables = sm + C::ROWS_OFF;
-  auto dec = [&](int idx) { return q_decode(p, idx); };
+  auto dec = [&](int idx) { return q_decode<WIN>(p, idx); };
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.q_slot];
   const int n_seg = n_items - p.hdr->n_items[p.q_tok_slot];  // segment records, then token ones
@@ -832,7 +843,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) idx = atomicAdd(p.q_counter, 1);
         idx = __shfl_sync(0xffffffffu, idx, 0);
         if (idx < n_seg) {
-          out = q_decode(p, idx);
+          out = q_decode<WIN>(p, idx);
           out.valid = 1;
         } else if (idx < n_items) {
           out = q_token_decode_w(p, idx, row_tables + (k & 3) * C::QB);
@@ -1065,9 +1076,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++sf;
         fence_after_sync();
         const float lse2 = qin ? lse_raw * kLog2e : INFINITY;
-        // key columns c > lim are masked: after the query (causal) or past the segment end
-        const int lim = p.causal ? qrow - n * 64 : I.l - 1 - n * 64;
-        const bool need_mask = p.causal ? (n * 64 + 63 > I.m * 128) : (n * 64 + 64 > I.l);
+        // key columns c > lim are masked: after the query (causal) or past the segment end;
+        // (window) key columns c < lo too: before the query's window
+        const int kn = WIN ? I.kb - I.s0 + n * 64 : n * 64;  // the step's first key, segment-local
+        const int lim = p.causal ? qrow - kn : I.l - 1 - n * 64;
+        const int lo = WIN ? qrow - p.window - kn : 0;
+        const bool need_mask = p.causal ? (kn + 63 > I.m * 128 || (WIN && kn < I.m * 128 + 127 - p.window))
+                                        : (n * 64 + 64 > I.l);
         // one TMEM round trip: the step's 64 scores and 64 dP values of this q row
         uint32_t sv[64], dpv[64];
         tmem_ld32(s_addr, sv);
@@ -1081,8 +1096,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           if (need_mask) {
-            if (c > lim) p0 = 0.f;
-            if (c + 1 > lim) p1 = 0.f;
+            if (c > lim || (WIN && c < lo)) p0 = 0.f;
+            if (c + 1 > lim || (WIN && c + 1 < lo)) p1 = 0.f;
           }
           float t0, t1;
           fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
@@ -1188,7 +1203,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------- host side
 
 
-template <int D, bool TOK>
+template <int D, bool TOK, bool WIN>
 static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   using C = KvCfg<D>;
   CUtensorMap tq, tk, tv, tdo;
@@ -1197,11 +1212,11 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
       !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
       !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D, TOK, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D, TOK>);
+  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D, TOK, WIN>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -1209,10 +1224,10 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dkdv_tc_kernel<D, TOK>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dkdv_tc_kernel<D, TOK, WIN>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
-template <int D, bool TOK>
+template <int D, bool TOK, bool WIN>
 static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   using C = QCfg<D>;
   CUtensorMap tq, tk, tv, tdo;
@@ -1221,11 +1236,11 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
       !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 64) ||
       !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 64))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D, TOK, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D, TOK>);
+  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D, TOK, WIN>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -1233,20 +1248,24 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dq_tc_kernel<D, TOK>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dq_tc_kernel<D, TOK, WIN>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
 // tok: the maps hold token records.  The two forms are compiled separately so that the
 // segment-only kernels keep their own code: the token branch in the softmax item loop
 // measured 15% slower on segment records.
 cudaError_t launch_bwd_dkdv_tc(const BwdParams& p, int d, int cap, bool tok, cudaStream_t st) {
-  if (tok) return d == 64 ? launch_dkdv_d<64, true>(p, cap, st) : launch_dkdv_d<128, true>(p, cap, st);
-  return d == 64 ? launch_dkdv_d<64, false>(p, cap, st) : launch_dkdv_d<128, false>(p, cap, st);
+  if (p.window >= 0)  // window calls plan no token records
+    return d == 64 ? launch_dkdv_d<64, false, true>(p, cap, st) : launch_dkdv_d<128, false, true>(p, cap, st);
+  if (tok) return d == 64 ? launch_dkdv_d<64, true, false>(p, cap, st) : launch_dkdv_d<128, true, false>(p, cap, st);
+  return d == 64 ? launch_dkdv_d<64, false, false>(p, cap, st) : launch_dkdv_d<128, false, false>(p, cap, st);
 }
 
 cudaError_t launch_bwd_dq_tc(const BwdParams& p, int d, int cap, bool tok, cudaStream_t st) {
-  if (tok) return d == 64 ? launch_dq_d<64, true>(p, cap, st) : launch_dq_d<128, true>(p, cap, st);
-  return d == 64 ? launch_dq_d<64, false>(p, cap, st) : launch_dq_d<128, false>(p, cap, st);
+  if (p.window >= 0)
+    return d == 64 ? launch_dq_d<64, false, true>(p, cap, st) : launch_dq_d<128, false, true>(p, cap, st);
+  if (tok) return d == 64 ? launch_dq_d<64, true, false>(p, cap, st) : launch_dq_d<128, true, false>(p, cap, st);
+  return d == 64 ? launch_dq_d<64, false, false>(p, cap, st) : launch_dq_d<128, false, false>(p, cap, st);
 }
 
 int bwd_tc_token_short() { return kBwdTokenShort; }

@@ -52,6 +52,8 @@ struct PlanArgs {
                       // (records {-1 - f, t0, head, rows}); 0 = off
   int32_t* n_tok;     // may be null: out, the number of token records (the map's last ones)
   int32_t* tok_counter;  // may be null: the token kernel's work counter; zeroed here
+  int window = -1;       // causal local window w >= 0 (query i sees keys i-w..i), -1 = none;
+                         // window maps have no token records
 };
 
 __device__ __forceinline__ void set_status(WsHeader* h, int code) {

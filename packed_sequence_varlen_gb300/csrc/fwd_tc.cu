@@ -69,8 +69,10 @@ struct Item {
   int s0, l, h, hk, m, nb, nb0;
   int t1;
   int valid;
+  int kb;  // local window: the item's first key tile (its key tiles are kb .. kb + nb - 1)
 };
 
+template <bool WIN>
 __device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
   const TileItem it = p.items[idx];
   Item r;
@@ -82,7 +84,25 @@ __device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
   r.nb = it.count;
   r.t1 = r.m * kTcBM + 128 < r.l ? 1 : 0;
   r.nb0 = (p.causal && r.t1) ? r.nb - 1 : r.nb;
+  if (WIN) r.kb = max(0, r.m * kTcBM - p.window) / kTcBN;
   return r;
+}
+
+// Masks columns j < lo and j > lim, and returns the row max x sl2 (local window: the left
+// edge of the row's window and its diagonal).
+__device__ __forceinline__ float row_max2(uint32_t* v, int lo, int lim, float sl2) {
+#pragma unroll
+  for (int j = 0; j < 128; ++j)
+    if (j < lo || j > lim) v[j] = __float_as_uint(-INFINITY);
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    m0 = fmax3(m0, __uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]));
+    m1 = fmax3(m1, __uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+    m2 = fmax3(m2, __uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+    m3 = fmax3(m3, __uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
 }
 
 // Bounded wait used only while shutting down after an abort: ignores the abort flag.
@@ -136,7 +156,11 @@ __device__ __forceinline__ float row_exp(uint32_t* v, float sl2, float mu) {
 
 }  // namespace
 
-template <int D>
+// WIN: causal local window p.window (query i sees keys i-w..i): an item's key tiles start at
+// the window of its first row, and tiles that cross a row's window edge are masked on both
+// sides; a row may see nothing in its first tiles (its running max stays -inf and the first
+// visible tile takes over with a zero-weight rescale).
+template <int D, bool WIN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -150,7 +174,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   Item* queue = reinterpret_cast<Item*>(sm + C::QUEUE_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
-  auto dec = [&](int idx) { return decode(p, idx); };
+  auto dec = [&](int idx) { return decode<WIN>(p, idx); };
 
   griddep_begin();  // the tile map and status come from the planning launch just before
   if (p.hdr->status != VA_OK) return;
@@ -230,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_expect_tx_w(bar(C::B_KVF + s), C::TILE);
             for (int pn = 0; pn < D / 64; ++pn)
               tma_load_3d_w(base + C::KV_OFF + s * C::TILE + pn * C::PANEL, kv ? &tv : &tk,
-                          bar(C::B_KVF + s), pn * 64, I.hk, I.s0 + n * kTcBN);
+                          bar(C::B_KVF + s), pn * 64, I.hk, I.s0 + (WIN ? I.kb + n : n) * kTcBN);
             ++kv_it;
           }
         }
@@ -392,14 +416,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // The causal mask touches only the last key tile of each q tile (its diagonal
         // tile); non-causal masks only key columns past the segment end.
         const bool need_mask = p.causal ? (n == nbt - 1) : (n * kTcBN + kTcBN > I.l);
-        const int lim = p.causal ? qrow - n * kTcBN : I.l - 1 - n * kTcBN;  // mask j > lim
+        const int lim = p.causal ? qrow - (WIN ? I.kb + n : n) * kTcBN : I.l - 1 - n * kTcBN;  // mask j > lim
         // One TMEM round trip per tile: the row into registers, its max, then
         // p = exp2(s * sl2 - m_ref) packed in place and stored over the first half of S_t.
         // The reference max m_ref is raised only when the row max grew by more than 2^8
         // (rare); O_t, which holds PV_{n-1}, is then rescaled in TMEM first.
         uint32_t v[128];
         row_load(s_addr, v);
-        const float mt = need_mask ? row_max<true>(v, lim, sl2) : row_max<false>(v, lim, sl2);
+        float mt;
+        if constexpr (WIN) {  // keys before qrow - w are outside the window
+          const int ka = (I.kb + n) * kTcBN;
+          const bool need_w = ka < I.m * kTcBM + t * 128 + 127 - p.window;
+          mt = (need_mask || need_w) ? row_max2(v, qrow - p.window - ka, lim, sl2) : row_max<false>(v, lim, sl2);
+        } else {
+          mt = need_mask ? row_max<true>(v, lim, sl2) : row_max<false>(v, lim, sl2);
+        }
         if (n == 0) {
           m_ref = mt;
         } else {
@@ -476,7 +507,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int D>
+template <int D, bool WIN>
 static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
   using C = TcCfg<D>;
   CUtensorMap tq, tk, tv;
@@ -484,11 +515,11 @@ static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
       !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
       !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D>);
+  e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, WIN>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -496,11 +527,12 @@ static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(fwd_tc_kernel<D>, dim3(grid), dim3(kTcThreads), C::SMEM, st, tq, tk, tv, p);
+  return launch_pdl(fwd_tc_kernel<D, WIN>, dim3(grid), dim3(kTcThreads), C::SMEM, st, tq, tk, tv, p);
 }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, int cap, cudaStream_t st) {
-  return d == 64 ? launch_d<64>(p, cap, st) : launch_d<128>(p, cap, st);
+  if (p.window >= 0) return d == 64 ? launch_d<64, true>(p, cap, st) : launch_d<128, true>(p, cap, st);
+  return d == 64 ? launch_d<64, false>(p, cap, st) : launch_d<128, false>(p, cap, st);
 }
 
 void fwd_tc_tiles(int* BM, int* BN) {

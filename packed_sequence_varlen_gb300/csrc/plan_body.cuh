@@ -55,10 +55,25 @@ __device__ __forceinline__ bool token_mode(const PlanArgs& a) { return a.causal 
 // What a map build is, fixed at compile time: the planner's time is mostly fetching its
 // own instructions (it runs once per call, on one SM), so each kind of map gets its own
 // compact code path.  KV: kv-block map (kind 1), else q-block map (kinds 0 and 2).
-template <bool KV, bool CAUSAL, bool TOKENS>
+// WIN: causal local window a.window (query i sees keys i-w..i): a q block m's key blocks
+// start at floor(max(0, m*BM - w) / BN); a kv block n's q blocks stop after
+// floor((n*BN + BN - 1 + w) / BM) ("Packing与 FlashAttention Varlen", section 5: the local
+// window narrows n_block_min/max).
+template <bool KV, bool CAUSAL, bool TOKENS, bool WIN = false>
 struct MapKind {
-  static constexpr bool kv = KV, causal = CAUSAL, tokens = TOKENS;
+  static constexpr bool kv = KV, causal = CAUSAL, tokens = TOKENS, win = WIN;
 };
+
+// Windowed record count of q block m (q-block maps) or kv block n (kv-block maps).
+template <class M>
+__device__ __forceinline__ int win_count(const PlanArgs& a, int l, int blk) {
+  if (!M::kv) {
+    const int nmax = ceil_p2(min(l, (blk + 1) * a.BM), a.BN);
+    return nmax - div_p2(max(0, blk * a.BM - a.window), a.BN);
+  }
+  const int Mq = ceil_p2(l, a.BM);
+  return min(Mq, div_p2(blk * a.BN + a.BN - 1 + a.window, a.BM) + 1) - div_p2(blk * a.BN, a.BM);
+}
 
 // Blocks of a segment of length l and its total tile count (none for token-tiled segments).
 template <class M>
@@ -66,6 +81,10 @@ __device__ __forceinline__ void seg_cost(const PlanArgs& a, int l, int& nblk, in
   if (M::tokens && l <= a.short_len) {
     nblk = 0;
     cost = 0;
+  } else if (M::win) {  // no closed form worth keeping: sum the blocks (one thread per segment)
+    nblk = M::kv ? ceil_p2(l, a.BN) : ceil_p2(l, a.BM);
+    cost = 0;
+    for (int b = 0; b < nblk; ++b) cost += win_count<M>(a, l, b);
   } else if (!M::kv) {
     const int M_ = ceil_p2(l, a.BM), Lk = ceil_p2(l, a.BN);
     nblk = M_;
@@ -80,7 +99,10 @@ __device__ __forceinline__ void seg_cost(const PlanArgs& a, int l, int& nblk, in
 // The j-th record of one (segment, head): most tiles first.
 template <class M>
 __device__ __forceinline__ void seg_record(const PlanArgs& a, int l, int nblk, int j, int& blk, int& count) {
-  if (!M::kv) {
+  if (M::win) {  // q blocks last-first, kv blocks first-first: the no-window orders
+    blk = M::kv ? j : nblk - 1 - j;
+    count = win_count<M>(a, l, blk);
+  } else if (!M::kv) {
     const int Lk = ceil_p2(l, a.BN);
     blk = M::causal ? nblk - 1 - j : j;
     count = M::causal ? min(Lk, div_p2(a.BM, a.BN) * (blk + 1)) : Lk;
@@ -430,6 +452,11 @@ __device__ __forceinline__ void plan_body_m(const PlanArgs& a, PlanSmem& sh, con
 }
 
 __device__ __forceinline__ void plan_body(const PlanArgs& a, PlanSmem& sh, const int* cu, int* seg_off) {
+  if (a.causal && a.window >= 0) {
+    if (a.kind == 1) plan_body_m<MapKind<true, true, false, true>>(a, sh, cu, seg_off);
+    else plan_body_m<MapKind<false, true, false, true>>(a, sh, cu, seg_off);
+    return;
+  }
   if (a.kind == 1) {
     if (!a.causal) plan_body_m<MapKind<true, false, false>>(a, sh, cu, seg_off);
     else if (token_mode(a)) plan_body_m<MapKind<true, true, true>>(a, sh, cu, seg_off);
