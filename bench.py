@@ -96,8 +96,27 @@ def batch_packs(rank: int, planners):
     raw = si.raw_lengths(WORKLOAD).tolist()
     planner = host_planner(w, planners)
     packs = [raw] if planner is None else [[raw[i] for i in p] for p in planner(raw, w.capacity)]
-    idx = [(rank * PACKS_PER_STEP + i) % len(packs) for i in range(PACKS_PER_STEP)]
+    idx = rank_pack_indices(rank, PACKS_PER_STEP, len(packs))
     return [packs[i] for i in idx], idx, w
+
+
+def rank_pack_indices(rank: int, packs_per_step: int, n_packs: int):
+    """Weak scaling without a data-path exchange: rank r takes the workload's packs
+    r*P .. r*P + P - 1 (wrapping around the workload's packs)."""
+    return [(rank * packs_per_step + i) % n_packs for i in range(packs_per_step)]
+
+
+def aggregate(elapsed_ms: float, step_flops: float, steps: int, dist=None, device="cpu"):
+    """Whole-job figures: the elapsed time is the maximum over ranks, the work the sum over
+    ranks (ranks process different packs).  Returns (max_ms, total_flops)."""
+    import torch
+    if dist is None:
+        return elapsed_ms, step_flops * steps
+    mx = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    sm = torch.tensor([step_flops * steps], dtype=torch.float64, device=device)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx.item()), float(sm.item())
 
 
 def host_planner(w, planners):
@@ -286,12 +305,7 @@ def run_ours(args, rank, world, local_rank):
         t, c = per_kernel.get(name, (0.0, 0))
         per_kernel[name] = (t + ms[i], c + 1)
 
-    max_ms = elapsed_ms
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
-    total_flops = step_flops * args.steps * world
+    max_ms, total_flops = aggregate(elapsed_ms, step_flops, args.steps, dist, dev)
     value = total_flops / (max_ms * 1e-3) / 1e12
 
     # roofline of the dominant kernel: algorithmic flops per launch / launch time
@@ -425,12 +439,8 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
         step()
     barrier()
     dt = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([dt], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
-    world = dist.get_world_size() if dist is not None else 1
-    return {"value": round(step_flops * args.steps * world / dt / 1e12, 3), "unit": UNIT,
+    max_ms, total_flops = aggregate(dt * 1e3, step_flops, args.steps, dist, dev)
+    return {"value": round(total_flops / (max_ms * 1e-3) / 1e12, 3), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "H2D, compute and D2H on three streams, two device buffer sets"}
 
