@@ -28,6 +28,13 @@ narrows the key blocks a query block may see): with ``window = w`` (causal only)
 query i sees the keys i - w <= j <= i of its segment, i.e. itself and the w keys
 before it (FlashAttention's left window size; its right size is 0 under causality).
 
+Cross-attention (``cu_k`` given, blog section 3: cu_q and cu_k cut Q and K/V separately,
+the b-th Q slice and K/V slice belong to the same sample; section 5: the causal bound is
+aligned bottom-right, (m+1)*BM + seqlen_k - seqlen_q): query i of a segment sees the keys
+j <= i + (lk - lq) of the same segment.  Reading taken here: causal cross-attention needs
+lq <= lk in every segment (every query then sees at least one key); other lengths are
+rejected rather than given empty softmax rows.
+
 The GQA head mapping h -> h // (Hq/Hkv) is not on the pages; it is the plainest
 reading (consecutive q heads share a kv head).  Rows of long segments are
 processed in blocks only to bound memory; each block computes full rows.
@@ -60,11 +67,12 @@ def _expand(x: np.ndarray, g: int) -> np.ndarray:
     return np.repeat(x, g, axis=1).transpose(1, 0, 2)
 
 
-def _visible(i, j, causal: bool, window):
-    """Permission of query rows i (column vector) on key columns j (row vector)."""
+def _visible(i, j, causal: bool, window, off: int = 0):
+    """Permission of query rows i (column vector) on key columns j (row vector); off is the
+    bottom-right causal offset lk - lq (0 for self-attention)."""
     if not causal:
         return np.ones(np.broadcast(i, j).shape, dtype=bool)
-    vis = j <= i
+    vis = j <= i + off
     if window is not None:
         vis = vis & (j >= i - window)
     return vis
@@ -76,12 +84,19 @@ def _check_window(causal: bool, window):
 
 
 def segment_forward(q, k, v, scale: float, causal: bool = True, window=None):
-    """One segment, all heads.  q [l,Hq,d], k/v [l,Hkv,d] (float64).
+    """One segment, all heads.  q [lq,Hq,d], k/v [lk,Hkv,d] (float64); lq == lk unless
+    cross-attention (bottom-right causal alignment, lq <= lk when causal).
 
-    Returns (o [l,Hq,d], lse [Hq,l]).
+    Returns (o [lq,Hq,d], lse [Hq,lq]).
     """
     _check_window(causal, window)
     l, Hq, d = q.shape
+    lk = k.shape[0]
+    off = lk - l
+    if causal and off < 0:
+        raise ValueError("causal cross-attention needs lq <= lk")
+    if window is not None and off != 0:
+        raise ValueError("a local window is for self-attention")
     g = Hq // k.shape[1]
     Q = q.transpose(1, 0, 2)
     K = _expand(k, g)
@@ -91,12 +106,12 @@ def segment_forward(q, k, v, scale: float, causal: bool = True, window=None):
     rb = _row_block(l, Hq)
     for r0 in range(0, l, rb):
         r1 = min(l, r0 + rb)
-        kend = r1 if causal else l
+        kend = r1 + off if causal else lk
         s = scale * (Q[:, r0:r1] @ K[:, :kend].transpose(0, 2, 1))
         if causal:
             i = np.arange(r0, r1)[:, None]
             j = np.arange(kend)[None, :]
-            s = np.where(_visible(i, j, causal, window), s, -np.inf)
+            s = np.where(_visible(i, j, causal, window, off), s, -np.inf)
         mx = s.max(axis=2, keepdims=True)
         e = np.exp(s - mx)
         z = e.sum(axis=2, keepdims=True)
@@ -115,31 +130,35 @@ def segment_backward(q, k, v, o, lse, do, scale: float, causal: bool = True, win
     l, Hq, d = q.shape
     Hkv = k.shape[1]
     g = Hq // Hkv
+    lk = k.shape[0]
+    off = lk - l
+    if causal and off < 0:
+        raise ValueError("causal cross-attention needs lq <= lk")
     Q = q.transpose(1, 0, 2)
     K = _expand(k, g)
     V = _expand(v, g)
     dO = do.transpose(1, 0, 2)
     D = (do * o).sum(axis=2).T                    # [Hq, l]
     dQ = np.zeros((Hq, l, d))
-    dKx = np.zeros((Hq, l, d))
-    dVx = np.zeros((Hq, l, v.shape[2]))
+    dKx = np.zeros((Hq, lk, d))
+    dVx = np.zeros((Hq, lk, v.shape[2]))
     rb = _row_block(l, Hq)
     for r0 in range(0, l, rb):
         r1 = min(l, r0 + rb)
-        kend = r1 if causal else l
+        kend = r1 + off if causal else lk
         s = scale * (Q[:, r0:r1] @ K[:, :kend].transpose(0, 2, 1))
         p = np.exp(s - lse[:, r0:r1, None])
         if causal:
             i = np.arange(r0, r1)[:, None]
             j = np.arange(kend)[None, :]
-            p = np.where(_visible(i, j, causal, window), p, 0.0)
+            p = np.where(_visible(i, j, causal, window, off), p, 0.0)
         dVx[:, :kend] += p.transpose(0, 2, 1) @ dO[:, r0:r1]
         dp = dO[:, r0:r1] @ V[:, :kend].transpose(0, 2, 1)
         ds = p * (dp - D[:, r0:r1, None])
         dQ[:, r0:r1] = scale * (ds @ K[:, :kend])
         dKx[:, :kend] += scale * (ds.transpose(0, 2, 1) @ Q[:, r0:r1])
-    dK = dKx.reshape(Hkv, g, l, d).sum(axis=1)
-    dV = dVx.reshape(Hkv, g, l, v.shape[2]).sum(axis=1)
+    dK = dKx.reshape(Hkv, g, lk, d).sum(axis=1)
+    dV = dVx.reshape(Hkv, g, lk, v.shape[2]).sum(axis=1)
     return dQ.transpose(1, 0, 2), dK.transpose(1, 0, 2), dV.transpose(1, 0, 2)
 
 
@@ -151,27 +170,33 @@ def _head_slices(Hq: int, Hkv: int, kv_heads):
     return kv_heads, g
 
 
-def varlen_forward(q, k, v, cu_seqlens, scale=None, causal=True, kv_heads=None, window=None):
+def varlen_forward(q, k, v, cu_seqlens, scale=None, causal=True, kv_heads=None, window=None,
+                   cu_seqlens_k=None):
     """Packed forward: every segment of ``cu_seqlens`` is its own attention.
 
     q [T,Hq,d], k/v [T,Hkv,d] float64.  Returns (o [T,Hq,d], lse [Hq,T]).
     With ``kv_heads`` set, only those kv heads and their q-head groups are
-    computed; every other entry is NaN.
+    computed; every other entry is NaN.  With ``cu_seqlens_k`` (cross-attention) k/v are
+    [Tk,Hkv,d] cut by their own boundaries.
     """
     T, Hq, d = q.shape
     Hkv = k.shape[1]
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
     cu = check_cu_seqlens(cu_seqlens, T)
+    cuk = cu if cu_seqlens_k is None else check_cu_seqlens(cu_seqlens_k, k.shape[0])
+    if cuk.size != cu.size:
+        raise ValueError("cu_seqlens and cu_seqlens_k need the same number of segments")
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     kvh, g = _head_slices(Hq, Hkv, kv_heads)
     o = np.full((T, Hq, v.shape[2]), np.nan)
     lse = np.full((Hq, T), np.nan)
     for b in range(cu.size - 1):
         s, e = cu[b], cu[b + 1]
+        sk, ek = cuk[b], cuk[b + 1]
         for hk in kvh:
             hq = slice(hk * g, (hk + 1) * g)
-            ob, lb = segment_forward(q[s:e, hq], k[s:e, hk:hk + 1], v[s:e, hk:hk + 1],
+            ob, lb = segment_forward(q[s:e, hq], k[sk:ek, hk:hk + 1], v[sk:ek, hk:hk + 1],
                                      scale, causal, window)
             o[s:e, hq] = ob
             lse[hq, s:e] = lb
@@ -179,11 +204,12 @@ def varlen_forward(q, k, v, cu_seqlens, scale=None, causal=True, kv_heads=None, 
 
 
 def varlen_backward(q, k, v, o, lse, do, cu_seqlens, scale=None, causal=True,
-                    kv_heads=None, window=None):
+                    kv_heads=None, window=None, cu_seqlens_k=None):
     """Packed backward (dq, dk, dv); entries of heads outside ``kv_heads`` are NaN."""
     T, Hq, d = q.shape
     Hkv = k.shape[1]
     cu = check_cu_seqlens(cu_seqlens, T)
+    cuk = cu if cu_seqlens_k is None else check_cu_seqlens(cu_seqlens_k, k.shape[0])
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     kvh, g = _head_slices(Hq, Hkv, kv_heads)
     dq = np.full(q.shape, np.nan)
@@ -191,14 +217,15 @@ def varlen_backward(q, k, v, o, lse, do, cu_seqlens, scale=None, causal=True,
     dv = np.full(v.shape, np.nan)
     for b in range(cu.size - 1):
         s, e = cu[b], cu[b + 1]
+        sk, ek = cuk[b], cuk[b + 1]
         for hk in kvh:
             hq = slice(hk * g, (hk + 1) * g)
-            a, bk, c = segment_backward(q[s:e, hq], k[s:e, hk:hk + 1], v[s:e, hk:hk + 1],
+            a, bk, c = segment_backward(q[s:e, hq], k[sk:ek, hk:hk + 1], v[sk:ek, hk:hk + 1],
                                         o[s:e, hq], lse[hq, s:e], do[s:e, hq],
                                         scale, causal, window)
             dq[s:e, hq] = a
-            dk[s:e, hk:hk + 1] = bk
-            dv[s:e, hk:hk + 1] = c
+            dk[sk:ek, hk:hk + 1] = bk
+            dv[sk:ek, hk:hk + 1] = c
     return dq, dk, dv
 
 

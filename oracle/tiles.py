@@ -40,6 +40,12 @@ every segment record, ordered by (t0, h).  Segments covered by token tiles have
 no segment records.  The dK/dV map cuts the same runs into BN-row tiles of key
 rows: key j of a tile is seen by the queries [j, end of its segment).
 
+Cross-attention (``cu_k``, section 5: the causal bound is aligned bottom-right,
+ceil(((m+1)*BM + lk - lq) / BN)): q block m of a segment with lq queries and lk keys has
+ceil(min(lk, (m+1)*BM + lk - lq) / BN) key blocks (ceil(lk / BN) non-causal); kv block n has
+its q blocks from floor(max(0, n*BN - (lk - lq)) / BM) (0 non-causal) to ceil(lq / BM) - 1.
+Same order keys; no token records.
+
 Local window w (causal; section 5: "causal or local window further narrows
 n_block_min/max"): q block m's key blocks run from n_min = floor(max(0, m*BM - w) / BN)
 to its diagonal, count = n_max - n_min; kv block n's q blocks run from its diagonal
@@ -71,20 +77,24 @@ def window_q_end(n: int, l: int, BM: int, BN: int, window) -> int:
     return Mq if window is None else min(Mq, (n * BN + BN - 1 + window) // BM + 1)
 
 
-def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, short: int = 0, window=None):
+def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, short: int = 0, window=None,
+                 cu_k=None):
     """Items as an int32 array [N, 4], in the order above: segment records
     (b, m, h, n_blocks), then (causal, short > 0) token records (-1 - f, t0, h, rows)."""
     cu = [int(x) for x in cu_seqlens]
+    cuk = cu if cu_k is None else [int(x) for x in cu_k]
     B = len(cu) - 1
-    tok = [causal and short > 0 and window is None and cu[b + 1] - cu[b] <= short for b in range(B)]
+    tok = [causal and short > 0 and window is None and cu_k is None and cu[b + 1] - cu[b] <= short
+           for b in range(B)]
     items = []
     for b in range(B):
         if tok[b]:
             continue
         l = cu[b + 1] - cu[b]
+        lk = cuk[b + 1] - cuk[b]
         blocks = []
         for m in range(_ceil(l, BM)):
-            nb = _ceil(min(l, (m + 1) * BM), BN) if causal else _ceil(l, BN)
+            nb = _ceil(min(lk, (m + 1) * BM + lk - l), BN) if causal else _ceil(lk, BN)
             blocks.append((m, nb - window_key_start(m, BM, BN, window)))
         cls = _cost_class(sum(nb for _, nb in blocks))
         for h in range(Hq):
@@ -95,22 +105,25 @@ def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, sho
     return np.asarray(out, dtype=np.int32).reshape(-1, 4)
 
 
-def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True, short: int = 0, window=None):
+def bwd_tile_map(cu_seqlens, Hkv: int, BM: int, BN: int, causal: bool = True, short: int = 0, window=None,
+                 cu_k=None):
     """Items as an int32 array [N, 4], in the order above: segment records
     (b, n, h_kv, n_q), then (causal, short > 0) token records (-1 - f, t0, h_kv, rows)
     whose BN-row tiles hold the key rows [t0, t0 + rows) of a run of short segments."""
     cu = [int(x) for x in cu_seqlens]
+    cuk = cu if cu_k is None else [int(x) for x in cu_k]
     B = len(cu) - 1
-    tok = [causal and short > 0 and window is None and cu[b + 1] - cu[b] <= short for b in range(B)]
+    tok = [causal and short > 0 and window is None and cu_k is None and cu[b + 1] - cu[b] <= short
+           for b in range(B)]
     items = []
     for b in range(B):
         if tok[b]:
             continue
         l = cu[b + 1] - cu[b]
-        Mq = _ceil(l, BM)
+        lk = cuk[b + 1] - cuk[b]
         blocks = []
-        for n in range(_ceil(l, BN)):
-            m_start = (n * BN) // BM if causal else 0
+        for n in range(_ceil(lk, BN)):
+            m_start = max(0, n * BN - (lk - l)) // BM if causal else 0
             blocks.append((n, window_q_end(n, l, BM, BN, window) - m_start))
         cls = _cost_class(sum(nq for _, nq in blocks))
         for h in range(Hkv):
@@ -139,24 +152,28 @@ def _token_records(cu, tok, H, rows_per_tile):
     return out
 
 
-def bwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None):
-    """(query, key) token pairs a backward kv item's tiles cover, in global indices."""
+def bwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None, cu_k=None):
+    """(query, key) token pairs a backward kv item's tiles cover, in global indices (keys in
+    the K/V stream's indices under cross-attention)."""
     b, n, _h, nq = (int(x) for x in item)
     cu = [int(x) for x in cu_seqlens]
+    cuk = cu if cu_k is None else [int(x) for x in cu_k]
     if b < 0:                                     # token record: key rows [t0, t0 + rows)
         t0, rows = n, nq
         last = t0 + rows - 1
         end = min(cu[x + 1] for x in range(len(cu) - 1) if cu[x + 1] > last)
         return [(i, j) for j in range(t0, t0 + rows) for i in range(t0, end)]
     s, l = cu[b], cu[b + 1] - cu[b]
+    sk, lk = cuk[b], cuk[b + 1] - cuk[b]
     m0 = window_q_end(n, l, BM, BN, window) - nq
-    cols = range(s + n * BN, s + min(l, (n + 1) * BN))
+    cols = range(sk + n * BN, sk + min(lk, (n + 1) * BN))
     rows = range(s + m0 * BM, s + min(l, (m0 + nq) * BM))
     return [(i, j) for i in rows for j in cols]
 
 
-def fwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None):
-    """(query, key) token pairs a forward item's tiles cover, in global indices."""
+def fwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None, cu_k=None):
+    """(query, key) token pairs a forward item's tiles cover, in global indices (keys in the
+    K/V stream's indices under cross-attention)."""
     b, m, _h, nb = (int(x) for x in item)
     if b < 0:                                     # token record (-1 - f, t0, h, rows)
         t0, rows = m, nb
@@ -164,9 +181,11 @@ def fwd_item_edges(cu_seqlens, item, BM: int, BN: int, window=None):
         return [(i, j) for i in range(t0, t0 + rows) for j in range(kb, t0 + rows)]
     s = int(cu_seqlens[b])
     l = int(cu_seqlens[b + 1]) - s
+    cuk = cu_seqlens if cu_k is None else cu_k
+    sk, lk = int(cuk[b]), int(cuk[b + 1]) - int(cuk[b])
     n0 = window_key_start(m, BM, BN, window)
     rows = range(s + m * BM, s + min(l, (m + 1) * BM))
-    cols = range(s + n0 * BN, s + min(l, (n0 + nb) * BN))
+    cols = range(sk + n0 * BN, sk + min(lk, (n0 + nb) * BN))
     return [(i, j) for i in rows for j in cols]
 
 

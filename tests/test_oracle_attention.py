@@ -375,3 +375,38 @@ def test_local_window_closed_forms():
         assert close(o1[t, h], w1 * v[t - 1, h] + w2 * v[t, h], 1e-12, 1e-12)
     with pytest.raises(ValueError):
         oa.varlen_forward(q, k, v, cu, scale, causal=False, window=2)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_cross_attention_against_sdpa(causal):
+    """cu_q != cu_k: each segment equals torch's float64 SDPA on its own Q slice and K/V slice,
+    causal with the bottom-right mask built as a shifted triangle (tril with diagonal lk - lq),
+    forward and autograd backward; lq = lk reduces to self-attention."""
+    rng = np.random.default_rng(3)
+    lq = [1, 5, 17, 3, 40]
+    lk = [1, 9, 17, 30, 41]
+    cuq, cuk = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    Tq, Tk, Hq, Hkv, d = cuq[-1], cuk[-1], 4, 2, 8
+    q, do = rng.standard_normal((Tq, Hq, d)), rng.standard_normal((Tq, Hq, d))
+    k, v = rng.standard_normal((Tk, Hkv, d)), rng.standard_normal((Tk, Hkv, d))
+    scale = 0.41
+    o, lse = oa.varlen_forward(q, k, v, cuq, scale, causal, cu_seqlens_k=cuk)
+    dq, dk, dv = oa.varlen_backward(q, k, v, o, lse, do, cuq, scale, causal, cu_seqlens_k=cuk)
+    for b in range(len(lq)):
+        s, e, sk, ek = cuq[b], cuq[b + 1], cuk[b], cuk[b + 1]
+        mask = torch.tril(torch.ones(lq[b], lk[b], dtype=torch.bool), diagonal=lk[b] - lq[b]) if causal else None
+        tq = torch.tensor(q[s:e].transpose(1, 0, 2), requires_grad=True)
+        tk, tv = (torch.tensor(x[sk:ek].transpose(1, 0, 2), requires_grad=True) for x in (k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk.repeat_interleave(2, 0), tv.repeat_interleave(2, 0), attn_mask=mask, scale=scale)
+        (to * torch.tensor(do[s:e].transpose(1, 0, 2))).sum().backward()
+        assert close(o[s:e], to.detach().numpy().transpose(1, 0, 2), 1e-12, 1e-10)
+        assert close(dq[s:e], tq.grad.numpy().transpose(1, 0, 2), 1e-12, 1e-9)
+        assert close(dk[sk:ek], tk.grad.numpy().transpose(1, 0, 2), 1e-12, 1e-9)
+        assert close(dv[sk:ek], tv.grad.numpy().transpose(1, 0, 2), 1e-12, 1e-9)
+    # a single query (lq = 1) under causality sees every key of its segment
+    o1, _ = oa.varlen_forward(q[:1], k[:9], v[:9], [0, 1], scale, True, cu_seqlens_k=[0, 9])
+    on, _ = oa.varlen_forward(q[:1], k[:9], v[:9], [0, 1], scale, False, cu_seqlens_k=[0, 9])
+    assert np.array_equal(o1, on)
+    with pytest.raises(ValueError):  # causal needs lq <= lk
+        oa.varlen_forward(q[:5], k[:3], v[:3], [0, 5], scale, True, cu_seqlens_k=[0, 3])

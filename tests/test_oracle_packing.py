@@ -417,3 +417,28 @@ def test_window_tile_maps_cover_each_allowed_edge_once(BM, BN, w):
         for b in set(int(x) for x in tm[:, 0]):
             blk = [int(r[1]) for r in tm if r[0] == b]
             assert blk == (sorted(blk, reverse=True) if tm is fm else sorted(blk))
+
+
+@pytest.mark.parametrize("BM,BN", [(2, 2), (4, 2), (2, 4), (256, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_cross_tile_maps_cover_each_allowed_edge_once(BM, BN, causal):
+    """cu_q != cu_k with bottom-right causal alignment (query i of a segment sees keys
+    j <= i + lk - lq): the q-block and kv-block maps cover every permitted (query, key) pair
+    exactly once, every listed tile holds one, and lq = lk gives the self-attention maps."""
+    lq = [1, 5, 17, 3, 40, 300, 129, 2]
+    lk = [1, 9, 17, 30, 41, 700, 129, 260]
+    cuq, cuk = [int(x) for x in np.cumsum([0] + lq)], [int(x) for x in np.cumsum([0] + lk)]
+    allowed = {(cuq[b] + i, cuk[b] + j) for b in range(len(lq)) for i in range(lq[b]) for j in range(lk[b])
+               if not causal or j <= i + lk[b] - lq[b]}
+    fm = ot.fwd_tile_map(cuq, 1, BM, BN, causal, 64, cu_k=cuk)
+    bm = ot.bwd_tile_map(cuq, 1, BM, BN, causal, 64, cu_k=cuk)
+    assert (fm[:, 0] >= 0).all() and (bm[:, 0] >= 0).all()   # no token records
+    for tm, edges in ((fm, ot.fwd_item_edges), (bm, ot.bwd_item_edges)):
+        seen = []
+        for it in tm:
+            hit = [e for e in edges(cuq, it, BM, BN, cu_k=cuk) if e in allowed]
+            assert hit, "a listed tile has no permitted edge"
+            seen.extend(hit)
+        assert sorted(seen) == sorted(allowed)
+    assert np.array_equal(ot.fwd_tile_map(cuq, 2, BM, BN, causal, cu_k=cuq), ot.fwd_tile_map(cuq, 2, BM, BN, causal))
+    assert np.array_equal(ot.bwd_tile_map(cuq, 2, BM, BN, causal, cu_k=cuq), ot.bwd_tile_map(cuq, 2, BM, BN, causal))
