@@ -44,7 +44,9 @@ Cross-attention (``cu_k``, section 5: the causal bound is aligned bottom-right,
 ceil(((m+1)*BM + lk - lq) / BN)): q block m of a segment with lq queries and lk keys has
 ceil(min(lk, (m+1)*BM + lk - lq) / BN) key blocks (ceil(lk / BN) non-causal); kv block n has
 its q blocks from floor(max(0, n*BN - (lk - lq)) / BM) (0 non-causal) to ceil(lq / BM) - 1.
-Same order keys; no token records.
+The key-block cap lk can give the last q blocks of a causal segment equal counts, so causal
+cross maps keep a segment's q blocks last-first (the same order whenever counts differ);
+kv blocks and non-causal maps keep the self-attention order.  No token records.
 
 Local window w (causal; section 5: "causal or local window further narrows
 n_block_min/max"): q block m's key blocks run from n_min = floor(max(0, m*BM - w) / BN)
@@ -99,7 +101,8 @@ def fwd_tile_map(cu_seqlens, Hq: int, BM: int, BN: int, causal: bool = True, sho
         cls = _cost_class(sum(nb for _, nb in blocks))
         for h in range(Hq):
             for m, nb in blocks:
-                items.append(((-cls, b, h, -m if window is not None else -nb, m), (b, m, h, nb)))
+                items.append(((-cls, b, h, -m if (window is not None or (causal and cu_k is not None)) else -nb, m),
+                              (b, m, h, nb)))
     items.sort(key=lambda t: t[0])
     out = [r for _, r in items] + _token_records(cu, tok, Hq, BM)
     return np.asarray(out, dtype=np.int32).reshape(-1, 4)
