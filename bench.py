@@ -515,6 +515,71 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ cross-attention
+
+def run_cross(args, rank, world, local_rank):
+    """Cross-attention (prefix-cache shape): every sft8k segment's queries attend to a P-token
+    prefix followed by the segment itself (lk = lq + P, causal aligned bottom-right).  One step =
+    forward + backward over `--packs` packs; the boundaries are built once, outside the step.
+    FLOPs count the visible edges of every segment (the tail pad included): i + P + 1 keys for
+    query i."""
+    import torch
+    import packed_sequence_varlen_gb300 as va
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    global WORKLOAD
+    WORKLOAD = "sft8k"
+    packs, idx, w = batch_packs(rank, (va.pack_next_fit, va.pack_best_fit_decreasing))
+    P, T, d, Hq, Hkv = args.cross_prefix, w.pad_to, w.d, w.Hq, w.Hkv
+    ins, edges_all = [], 0
+    for pi, docs in zip(idx, packs):
+        segs = docs + ([T - sum(docs)] if sum(docs) < T else [])
+        cuq = [0]
+        cuk = [0]
+        for x in segs:
+            cuq.append(cuq[-1] + x)
+            cuk.append(cuk[-1] + x + P)
+            edges_all += x * (x + 1) // 2 + x * P
+        q, _, _, do = si.tensors(T, Hq, Hkv, d, seed_offset=1000 * pi)
+        _, k, v, _ = si.tensors(cuk[-1], Hq, Hkv, d, seed_offset=1000 * pi + 1)
+        ins.append((q.to(dev), k.to(dev), v.to(dev), do.to(dev),
+                    torch.tensor(cuq, dtype=torch.int32, device=dev), torch.tensor(cuk, dtype=torch.int32, device=dev),
+                    max(segs), max(segs) + P))
+    step_flops = 14 * d * Hq * edges_all
+    ws_f = torch.empty(1 << 26, dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(1 << 28, dtype=torch.uint8, device=dev)
+
+    def step():
+        for q, k, v, do, cq, ck, mq, mk in ins:
+            o, lse = va.varlen_attn_fwd_cross(q, k, v, cq, ck, mq, mk, None, True, workspace=ws_f)
+            va.varlen_attn_bwd_cross(q, k, v, o, lse, do, cq, ck, mq, mk, None, True, workspace=ws_b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if va.read_status(ws_f) or va.read_status(ws_b):
+        raise RuntimeError("device-detected error in the cross-attention run")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks = load_peaks()
+    value = step_flops / (ms * 1e-3) / 1e12
+    return {"metric": "varlen causal cross-attention fwd+bwd TFLOP/s (visible edges)", "value": round(value, 3),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"cross: {len(packs)} sft8k pack(s) of {T} queries, each segment's keys a "
+                                   f"{P}-token prefix + the segment (Hq=Hkv={Hq}, d={d}), causal bottom-right",
+                       "pct_of_bf16_peak_burst": round(100 * value / peaks["bf16_tflops"], 2)},
+            "e2e": None, "clocks": clocks.summary()}
+
+
 # ------------------------------------------------------------------ packed loss
 
 def run_loss(args, rank, world, local_rank):
@@ -614,6 +679,8 @@ def main():
                     help="configuration (sft8k is the benchmark; the others are for measurement)")
     ap.add_argument("--window", type=int, default=None,
                     help="causal local window (query i sees keys i-w..i); FLOPs count in-window edges")
+    ap.add_argument("--cross-prefix", type=int, default=None,
+                    help="measure cross-attention: each segment's keys are a P-token prefix + the segment")
     ap.add_argument("--loss", action="store_true",
                     help="measure the packed loss (targets + token-weighted CE + gradient) instead")
     ap.add_argument("--vocab", type=int, default=32768, help="classes of the --loss logits")
@@ -638,7 +705,12 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    res = run_loss(args, rank, world, local_rank) if args.loss else run_ours(args, rank, world, local_rank)
+    if args.loss:
+        res = run_loss(args, rank, world, local_rank)
+    elif args.cross_prefix is not None:
+        res = run_cross(args, rank, world, local_rank)
+    else:
+        res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

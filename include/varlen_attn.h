@@ -293,6 +293,37 @@ va_status varlen_read_status(const void* ws_dev, int32_t* status_host, va_stream
 /* Clears the workspace status word (asynchronous). */
 va_status varlen_clear_status(void* ws_dev, va_stream_t stream);
 
+/* ---------------------------------------------------------------- cross-attention
+ * Q [Tq, Hq, d] cut by cu_seqlens_q[B+1] and K/V [Tk, Hkv, d] cut by cu_seqlens_k[B+1]: the
+ * b-th Q slice attends to the b-th K/V slice.  Source: "Packing与 FlashAttention Varlen",
+ * section 3 (cu_q and cu_k, each with the boundary contract; the b-th Q slice and K/V slice
+ * belong to the same sample) and section 5 (the causal bound is aligned bottom-right:
+ * (m+1)*BM + seqlen_k - seqlen_q).  Query i of segment b sees key j when j <= i + lk_b - lq_b
+ * (causal) or always (non-causal).  Reading taken here: causal calls need lq_b <= lk_b in every
+ * segment (every query sees a key); a segment with lq_b > lk_b, or a cu_seqlens_k that breaks
+ * the contract (first 0, last Tk, strictly increasing, lengths <= max_seqlen_k), sets
+ * VA_ERR_BAD_SEQLENS in the status word.  shape describes the Q side (T = Tq, max_seqlen =
+ * longest Q segment) and every stride; Tk and max_seqlen_k the K/V side.  No token tiles, no
+ * local window.  Outputs as varlen_attn_fwd / varlen_attn_bwd (dk, dv have K's rows). */
+size_t varlen_attn_workspace_size_cross(const va_shape* shape, int32_t Tk, int32_t for_bwd);
+
+va_status varlen_attn_plan_cross(const va_shape* shape, const int32_t* cu_seqlens_q_dev,
+                                 const int32_t* cu_seqlens_k_dev, int32_t Tk, int32_t kind, int32_t causal,
+                                 int32_t* tile_map_dev, int32_t capacity, int32_t* n_items_dev,
+                                 int32_t* scratch_dev, va_stream_t stream);
+
+va_status varlen_attn_fwd_cross(const void* q_dev, const void* k_dev, const void* v_dev,
+                                const int32_t* cu_seqlens_q_dev, const int32_t* cu_seqlens_k_dev,
+                                const va_shape* shape, int32_t Tk, int32_t max_seqlen_k, float scale,
+                                int32_t causal, void* out_dev, float* lse_dev, void* ws_dev, size_t ws_bytes,
+                                va_stream_t stream);
+
+va_status varlen_attn_bwd_cross(const void* q_dev, const void* k_dev, const void* v_dev, const void* out_dev,
+                                const float* lse_dev, const void* dout_dev, const int32_t* cu_seqlens_q_dev,
+                                const int32_t* cu_seqlens_k_dev, const va_shape* shape, int32_t Tk,
+                                int32_t max_seqlen_k, float scale, int32_t causal, void* dq_dev, void* dk_dev,
+                                void* dv_dev, void* ws_dev, size_t ws_bytes, va_stream_t stream);
+
 /* ---------------------------------------------------------------- padded-batch bridge
  * A batch padded to [Bp, S] with a 2-D attention mask enters the varlen path by dropping its
  * padding, and the packed output goes back to the padded shape.  Source: "Packing与

@@ -22,7 +22,8 @@ __all__ = [
     "pack_next_fit", "pack_best_fit_decreasing", "build_metadata", "validate_cu_seqlens",
     "tile_sizes", "workspace_size", "plan", "varlen_attn_fwd", "varlen_attn_bwd", "varlen_attn",
     "read_status", "VarlenError", "make_shape", "library_path", "loss_targets", "token_ce",
-    "IGNORE_INDEX", "unpad_index", "gather_rows", "unpad", "pad",
+    "IGNORE_INDEX", "unpad_index", "gather_rows", "unpad", "pad", "plan_cross", "varlen_attn_fwd_cross",
+    "varlen_attn_bwd_cross",
 ]
 
 
@@ -269,6 +270,74 @@ def varlen_attn(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None
                 causal: bool = True, window: int | None = None):
     """Differentiable packed attention: out [T, Hq, d] (``window``: causal local window)."""
     return _VarlenAttn.apply(q, k, v, cu_seqlens, max_seqlen, scale, causal, window)
+
+
+# ----------------------------------------------------------------- cross-attention
+
+def plan_cross(cu_q: torch.Tensor, cu_k: torch.Tensor, Tq: int, Tk: int, Hq: int, Hkv: int, d: int,
+               max_seqlen_q: int, kind: int = 0, causal: bool = True):
+    """Cross-attention tile map on the device: (records int32 [n, 4], n)."""
+    B = cu_q.numel() - 1
+    s = _contig_shape(Tq, B, Hq, Hkv, d, max_seqlen_q)
+    BM, BN = tile_sizes(kind, d)
+    cap = ((Tk // BN) + B) * Hkv if kind == 1 else (Tq // BM + B) * Hq
+    tm = torch.empty((max(cap, 1), 4), dtype=torch.int32, device=cu_q.device)
+    n = torch.zeros(1, dtype=torch.int32, device=cu_q.device)
+    scratch = torch.empty(B + 4, dtype=torch.int32, device=cu_q.device)
+    check(_lib.load().varlen_attn_plan_cross(ctypes.byref(s), _ptr(cu_q), _ptr(cu_k), Tk, kind, int(causal),
+                                             _ptr(tm), cap, _ptr(n), _ptr(scratch), _stream(cu_q.device)))
+    k = int(n.item())
+    return tm[:k], k
+
+
+def varlen_attn_fwd_cross(q, k, v, cu_q, cu_k, max_seqlen_q: int, max_seqlen_k: int, scale: float | None = None,
+                          causal: bool = True, out=None, lse=None, workspace=None, check_status=False):
+    """Cross-attention forward (q [Tq,Hq,d] against k/v [Tk,Hkv,d], boundaries cu_q / cu_k;
+    causal aligned bottom-right): returns (out [Tq,Hq,d] bf16, lse [Hq,Tq] fp32)."""
+    _check_inputs(q, k, v)
+    Tq, Hq, d = q.shape
+    Tk = k.shape[0]
+    B = cu_q.numel() - 1
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    s = make_shape(q, k, v, B, max_seqlen_q, out)
+    lib = _lib.load()
+    need = lib.varlen_attn_workspace_size_cross(ctypes.byref(s), Tk, 0)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    check(lib.varlen_attn_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), ctypes.byref(s), Tk,
+                                    int(max_seqlen_k), scale, int(causal), _ptr(out), _ptr(lse), _ptr(workspace),
+                                    workspace.numel(), _stream(q.device)))
+    if check_status:
+        _raise_status(workspace)
+    return out, lse
+
+
+def varlen_attn_bwd_cross(q, k, v, out, lse, dout, cu_q, cu_k, max_seqlen_q: int, max_seqlen_k: int,
+                          scale: float | None = None, causal: bool = True, workspace=None, check_status=False):
+    """Cross-attention backward: returns (dq, dk, dv) bf16 with the shapes of q, k, v."""
+    _check_inputs(q, k, v, out, dout)
+    Tq, Hq, d = q.shape
+    Tk = k.shape[0]
+    B = cu_q.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_strided(out.shape, out.stride(), dtype=q.dtype, device=q.device)
+    dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    dv = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    s = make_shape(q, k, v, B, max_seqlen_q, out)
+    lib = _lib.load()
+    need = lib.varlen_attn_workspace_size_cross(ctypes.byref(s), Tk, 1)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    check(lib.varlen_attn_bwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(cu_q),
+                                    _ptr(cu_k), ctypes.byref(s), Tk, int(max_seqlen_k), scale, int(causal), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(q.device)))
+    if check_status:
+        _raise_status(workspace)
+    return dq, dk, dv
 
 
 # ----------------------------------------------------------------- packed loss

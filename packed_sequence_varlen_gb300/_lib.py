@@ -29,6 +29,8 @@ EXPORTS = (
     "varlen_loss_targets", "varlen_token_ce_workspace_size", "varlen_token_ce",
     "varlen_unpad_index", "varlen_gather_rows",
     "varlen_attn_plan_window", "varlen_attn_fwd_window", "varlen_attn_bwd_window",
+    "varlen_attn_workspace_size_cross", "varlen_attn_plan_cross", "varlen_attn_fwd_cross",
+    "varlen_attn_bwd_cross",
 )
 
 
@@ -81,6 +83,16 @@ def _declare(lib):
         "varlen_attn_bwd_window": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, POINTER(VaShape), c_float, c_int32, c_int32,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+        "varlen_attn_workspace_size_cross": (c_size_t, [POINTER(VaShape), c_int32, c_int32]),
+        "varlen_attn_plan_cross": (c_int32, [POINTER(VaShape), c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                             c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
+        "varlen_attn_fwd_cross": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(VaShape),
+                                            c_int32, c_int32, c_float, c_int32, c_void_p, c_void_p, c_void_p,
+                                            c_size_t, c_void_p]),
+        "varlen_attn_bwd_cross": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_void_p, POINTER(VaShape), c_int32, c_int32, c_float,
+                                            c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                            c_void_p]),
         "varlen_attn_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                               POINTER(VaShape), c_float, c_int32, c_void_p,
                                               c_void_p, c_void_p]),

@@ -18,13 +18,13 @@ cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaSt
 cudaError_t launch_cu_from_positions(const int32_t*, int, int, int, int32_t*, int, int32_t*, int32_t*,
                                      int32_t*, cudaStream_t);
 cudaError_t launch_plan(const PlanArgs&, cudaStream_t);
-cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, cudaStream_t);
+cudaError_t launch_validate_plan(const PlanArgs*, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_fwd_tc(const FwdParams&, int, int, cudaStream_t);
 cudaError_t launch_fwd_tok(const FwdParams&, int, int, cudaStream_t);
 void fwd_tc_tiles(int*, int*);
 int fwd_tc_token_short();
 int bwd_tc_token_short();
-cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, cudaStream_t);
+cudaError_t launch_bwd_prep(const BwdParams&, const PlanArgs*, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_unpad_index(int, const int32_t*, int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
                                int32_t*, cudaStream_t);
 cudaError_t launch_gather_rows(const void*, int64_t, const int32_t*, int, int64_t, void*, int64_t, cudaStream_t);
@@ -114,13 +114,24 @@ void tiles(int kind, int* BM, int* BN) {
   }
 }
 
-// Upper bound on records of a map: blocks per segment <= l/blk + 1.
-int64_t map_capacity(const va_shape& s, int kind) {
+// Upper bound on records of a map: blocks per segment <= l/blk + 1.  Tk: rows of K/V
+// (cross-attention; -1 = s.T), which the kv-block map is cut from.
+int64_t map_capacity(const va_shape& s, int kind, int Tk = -1) {
   int BM, BN;
   tiles(kind, &BM, &BN);
   const int blk = kind == 1 ? BN : BM;
   const int heads = kind == 1 ? s.Hkv : s.Hq;
-  return (static_cast<int64_t>(s.T) / blk + s.B) * heads;
+  const int rows = kind == 1 && Tk >= 0 ? Tk : s.T;
+  return (static_cast<int64_t>(rows) / blk + s.B) * heads;
+}
+
+// Cross-attention arguments: the K/V stream's rows and longest segment.
+va_status check_cross(const va_shape* s, const int32_t* cu_k, int32_t Tk, int32_t max_k, int32_t window) {
+  if (!cu_k) return fail(VA_ERR_INVALID_ARG, "cross: cu_seqlens_k is null");
+  if (Tk < 1 || max_k < 1 || max_k > Tk) return fail(VA_ERR_INVALID_ARG, "cross: Tk >= 1 and 1 <= max_seqlen_k <= Tk");
+  if (static_cast<int64_t>(Tk) * s->Hkv >= (int64_t(1) << 31)) return fail(VA_ERR_UNSUPPORTED, "Tk * Hkv must stay below 2^31");
+  if (window != -1) return fail(VA_ERR_UNSUPPORTED, "cross: no local window");
+  return VA_OK;
 }
 
 va_status check_shape(const va_shape* s) {
@@ -158,9 +169,9 @@ struct BwdLayout {
   size_t dsum, kvmap, qmap, segoff, total;
   int64_t cap_kv, cap_q;
 };
-BwdLayout bwd_layout(const va_shape& s) {
+BwdLayout bwd_layout(const va_shape& s, int Tk = -1) {
   BwdLayout L;
-  L.cap_kv = map_capacity(s, 1);
+  L.cap_kv = map_capacity(s, 1, Tk);
   L.cap_q = map_capacity(s, 2);
   L.dsum = sizeof(WsHeader);
   L.kvmap = align256(L.dsum + static_cast<size_t>(s.Hq) * s.T * sizeof(float));
@@ -174,6 +185,17 @@ BwdLayout bwd_layout(const va_shape& s) {
 }  // namespace va
 
 using namespace va;
+
+static va_status plan_impl(const va_shape* s, const int32_t* cu_dev, const int32_t* cu_k, int32_t Tk, int32_t kind,
+                           int32_t causal, int32_t window, int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
+                           int32_t* scratch_dev, va_stream_t stream);
+static va_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* cu, const int32_t* cu_k,
+                          int32_t Tk, int32_t max_k, const va_shape* s, float scale, int32_t causal, int32_t window,
+                          void* out, float* lse, void* ws, size_t ws_bytes, va_stream_t stream);
+static va_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                          const void* dout, const int32_t* cu, const int32_t* cu_k, int32_t Tk, int32_t max_k,
+                          const va_shape* s, float scale, int32_t causal, int32_t window, void* dq, void* dk, void* dv,
+                          void* ws, size_t ws_bytes, va_stream_t stream);
 
 extern "C" {
 
@@ -269,13 +291,28 @@ va_status varlen_attn_plan(const va_shape* s, const int32_t* cu_dev, int32_t kin
 va_status varlen_attn_plan_window(const va_shape* s, const int32_t* cu_dev, int32_t kind, int32_t causal,
                                   int32_t window, int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
                                   int32_t* scratch_dev, va_stream_t stream) {
+  return plan_impl(s, cu_dev, nullptr, -1, kind, causal, window, map_dev, capacity, n_items_dev, scratch_dev, stream);
+}
+
+va_status varlen_attn_plan_cross(const va_shape* s, const int32_t* cu_q, const int32_t* cu_k, int32_t Tk, int32_t kind,
+                                 int32_t causal, int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
+                                 int32_t* scratch_dev, va_stream_t stream) {
+  return plan_impl(s, cu_q, cu_k, Tk, kind, causal, -1, map_dev, capacity, n_items_dev, scratch_dev, stream);
+}
+
+}  // extern "C"
+
+static va_status plan_impl(const va_shape* s, const int32_t* cu_dev, const int32_t* cu_k, int32_t Tk, int32_t kind,
+                           int32_t causal, int32_t window, int32_t* map_dev, int32_t capacity, int32_t* n_items_dev,
+                           int32_t* scratch_dev, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
+  if (cu_k && (st = check_cross(s, cu_k, Tk, std::max(Tk, 1), window)) != VA_OK) return st;
   if (window < -1 || (window >= 0 && !causal)) return fail(VA_ERR_INVALID_ARG, "plan: window needs causal and >= 0 (-1 = none)");
   if (kind < 0 || kind > 2 || !cu_dev || !map_dev || !n_items_dev || !scratch_dev || capacity < 0)
     return fail(VA_ERR_INVALID_ARG, "plan: bad kind or null pointer");
   if (!aligned16(map_dev)) return fail(VA_ERR_INVALID_ARG, "plan: tile map must be 16-byte aligned");
-  if (map_capacity(*s, kind) > capacity)
+  if (map_capacity(*s, kind, cu_k ? Tk : -1) > capacity)
     return fail(VA_ERR_WORKSPACE, "plan: capacity below the record bound (T/blk + B) * heads");
   int BM, BN;
   tiles(kind, &BM, &BN);
@@ -283,11 +320,15 @@ va_status varlen_attn_plan_window(const va_shape* s, const int32_t* cu_dev, int3
   const PlanArgs pa{cu_dev, s->B, kind == 1 ? s->Hkv : s->Hq, BM, BN, kind, causal ? 1 : 0,
                     reinterpret_cast<TileItem*>(map_dev), capacity, nullptr, n_items_dev,
                     scratch_dev + 4, scratch_dev,
-                    !token_tiles(*s, causal, window) ? 0 : kind == 0 ? fwd_tc_token_short() : bwd_tc_token_short(),
-                    nullptr, nullptr, window};
+                    (cu_k || !token_tiles(*s, causal, window)) ? 0
+                    : kind == 0                                ? fwd_tc_token_short()
+                                                               : bwd_tc_token_short(),
+                    nullptr, nullptr, window, cu_k};
   cudaError_t e = launch(K_PLAN, cs, [&] { return launch_plan(pa, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "plan");
 }
+
+extern "C" {
 
 va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
                           const va_shape* s, float scale, int32_t causal, void* out, float* lse,
@@ -298,8 +339,23 @@ va_status varlen_attn_fwd(const void* q, const void* k, const void* v, const int
 va_status varlen_attn_fwd_window(const void* q, const void* k, const void* v, const int32_t* cu,
                                  const va_shape* s, float scale, int32_t causal, int32_t window, void* out,
                                  float* lse, void* ws, size_t ws_bytes, va_stream_t stream) {
+  return fwd_impl(q, k, v, cu, nullptr, -1, 0, s, scale, causal, window, out, lse, ws, ws_bytes, stream);
+}
+
+va_status varlen_attn_fwd_cross(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                                const int32_t* cu_k, const va_shape* s, int32_t Tk, int32_t max_seqlen_k, float scale,
+                                int32_t causal, void* out, float* lse, void* ws, size_t ws_bytes, va_stream_t stream) {
+  return fwd_impl(q, k, v, cu_q, cu_k, Tk, max_seqlen_k, s, scale, causal, -1, out, lse, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+static va_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* cu, const int32_t* cu_k,
+                          int32_t Tk, int32_t max_k, const va_shape* s, float scale, int32_t causal, int32_t window,
+                          void* out, float* lse, void* ws, size_t ws_bytes, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
+  if (cu_k && (st = check_cross(s, cu_k, Tk, max_k, window)) != VA_OK) return st;
   if (window < -1 || (window >= 0 && !causal)) return fail(VA_ERR_INVALID_ARG, "fwd: window needs causal and >= 0 (-1 = none)");
   if (!q || !k || !v || !cu || !out || !lse || !ws)
     return fail(VA_ERR_INVALID_ARG, "fwd: null pointer");
@@ -320,14 +376,14 @@ va_status varlen_attn_fwd_window(const void* q, const void* k, const void* v, co
   }
   int BM, BN;
   tiles(0, &BM, &BN);
-  const bool tok = token_tiles(*s, causal, window);
+  const bool tok = !cu_k && token_tiles(*s, causal, window);
   const PlanArgs pa{cu, s->B, s->Hq, BM, BN, 0, causal ? 1 : 0, map, static_cast<int>(L.cap),
                     &hdr->status, &hdr->n_items[0],
                     reinterpret_cast<int32_t*>(w + L.segoff), &hdr->counter[0],
                     tok ? fwd_tc_token_short() : 0, &hdr->n_items[kTokSlot],
-                    &hdr->counter[kTokSlot], window};
+                    &hdr->counter[kTokSlot], window, cu_k};
   cudaError_t e = launch(K_VALIDATE_PLAN, cs, [&] {
-    return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cs);
+    return launch_validate_plan(&pa, 1, s->T, s->max_seqlen, cu_k ? Tk : 0, cu_k ? max_k : 0, cs);
   });
   if (e != cudaSuccess) return cuda_fail(e, "fwd plan");
   FwdParams p{};
@@ -357,6 +413,8 @@ va_status varlen_attn_fwd_window(const void* q, const void* k, const void* v, co
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
   p.window = window;
+  p.cu_k = cu_k;
+  p.Tk = cu_k ? Tk : 0;
   // segment records, then (as its programmatic dependent, filling its tail) token records
   e = launch(K_FWD, cs, [&] { return launch_fwd_tc(p, s->d, static_cast<int>(L.cap), cs); });
   if (e != cudaSuccess) return cuda_fail(e, "fwd kernel");
@@ -366,6 +424,8 @@ va_status varlen_attn_fwd_window(const void* q, const void* k, const void* v, co
   e = launch(K_FWD_TOK, cs, [&] { return launch_fwd_tok(pt, s->d, static_cast<int>(L.cap), cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "fwd token kernel");
 }
+
+extern "C" {
 
 va_status varlen_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                           const float* lse, const void* dout, const int32_t* cu, const va_shape* s,
@@ -379,8 +439,32 @@ va_status varlen_attn_bwd_window(const void* q, const void* k, const void* v, co
                                  const float* lse, const void* dout, const int32_t* cu, const va_shape* s,
                                  float scale, int32_t causal, int32_t window, void* dq, void* dk, void* dv,
                                  void* ws, size_t ws_bytes, va_stream_t stream) {
+  return bwd_impl(q, k, v, out, lse, dout, cu, nullptr, -1, 0, s, scale, causal, window, dq, dk, dv, ws, ws_bytes,
+                  stream);
+}
+
+va_status varlen_attn_bwd_cross(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                const void* dout, const int32_t* cu_q, const int32_t* cu_k, const va_shape* s,
+                                int32_t Tk, int32_t max_seqlen_k, float scale, int32_t causal, void* dq, void* dk,
+                                void* dv, void* ws, size_t ws_bytes, va_stream_t stream) {
+  return bwd_impl(q, k, v, out, lse, dout, cu_q, cu_k, Tk, max_seqlen_k, s, scale, causal, -1, dq, dk, dv, ws,
+                  ws_bytes, stream);
+}
+
+size_t varlen_attn_workspace_size_cross(const va_shape* s, int32_t Tk, int32_t for_bwd) {
+  if (check_shape(s) != VA_OK || Tk < 1) return 0;
+  return for_bwd ? bwd_layout(*s, Tk).total : fwd_layout(*s).total;
+}
+
+}  // extern "C"
+
+static va_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                          const void* dout, const int32_t* cu, const int32_t* cu_k, int32_t Tk, int32_t max_k,
+                          const va_shape* s, float scale, int32_t causal, int32_t window, void* dq, void* dk, void* dv,
+                          void* ws, size_t ws_bytes, va_stream_t stream) {
   va_status st = check_shape(s);
   if (st != VA_OK) return st;
+  if (cu_k && (st = check_cross(s, cu_k, Tk, max_k, window)) != VA_OK) return st;
   if (window < -1 || (window >= 0 && !causal)) return fail(VA_ERR_INVALID_ARG, "bwd: window needs causal and >= 0 (-1 = none)");
   if (!q || !k || !v || !out || !lse || !dout || !cu || !dq || !dk || !dv || !ws)
     return fail(VA_ERR_INVALID_ARG, "bwd: null pointer");
@@ -388,7 +472,7 @@ va_status varlen_attn_bwd_window(const void* q, const void* k, const void* v, co
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(ws))
     return fail(VA_ERR_INVALID_ARG, "bwd: pointers must be 16-byte aligned");
   if (!(scale > 0.f) || !(scale < INFINITY)) return fail(VA_ERR_INVALID_ARG, "bwd: scale must be finite and > 0");
-  const BwdLayout L = bwd_layout(*s);
+  const BwdLayout L = bwd_layout(*s, cu_k ? Tk : -1);
   if (ws_bytes < L.total) return fail(VA_ERR_WORKSPACE, "bwd: workspace too small");
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -404,15 +488,15 @@ va_status varlen_attn_bwd_window(const void* q, const void* k, const void* v, co
   int BM, BN, BM2, BN2;
   tiles(1, &BM, &BN);
   tiles(2, &BM2, &BN2);
-  const bool tok = token_tiles(*s, causal, window);
+  const bool tok = !cu_k && token_tiles(*s, causal, window);
   int32_t* segoff = reinterpret_cast<int32_t*>(w + L.segoff);
   const PlanArgs pa[2] = {
       {cu, s->B, s->Hkv, BM, BN, 1, causal ? 1 : 0, kvmap, static_cast<int>(L.cap_kv), &hdr->status,
        &hdr->n_items[1], segoff, &hdr->counter[1], tok ? bwd_tc_token_short() : 0,
-       &hdr->n_items[kKvTokSlot], nullptr, window},
+       &hdr->n_items[kKvTokSlot], nullptr, window, cu_k},
       {cu, s->B, s->Hq, BM2, BN2, 2, causal ? 1 : 0, qmap, static_cast<int>(L.cap_q), &hdr->status,
        &hdr->n_items[2], segoff, &hdr->counter[2], tok ? bwd_tc_token_short() : 0,
-       &hdr->n_items[kQTokSlot], nullptr, window}};
+       &hdr->n_items[kQTokSlot], nullptr, window, cu_k}};
   BwdParams p{};
   p.q = static_cast<const bf16*>(q);
   p.k = static_cast<const bf16*>(k);
@@ -451,14 +535,20 @@ va_status varlen_attn_bwd_window(const void* q, const void* k, const void* v, co
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
   p.window = window;
+  p.cu_k = cu_k;
+  p.Tk = cu_k ? Tk : 0;
   // one launch validates, plans both maps and computes D = rowsum(dO * O)
-  cudaError_t e = launch(K_BWD_PREP, cs, [&] { return launch_bwd_prep(p, pa, 2, s->T, s->max_seqlen, s->d, cs); });
+  cudaError_t e = launch(K_BWD_PREP, cs, [&] {
+    return launch_bwd_prep(p, pa, 2, s->T, s->max_seqlen, cu_k ? Tk : 0, cu_k ? max_k : 0, s->d, cs);
+  });
   if (e == cudaSuccess)
     e = launch(K_BWD_DKDV, cs, [&] { return launch_bwd_dkdv_tc(p, s->d, static_cast<int>(L.cap_kv), tok, cs); });
   if (e == cudaSuccess)
     e = launch(K_BWD_DQ, cs, [&] { return launch_bwd_dq_tc(p, s->d, static_cast<int>(L.cap_q), tok, cs); });
   return e == cudaSuccess ? VA_OK : cuda_fail(e, "bwd kernels");
 }
+
+extern "C" {
 
 va_status varlen_unpad_index(const int32_t* mask, int32_t Bp, int32_t S, int32_t* indices, int32_t* inverse,
                              int32_t* cu, int32_t* T_out, int32_t* max_out, int32_t* status, va_stream_t stream) {

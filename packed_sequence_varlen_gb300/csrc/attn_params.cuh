@@ -23,6 +23,8 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int causal;
   int window = -1;   // causal local window: query i sees keys i-w..i; -1 = none
+  const int32_t* cu_k = nullptr;  // cross-attention: K/V boundaries (cu is Q's); null = cu
+  int Tk = 0;                     // cross-attention: rows of K and V
 };
 
 struct BwdParams {
@@ -51,6 +53,8 @@ struct BwdParams {
   float scale_log2;
   int causal;
   int window = -1;   // causal local window: query i sees keys i-w..i; -1 = none
+  const int32_t* cu_k = nullptr;  // cross-attention: K/V boundaries (cu is Q's); null = cu
+  int Tk = 0;                     // cross-attention: rows of K and V
 };
 
 }  // namespace va

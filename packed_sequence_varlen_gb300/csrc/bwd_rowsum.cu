@@ -96,13 +96,15 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) bwd_prep_kernel(cons
   rowsum_body<D, VB>(p, blockIdx.x - 1, gridDim.x - 1);
 }
 
-cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps, int T, int max_seqlen, int d,
-                            cudaStream_t st) {
+cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps, int T, int max_seqlen, int Tk,
+                            int max_seqlen_k, int d, cudaStream_t st) {
   PlanPair pp{};
   for (int i = 0; i < nmaps && i < 2; ++i) pp.map[i] = maps[i];
   pp.nmaps = nmaps;
   pp.T = T;
   pp.max_seqlen = max_seqlen;
+  pp.Tk = Tk;
+  pp.max_seqlen_k = max_seqlen_k;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -81,7 +81,7 @@ struct KvCfg {
                        B_IF = B_DR + 1, B_IE = B_IF + 2, B_LF = B_IE + 2, B_LE = B_LF + LDS,
                        NBAR = B_LE + LDS;
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
-  static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 32;   // four 128-byte row tables (item k & 3)
+  static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 48;   // four 128-byte row tables (item k & 3)
   static constexpr int MISC_OFF = ROWS_OFF + 4 * KB;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
   __host__ __device__ static constexpr uint32_t kv_off(int b) { return static_cast<uint32_t>(b) * 2 * TKV; }
@@ -97,9 +97,11 @@ struct KvItem {
   int s0, l, n, hk, m_start, steps;
   int valid;
   int kvn;
+  int s0k, lk, off;  // cross-attention: the keys' first row and count, the causal offset lk - l
 };
+static_assert(sizeof(KvItem) <= 48, "queue slots are 48 bytes");
 
-template <bool WIN>
+template <bool WIN, bool X>
 __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
   const TileItem it = p.kv_items[idx];
   KvItem r;
@@ -110,6 +112,11 @@ __device__ __forceinline__ KvItem kv_decode(const BwdParams& p, int idx) {
   const int Mq = (r.l + 63) / 64;
   // the q steps start at the diagonal; without a window they run to the segment's end
   r.m_start = WIN ? it.blk * 2 : Mq - it.count;
+  if (X) {  // keys from cu_k; the diagonal moves by the offset lk - l (bottom-right alignment)
+    r.s0k = p.cu_k[it.seg];
+    r.lk = p.cu_k[it.seg + 1] - r.s0k;
+    r.off = p.causal ? r.lk - r.l : 0;
+  }
   r.steps = it.count * p.g;
   r.kvn = 0;
   return r;
@@ -168,7 +175,9 @@ __device__ __forceinline__ KvItem kv_token_decode_w(const BwdParams& p, int idx,
 
 // WIN: causal local window p.window: a kv block's q steps stop at the window of its last key
 // row, and steps that cross a key's window edge also mask the queries past key + w.
-template <int D, bool TOK, bool WIN>
+// X: cross-attention (p.cu_k): the kv block's keys come from their own boundaries; query i
+// sees key j when j <= i + lk - lq, so the q steps start at floor(max(0, n*128 - off) / 64).
+template <int D, bool TOK, bool WIN, bool X>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   KvItem* queue = reinterpret_cast<KvItem*>(sm + C::QUEUE_OFF);
   uint8_t* row_tables = sm + C::ROWS_OFF;
-  auto dec = [&](int idx) { return kv_decode<WIN>(p, idx); };
+  auto dec = [&](int idx) { return kv_decode<WIN, X>(p, idx); };
   // Launched as a programmatic dependent of the preparation kernel: its maps, D and status
   // are read only after the wait.  The dQ kernel, which reads the same products but none
   // of this kernel's, may then start on SMs as this kernel's CTAs finish.
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) idx = atomicAdd(p.kv_counter, 1);
         idx = __shfl_sync(0xffffffffu, idx, 0);
         if (idx < n_seg) {
-          out = kv_decode<WIN>(p, idx);
+          out = kv_decode<WIN, X>(p, idx);
           out.valid = 1;
         } else if (idx < n_items) {
           out = kv_token_decode_w(p, idx, row_tables + (k & 3) * C::KB);
@@ -283,9 +292,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_expect_tx_w(bar(C::B_KVF + kb), 2 * C::TKV);
         for (int pn = 0; pn < D / 64; ++pn) {
           tma_load_3d_w(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, J.hk,
-                      J.s0 + J.n * 128);
+                      (X ? J.s0k : J.s0) + J.n * 128);
           tma_load_3d_w(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
-                      J.hk, J.s0 + J.n * 128);
+                      J.hk, (X ? J.s0k : J.s0) + J.n * 128);
         }
         kv_issued = j + 1;
         return true;
@@ -494,11 +503,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++sf;
         fence_after_sync();
         const int q0 = (I.m_start + i / p.g) * 64;
-        const int lim = kvrow - q0;  // query columns c < lim are masked (key after query)
+        const int lim = kvrow - (X ? I.off : 0) - q0;  // query columns c < lim are masked (key after query)
         // (window) query columns c >= hi are masked too: past the key's window
         const int hi = WIN ? kvrow + p.window + 1 - q0 : 0;
         const bool need_mask =
-            p.causal && (I.n * 128 + 127 > q0 || (WIN && q0 + 63 > I.n * 128 + p.window));
+            p.causal && (I.n * 128 + 127 - (X ? I.off : 0) > q0 || (WIN && q0 + 63 > I.n * 128 + p.window));
         const float* L = ldring + ls * 128;
         const float* Dd = L + 64;
         // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
@@ -546,8 +555,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       fence_after_sync();
       const float mul = x == 0 ? 1.f : p.scale;
-      const bool store = kvrow < I.l;
-      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>(I.s0 + kvrow) * p.k_rs +
+      const bool store = kvrow < (X ? I.lk : I.l);
+      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>((X ? I.s0k : I.s0) + kvrow) * p.k_rs +
                   static_cast<int64_t>(I.hk) * p.k_hs;
       {
         uint32_t o[D];  // the whole accumulator row in one TMEM round trip
@@ -683,7 +692,7 @@ struct QCfg {
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 2, B_DR = B_AE + 2,
                        B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;  // AF/AE: per dQ buffer
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
-  static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 32;   // four 128-byte row tables (item k & 3)
+  static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 48;   // four 128-byte row tables (item k & 3)
   static constexpr int MISC_OFF = ROWS_OFF + 4 * QB;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
   __host__ __device__ static constexpr uint32_t qd_off(int b) { return static_cast<uint32_t>(b) * 2 * TQ; }
@@ -699,9 +708,11 @@ struct QItem {
   int s0, l, m, h, hk, nb;
   int valid;
   int kb;
+  int lk, off;  // cross-attention: the keys' count, the causal offset lk - l
 };
+static_assert(sizeof(QItem) <= 48, "queue slots are 48 bytes");
 
-template <bool WIN>
+template <bool WIN, bool X>
 __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
   const TileItem it = p.q_items[idx];
   QItem r;
@@ -713,6 +724,11 @@ __device__ __forceinline__ QItem q_decode(const BwdParams& p, int idx) {
   r.nb = it.count;
   // key steps from the segment start, or (window) from the window of the item's first row
   r.kb = WIN ? r.s0 + max(0, it.blk * 128 - p.window) / 64 * 64 : r.s0;
+  if (X) {  // keys from cu_k, the causal bound moved by lk - l (bottom-right alignment)
+    r.kb = p.cu_k[it.seg];
+    r.lk = p.cu_k[it.seg + 1] - r.kb;
+    r.off = p.causal ? r.lk - r.l : 0;
+  }
   return r;
 }
 
@@ -759,7 +775,9 @@ __device__ __forceinline__ QItem q_token_decode_w(const BwdParams& p, int idx, u
 
 // WIN: causal local window p.window: an item's key steps start at the window of its first
 // row, and steps that cross a query's window edge also mask the keys before query - w.
-template <int D, bool TOK, bool WIN>
+// X: cross-attention (p.cu_k): the keys come from their own boundaries and query i sees key
+// j when j <= i + lk - lq.
+template <int D, bool TOK, bool WIN, bool X>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -779,7 +797,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   QItem* queue = reinterpret_cast<QItem*>(sm + C::QUEUE_OFF);
   uint8_t* row_tables = sm + C::ROWS_OFF;
-  auto dec = [&](int idx) { return q_decode<WIN>(p, idx); };
+  auto dec = [&](int idx) { return q_decode<WIN, X>(p, idx); };
   if (p.hdr->status != VA_OK) return;
   const int n_items = p.hdr->n_items[p.q_slot];
   const int n_seg = n_items - p.hdr->n_items[p.q_tok_slot];  // segment records, then token ones
@@ -843,7 +861,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) idx = atomicAdd(p.q_counter, 1);
         idx = __shfl_sync(0xffffffffu, idx, 0);
         if (idx < n_seg) {
-          out = q_decode<WIN>(p, idx);
+          out = q_decode<WIN, X>(p, idx);
           out.valid = 1;
         } else if (idx < n_items) {
           out = q_token_decode_w(p, idx, row_tables + (k & 3) * C::QB);
@@ -1079,10 +1097,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // key columns c > lim are masked: after the query (causal) or past the segment end;
         // (window) key columns c < lo too: before the query's window
         const int kn = WIN ? I.kb - I.s0 + n * 64 : n * 64;  // the step's first key, segment-local
-        const int lim = p.causal ? qrow - kn : I.l - 1 - n * 64;
+        int lim = p.causal ? qrow - kn : I.l - 1 - n * 64;
         const int lo = WIN ? qrow - p.window - kn : 0;
-        const bool need_mask = p.causal ? (kn + 63 > I.m * 128 || (WIN && kn < I.m * 128 + 127 - p.window))
-                                        : (n * 64 + 64 > I.l);
+        bool need_mask = p.causal ? (kn + 63 > I.m * 128 || (WIN && kn < I.m * 128 + 127 - p.window))
+                                  : (n * 64 + 64 > I.l);
+        if constexpr (X) {
+          lim = p.causal ? qrow + I.off - kn : I.lk - 1 - kn;
+          need_mask = p.causal ? (kn + 63 > I.m * 128 + I.off) : (kn + 64 > I.lk);
+        }
         // one TMEM round trip: the step's 64 scores and 64 dP values of this q row
         uint32_t sv[64], dpv[64];
         tmem_ld32(s_addr, sv);
@@ -1203,20 +1225,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------- host side
 
 
-template <int D, bool TOK, bool WIN>
+template <int D, bool TOK, bool WIN, bool X>
 static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   using C = KvCfg<D>;
   CUtensorMap tq, tk, tv, tdo;
   if (!tmap_rows(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs, 64) ||
       !tmap_rows(&tdo, p.dout, p.T, p.Hq, D, p.o_rs, p.o_hs, 64) ||
-      !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
-      !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
+      !tmap_rows(&tk, p.k, X ? p.Tk : p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
+      !tmap_rows(&tv, p.v, X ? p.Tk : p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D, TOK, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel<D, TOK, WIN, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D, TOK, WIN>);
+  e = cudaFuncGetAttributes(&fa, dkdv_tc_kernel<D, TOK, WIN, X>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -1224,23 +1246,23 @@ static cudaError_t launch_dkdv_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dkdv_tc_kernel<D, TOK, WIN>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dkdv_tc_kernel<D, TOK, WIN, X>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
-template <int D, bool TOK, bool WIN>
+template <int D, bool TOK, bool WIN, bool X>
 static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   using C = QCfg<D>;
   CUtensorMap tq, tk, tv, tdo;
   if (!tmap_rows(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs, 128) ||
       !tmap_rows(&tdo, p.dout, p.T, p.Hq, D, p.o_rs, p.o_hs, 128) ||
-      !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 64) ||
-      !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 64))
+      !tmap_rows(&tk, p.k, X ? p.Tk : p.T, p.Hkv, D, p.k_rs, p.k_hs, 64) ||
+      !tmap_rows(&tv, p.v, X ? p.Tk : p.T, p.Hkv, D, p.v_rs, p.v_hs, 64))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D, TOK, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(dq_tc_kernel<D, TOK, WIN, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D, TOK, WIN>);
+  e = cudaFuncGetAttributes(&fa, dq_tc_kernel<D, TOK, WIN, X>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -1248,24 +1270,30 @@ static cudaError_t launch_dq_d(const BwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(dq_tc_kernel<D, TOK, WIN>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
+  return launch_pdl(dq_tc_kernel<D, TOK, WIN, X>, dim3(grid), dim3(kBwdThreads), C::SMEM, st, tq, tk, tv, tdo, p);
 }
 
 // tok: the maps hold token records.  The two forms are compiled separately so that the
 // segment-only kernels keep their own code: the token branch in the softmax item loop
 // measured 15% slower on segment records.
 cudaError_t launch_bwd_dkdv_tc(const BwdParams& p, int d, int cap, bool tok, cudaStream_t st) {
-  if (p.window >= 0)  // window calls plan no token records
-    return d == 64 ? launch_dkdv_d<64, false, true>(p, cap, st) : launch_dkdv_d<128, false, true>(p, cap, st);
-  if (tok) return d == 64 ? launch_dkdv_d<64, true, false>(p, cap, st) : launch_dkdv_d<128, true, false>(p, cap, st);
-  return d == 64 ? launch_dkdv_d<64, false, false>(p, cap, st) : launch_dkdv_d<128, false, false>(p, cap, st);
+  if (p.cu_k)  // cross and window calls plan no token records
+    return d == 64 ? launch_dkdv_d<64, false, false, true>(p, cap, st) : launch_dkdv_d<128, false, false, true>(p, cap, st);
+  if (p.window >= 0)
+    return d == 64 ? launch_dkdv_d<64, false, true, false>(p, cap, st) : launch_dkdv_d<128, false, true, false>(p, cap, st);
+  if (tok)
+    return d == 64 ? launch_dkdv_d<64, true, false, false>(p, cap, st) : launch_dkdv_d<128, true, false, false>(p, cap, st);
+  return d == 64 ? launch_dkdv_d<64, false, false, false>(p, cap, st) : launch_dkdv_d<128, false, false, false>(p, cap, st);
 }
 
 cudaError_t launch_bwd_dq_tc(const BwdParams& p, int d, int cap, bool tok, cudaStream_t st) {
+  if (p.cu_k)
+    return d == 64 ? launch_dq_d<64, false, false, true>(p, cap, st) : launch_dq_d<128, false, false, true>(p, cap, st);
   if (p.window >= 0)
-    return d == 64 ? launch_dq_d<64, false, true>(p, cap, st) : launch_dq_d<128, false, true>(p, cap, st);
-  if (tok) return d == 64 ? launch_dq_d<64, true, false>(p, cap, st) : launch_dq_d<128, true, false>(p, cap, st);
-  return d == 64 ? launch_dq_d<64, false, false>(p, cap, st) : launch_dq_d<128, false, false>(p, cap, st);
+    return d == 64 ? launch_dq_d<64, false, true, false>(p, cap, st) : launch_dq_d<128, false, true, false>(p, cap, st);
+  if (tok)
+    return d == 64 ? launch_dq_d<64, true, false, false>(p, cap, st) : launch_dq_d<128, true, false, false>(p, cap, st);
+  return d == 64 ? launch_dq_d<64, false, false, false>(p, cap, st) : launch_dq_d<128, false, false, false>(p, cap, st);
 }
 
 int bwd_tc_token_short() { return kBwdTokenShort; }

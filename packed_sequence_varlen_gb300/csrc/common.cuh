@@ -54,6 +54,7 @@ struct PlanArgs {
   int32_t* tok_counter;  // may be null: the token kernel's work counter; zeroed here
   int window = -1;       // causal local window w >= 0 (query i sees keys i-w..i), -1 = none;
                          // window maps have no token records
+  const int32_t* cu_k = nullptr;  // cross-attention: the K/V boundaries (cu is Q's); null = cu
 };
 
 __device__ __forceinline__ void set_status(WsHeader* h, int code) {

@@ -60,7 +60,7 @@ struct TcCfg {
                        B_PF = B_SF + 2, B_OF = B_PF + 2, B_DR = B_OF + 2, B_IF = B_DR + 1,
                        B_IE = B_IF + 2, NBAR = B_IE + 2;
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;          // two Item slots
-  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 48;
+  static constexpr int MISC_OFF = QUEUE_OFF + 2 * 64;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;    // + slack to align the base to 1024
   static constexpr int OCOLS = D;                      // TMEM columns of one O accumulator
 };
@@ -70,9 +70,11 @@ struct Item {
   int t1;
   int valid;
   int kb;  // local window: the item's first key tile (its key tiles are kb .. kb + nb - 1)
+  int s0k, lk, off;  // cross-attention: the keys' first row and count, the causal offset lk - l
 };
+static_assert(sizeof(Item) <= 64, "queue slots are 64 bytes");
 
-template <bool WIN>
+template <bool WIN, bool X>
 __device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
   const TileItem it = p.items[idx];
   Item r;
@@ -85,6 +87,12 @@ __device__ __forceinline__ Item decode(const FwdParams& p, int idx) {
   r.t1 = r.m * kTcBM + 128 < r.l ? 1 : 0;
   r.nb0 = (p.causal && r.t1) ? r.nb - 1 : r.nb;
   if (WIN) r.kb = max(0, r.m * kTcBM - p.window) / kTcBN;
+  if (X) {  // keys from cu_k; q tile 0 may share its diagonal key tile with tile 1
+    r.s0k = p.cu_k[it.seg];
+    r.lk = p.cu_k[it.seg + 1] - r.s0k;
+    r.off = p.causal ? r.lk - r.l : 0;
+    if (p.causal && r.t1) r.nb0 = (min(r.lk, r.m * kTcBM + 128 + r.off) + kTcBN - 1) / kTcBN;
+  }
   return r;
 }
 
@@ -160,7 +168,10 @@ __device__ __forceinline__ float row_exp(uint32_t* v, float sl2, float mu) {
 // the window of its first row, and tiles that cross a row's window edge are masked on both
 // sides; a row may see nothing in its first tiles (its running max stays -inf and the first
 // visible tile takes over with a zero-weight rescale).
-template <int D, bool WIN>
+// X: cross-attention (p.cu_k): keys from their own boundaries, the causal bound aligned
+// bottom-right (key j visible to query i when j <= i + lk - lq), so the masked key tiles are
+// the one or two that cross a q tile's diagonal band.
+template <int D, bool WIN, bool X>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -174,7 +185,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   Item* queue = reinterpret_cast<Item*>(sm + C::QUEUE_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
-  auto dec = [&](int idx) { return decode<WIN>(p, idx); };
+  auto dec = [&](int idx) { return decode<WIN, X>(p, idx); };
 
   griddep_begin();  // the tile map and status come from the planning launch just before
   if (p.hdr->status != VA_OK) return;
@@ -254,7 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_expect_tx_w(bar(C::B_KVF + s), C::TILE);
             for (int pn = 0; pn < D / 64; ++pn)
               tma_load_3d_w(base + C::KV_OFF + s * C::TILE + pn * C::PANEL, kv ? &tv : &tk,
-                          bar(C::B_KVF + s), pn * 64, I.hk, I.s0 + (WIN ? I.kb + n : n) * kTcBN);
+                          bar(C::B_KVF + s), pn * 64, I.hk, (X ? I.s0k : I.s0) + (WIN ? I.kb + n : n) * kTcBN);
             ++kv_it;
           }
         }
@@ -415,8 +426,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_after_sync();
         // The causal mask touches only the last key tile of each q tile (its diagonal
         // tile); non-causal masks only key columns past the segment end.
-        const bool need_mask = p.causal ? (n == nbt - 1) : (n * kTcBN + kTcBN > I.l);
-        const int lim = p.causal ? qrow - (WIN ? I.kb + n : n) * kTcBN : I.l - 1 - n * kTcBN;  // mask j > lim
+        bool need_mask = p.causal ? (n == nbt - 1) : (n * kTcBN + kTcBN > I.l);
+        int lim = p.causal ? qrow - (WIN ? I.kb + n : n) * kTcBN : I.l - 1 - n * kTcBN;  // mask j > lim
+        if constexpr (X) {  // bottom-right alignment: the diagonal band may span two key tiles
+          need_mask = p.causal ? (n * kTcBN + kTcBN - 1 > I.m * kTcBM + t * 128 + I.off) : (n * kTcBN + kTcBN > I.lk);
+          lim = p.causal ? qrow + I.off - n * kTcBN : I.lk - 1 - n * kTcBN;
+        }
         // One TMEM round trip per tile: the row into registers, its max, then
         // p = exp2(s * sl2 - m_ref) packed in place and stored over the first half of S_t.
         // The reference max m_ref is raised only when the row max grew by more than 2^8
@@ -507,19 +522,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool X>
 static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
   using C = TcCfg<D>;
   CUtensorMap tq, tk, tv;
   if (!tmap_rows(&tq, p.q, p.T, p.Hq, D, p.q_rs, p.q_hs, 128) ||
-      !tmap_rows(&tk, p.k, p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
-      !tmap_rows(&tv, p.v, p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
+      !tmap_rows(&tk, p.k, X ? p.Tk : p.T, p.Hkv, D, p.k_rs, p.k_hs, 128) ||
+      !tmap_rows(&tv, p.v, X ? p.Tk : p.T, p.Hkv, D, p.v_rs, p.v_hs, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, WIN, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // the in-kernel register split assumes the full launch budget; refuse rather than wait
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, WIN>);
+  e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, WIN, X>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
@@ -527,12 +542,13 @@ static cudaError_t launch_d(const FwdParams& p, int cap, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = std::min(cap, std::max(sms, 1));
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(fwd_tc_kernel<D, WIN>, dim3(grid), dim3(kTcThreads), C::SMEM, st, tq, tk, tv, p);
+  return launch_pdl(fwd_tc_kernel<D, WIN, X>, dim3(grid), dim3(kTcThreads), C::SMEM, st, tq, tk, tv, p);
 }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, int cap, cudaStream_t st) {
-  if (p.window >= 0) return d == 64 ? launch_d<64, true>(p, cap, st) : launch_d<128, true>(p, cap, st);
-  return d == 64 ? launch_d<64, false>(p, cap, st) : launch_d<128, false>(p, cap, st);
+  if (p.cu_k) return d == 64 ? launch_d<64, false, true>(p, cap, st) : launch_d<128, false, true>(p, cap, st);
+  if (p.window >= 0) return d == 64 ? launch_d<64, true, false>(p, cap, st) : launch_d<128, true, false>(p, cap, st);
+  return d == 64 ? launch_d<64, false, false>(p, cap, st) : launch_d<128, false, false>(p, cap, st);
 }
 
 void fwd_tc_tiles(int* BM, int* BN) {

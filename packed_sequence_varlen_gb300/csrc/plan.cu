@@ -29,13 +29,15 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_validate_plan(const PlanArgs* maps, int nmaps, int T, int max_seqlen,
+cudaError_t launch_validate_plan(const PlanArgs* maps, int nmaps, int T, int max_seqlen, int Tk, int max_seqlen_k,
                                  cudaStream_t st) {
   PlanPair pp{};
   for (int i = 0; i < nmaps && i < 2; ++i) pp.map[i] = maps[i];
   pp.nmaps = nmaps;
   pp.T = T;
   pp.max_seqlen = max_seqlen;
+  pp.Tk = Tk;
+  pp.max_seqlen_k = max_seqlen_k;
   return launch_pdl(validate_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp);
 }
 

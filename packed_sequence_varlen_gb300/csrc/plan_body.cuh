@@ -59,10 +59,21 @@ __device__ __forceinline__ bool token_mode(const PlanArgs& a) { return a.causal 
 // start at floor(max(0, m*BM - w) / BN); a kv block n's q blocks stop after
 // floor((n*BN + BN - 1 + w) / BM) ("Packing与 FlashAttention Varlen", section 5: the local
 // window narrows n_block_min/max).
-template <bool KV, bool CAUSAL, bool TOKENS, bool WIN = false>
+// X: cross-attention (a.cu_k): a segment has lq queries and lk keys, the causal bound is
+// aligned bottom-right (key j visible to query i when j <= i + lk - lq): q block m has
+// ceil(min(lk, (m+1)*BM + lk - lq) / BN) key blocks, kv block n its q blocks from
+// floor(max(0, n*BN - (lk - lq)) / BM) ("Packing与 FlashAttention Varlen", section 5).
+template <bool KV, bool CAUSAL, bool TOKENS, bool WIN = false, bool X = false>
 struct MapKind {
-  static constexpr bool kv = KV, causal = CAUSAL, tokens = TOKENS, win = WIN;
+  static constexpr bool kv = KV, causal = CAUSAL, tokens = TOKENS, win = WIN, x = X;
 };
+
+// Cross-attention record count of q block m (q-block maps) or kv block n (kv-block maps).
+template <class M>
+__device__ __forceinline__ int x_count(const PlanArgs& a, int lq, int lk, int blk) {
+  if (!M::kv) return M::causal ? ceil_p2(min(lk, (blk + 1) * a.BM + lk - lq), a.BN) : ceil_p2(lk, a.BN);
+  return ceil_p2(lq, a.BM) - (M::causal ? div_p2(max(0, blk * a.BN - (lk - lq)), a.BM) : 0);
+}
 
 // Windowed record count of q block m (q-block maps) or kv block n (kv-block maps).
 template <class M>
@@ -75,10 +86,15 @@ __device__ __forceinline__ int win_count(const PlanArgs& a, int l, int blk) {
   return min(Mq, div_p2(blk * a.BN + a.BN - 1 + a.window, a.BM) + 1) - div_p2(blk * a.BN, a.BM);
 }
 
-// Blocks of a segment of length l and its total tile count (none for token-tiled segments).
+// Blocks of a segment of length l (lk keys under cross-attention) and its total tile count
+// (none for token-tiled segments).
 template <class M>
-__device__ __forceinline__ void seg_cost(const PlanArgs& a, int l, int& nblk, int& cost) {
-  if (M::tokens && l <= a.short_len) {
+__device__ __forceinline__ void seg_cost(const PlanArgs& a, int l, int lk, int& nblk, int& cost) {
+  if (M::x) {
+    nblk = M::kv ? ceil_p2(lk, a.BN) : ceil_p2(l, a.BM);
+    cost = 0;
+    for (int b = 0; b < nblk; ++b) cost += x_count<M>(a, l, lk, b);
+  } else if (M::tokens && l <= a.short_len) {
     nblk = 0;
     cost = 0;
   } else if (M::win) {  // no closed form worth keeping: sum the blocks (one thread per segment)
@@ -98,8 +114,11 @@ __device__ __forceinline__ void seg_cost(const PlanArgs& a, int l, int& nblk, in
 
 // The j-th record of one (segment, head): most tiles first.
 template <class M>
-__device__ __forceinline__ void seg_record(const PlanArgs& a, int l, int nblk, int j, int& blk, int& count) {
-  if (M::win) {  // q blocks last-first, kv blocks first-first: the no-window orders
+__device__ __forceinline__ void seg_record(const PlanArgs& a, int l, int lk, int nblk, int j, int& blk, int& count) {
+  if (M::x) {  // the no-cross orders: q blocks last-first (causal), kv blocks first-first
+    blk = (M::kv || !M::causal) ? j : nblk - 1 - j;
+    count = x_count<M>(a, l, lk, blk);
+  } else if (M::win) {  // q blocks last-first, kv blocks first-first: the no-window orders
     blk = M::kv ? j : nblk - 1 - j;
     count = win_count<M>(a, l, blk);
   } else if (!M::kv) {
@@ -269,11 +288,12 @@ template <class M>
 __device__ __forceinline__ void write_group(const PlanArgs& a, const int* cu, const int* seg_off, int g0, int s,
                                             int k) {
   const int lane = threadIdx.x & 31, b = g0 + lane;
-  int l = 0, nblk = 0, n = 0, off = 0;
+  int l = 0, lk = 0, nblk = 0, n = 0, off = 0;
   if (b < a.B) {
     int cost;
     l = cu[b + 1] - cu[b];
-    seg_cost<M>(a, l, nblk, cost);
+    lk = M::x ? a.cu_k[b + 1] - a.cu_k[b] : l;
+    seg_cost<M>(a, l, lk, nblk, cost);
     n = nblk * a.heads;
     if (n > 0) off = seg_off[b];
   }
@@ -291,12 +311,13 @@ __device__ __forceinline__ void write_group(const PlanArgs& a, const int* cu, co
     for (int step = 16; step > 0; step >>= 1)
       if (__shfl_sync(0xffffffffu, incl, sgi + step - 1) <= r) sgi += step;
     const int sl = __shfl_sync(0xffffffffu, l, sgi), snb = __shfl_sync(0xffffffffu, nblk, sgi);
+    const int slk = __shfl_sync(0xffffffffu, lk, sgi);
     const int soff = __shfl_sync(0xffffffffu, off, sgi);
     const int sbeg = __shfl_sync(0xffffffffu, incl - n, sgi);
     if (r < total) {
       const int rr = r - sbeg, h = rr / snb, j = rr - h * snb;
       TileItem t;
-      seg_record<M>(a, sl, snb, j, t.blk, t.count);
+      seg_record<M>(a, sl, slk, snb, j, t.blk, t.count);
       t.seg = g0 + sgi;
       t.head = h;
       if (soff + rr >= 0 && soff + rr < a.capacity) a.out[soff + rr] = t;  // boundaries that break
@@ -317,7 +338,7 @@ __device__ __forceinline__ void seg_class(const PlanArgs& a, const int* cu, int 
   if (b < a.B) {
     int cost;
     l = cu[b + 1] - cu[b];
-    seg_cost<M>(a, l, nblk, cost);
+    seg_cost<M>(a, l, M::x ? a.cu_k[b + 1] - a.cu_k[b] : l, nblk, cost);
     if (nblk > 0) {
       c = cost_class(cost);
       n = nblk * a.heads;
@@ -452,6 +473,16 @@ __device__ __forceinline__ void plan_body_m(const PlanArgs& a, PlanSmem& sh, con
 }
 
 __device__ __forceinline__ void plan_body(const PlanArgs& a, PlanSmem& sh, const int* cu, int* seg_off) {
+  if (a.cu_k) {
+    if (a.kind == 1) {
+      if (a.causal) plan_body_m<MapKind<true, true, false, false, true>>(a, sh, cu, seg_off);
+      else plan_body_m<MapKind<true, false, false, false, true>>(a, sh, cu, seg_off);
+    } else {
+      if (a.causal) plan_body_m<MapKind<false, true, false, false, true>>(a, sh, cu, seg_off);
+      else plan_body_m<MapKind<false, false, false, false, true>>(a, sh, cu, seg_off);
+    }
+    return;
+  }
   if (a.causal && a.window >= 0) {
     if (a.kind == 1) plan_body_m<MapKind<true, true, false, true>>(a, sh, cu, seg_off);
     else plan_body_m<MapKind<false, true, false, true>>(a, sh, cu, seg_off);
@@ -473,6 +504,7 @@ struct PlanPair {
   PlanArgs map[2];
   int nmaps;
   int T, max_seqlen;
+  int Tk = 0, max_seqlen_k = 0;  // cross-attention (map[0].cu_k set): the K/V stream
 };
 
 // Copies cu[0..B] into shared memory when it fits; returns the array to read.
@@ -493,6 +525,14 @@ __device__ __forceinline__ void validate_plan_body(const PlanPair& pp, PlanSmem&
     if (y <= x || y - x > pp.max_seqlen) bad = 1;
   }
   if (threadIdx.x == 0 && (cu[0] != 0 || cu[a0.B] != pp.T)) bad = 1;
+  if (a0.cu_k) {  // the K/V boundaries obey the same contract; causal needs lq <= lk
+    const int32_t* ck = a0.cu_k;
+    for (int b = threadIdx.x; b < a0.B; b += blockDim.x) {
+      const int x = ck[b], y = ck[b + 1];
+      if (y <= x || y - x > pp.max_seqlen_k || (a0.causal && cu[b + 1] - cu[b] > y - x)) bad = 1;
+    }
+    if (threadIdx.x == 0 && (ck[0] != 0 || ck[a0.B] != pp.Tk)) bad = 1;
+  }
   bad = __syncthreads_or(bad);
   if (bad) {
     if (threadIdx.x == 0) {

