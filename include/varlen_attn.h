@@ -119,6 +119,8 @@ va_status varlen_pack_best_fit_decreasing(const int32_t* lengths, int32_t n, int
  *   status_dev[1]         device out: 0, or VA_ERR_BAD_SEQLENS for a length <= 0
  *                         or pad_to < sum
  *   T_capacity            elements available in position_ids_dev/segment_ids_dev
+ * One kernel launch when T_capacity <= 16384 and n <= 2046 (the scan's block also
+ * writes positions and segment ids), else two.
  * Errors: VA_ERR_INVALID_ARG, VA_ERR_CUDA.  Asynchronous. */
 va_status varlen_build_metadata(const int32_t* lengths_dev, int32_t n, int32_t pad_to,
                                 int32_t T_capacity, int32_t* cu_seqlens_dev,

@@ -10,8 +10,9 @@
 namespace va {
 
 // kernels (other translation units)
-cudaError_t launch_metadata_scan(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*,
-                                 cudaStream_t);
+cudaError_t launch_metadata_scan(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*,
+                                 int32_t*, cudaStream_t);
+bool metadata_inline_fill(int n, int T_capacity);
 cudaError_t launch_metadata_fill(const int32_t*, int, int, int32_t*, int32_t*, const int32_t*,
                                  cudaStream_t);
 cudaError_t launch_validate(const int32_t*, int, int, int, int32_t*, int, cudaStream_t);
@@ -231,9 +232,11 @@ va_status varlen_build_metadata(const int32_t* lengths_dev, int32_t n, int32_t p
     return fail(VA_ERR_INVALID_ARG, "build_metadata: null pointer or negative size");
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch(K_META_SCAN, cs, [&] {
-    return launch_metadata_scan(lengths_dev, n, pad_to, T_capacity, cu_dev, max_dev, status_dev, cs);
+    return launch_metadata_scan(lengths_dev, n, pad_to, T_capacity, cu_dev, max_dev, status_dev, pos_dev, seg_dev,
+                                cs);
   });
-  if (e == cudaSuccess && T_capacity > 0)
+  // short streams get their positions and segment ids from the scan's block
+  if (e == cudaSuccess && T_capacity > 0 && !metadata_inline_fill(n, T_capacity))
     e = launch(K_META_FILL, cs, [&] {
       return launch_metadata_fill(cu_dev, n, T_capacity, pos_dev, seg_dev, status_dev, cs);
     });

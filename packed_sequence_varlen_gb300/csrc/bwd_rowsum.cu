@@ -1,8 +1,8 @@
 // Backward preparation, one launch: D_i = dO_i . O_i for every (token, q head), fp32
 // [Hq, T] -- the row term of dS_ij = P_ij (dP_ij - D_i) in the analytic gradient of the
 // forward ("Packing与 FlashAttention Varlen", section 5 names the training branch) --
-// while one extra CTA validates cu_seqlens and builds the dK/dV and dQ tile maps
-// (plan_body.cuh).  D does not depend on the boundaries, so the two run side by side.
+// while two extra CTAs validate cu_seqlens and build the dK/dV and the dQ tile map, one map
+// each (plan_body.cuh).  D does not depend on the boundaries, so all of them run side by side.
 // HBM-bound: 16-byte streaming loads, several rows in flight per warp.
 #include <algorithm>
 
@@ -79,21 +79,23 @@ __device__ __forceinline__ void rowsum_body(const BwdParams& p, int blk, int nbl
   }
 }
 
-// Two CTAs of 512 threads per SM: one wave holds the planning CTA and the D blocks.
+// Two CTAs of 512 threads per SM: one wave holds the planning CTAs and the D blocks.
 constexpr int kPrepThreads = 512;
 constexpr int kPrepPerSm = 2;
 
-// Block 0 validates and plans (the status word it writes gates the attention kernels that
-// follow, not this launch); blocks 1.. compute D.
+// The first nplan blocks validate and plan (the status word gates the attention kernels
+// that follow, not this launch): with nplan = 2 block i builds map i, so the two maps are
+// built side by side; with nplan = 1 block 0 builds both.  The other blocks compute D.
 template <int D, int VB>
-__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) bwd_prep_kernel(const BwdParams p, const PlanPair pp) {
+__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm)
+    bwd_prep_kernel(const BwdParams p, const PlanPair pp, int nplan) {
   __shared__ PlanSmem sh;
   griddep_begin();  // O comes from the forward, and the workspace may be the forward's
-  if (blockIdx.x == 0) {
-    validate_plan_body(pp, sh);
+  if (static_cast<int>(blockIdx.x) < nplan) {
+    validate_plan_body(pp, sh, nplan == 1 ? -1 : static_cast<int>(blockIdx.x));
     return;
   }
-  rowsum_body<D, VB>(p, blockIdx.x - 1, gridDim.x - 1);
+  rowsum_body<D, VB>(p, blockIdx.x - nplan, gridDim.x - nplan);
 }
 
 cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps, int T, int max_seqlen, int Tk,
@@ -108,19 +110,22 @@ cudaError_t launch_bwd_prep(const BwdParams& p, const PlanArgs* maps, int nmaps,
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one planning block per map while the per-segment offsets fit in shared memory (beyond
+  // that the maps share one global array of them, and one block builds both in turn)
+  const int nplan = nmaps == 2 && maps[0].B + 1 <= kSmemSegs ? 2 : 1;
   const int64_t rows = static_cast<int64_t>(p.T) * p.Hq;
   const int rpb = (kPrepThreads / 32) * (32 / (d / 8)) * 4;   // rows per block per pass (16-byte loads)
-  const int rb = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(std::max(sms, 1) * kPrepPerSm - 1,
+  const int rb = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(std::max(sms, 1) * kPrepPerSm - nplan,
                                                                         (rows + rpb - 1) / rpb)));
   // 32-byte loads when every row start of O and dO is 32-byte aligned
   const bool a32 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0 && (reinterpret_cast<uintptr_t>(p.dout) & 31) == 0 &&
                    p.o_rs % 16 == 0 && p.o_hs % 16 == 0;
-  const dim3 grid(rb + 1), block(kPrepThreads);
+  const dim3 grid(rb + nplan), block(kPrepThreads);
   if (d == 64)
-    return a32 ? launch_pdl(bwd_prep_kernel<64, 32>, grid, block, 0, st, p, pp)
-               : launch_pdl(bwd_prep_kernel<64, 16>, grid, block, 0, st, p, pp);
-  return a32 ? launch_pdl(bwd_prep_kernel<128, 32>, grid, block, 0, st, p, pp)
-             : launch_pdl(bwd_prep_kernel<128, 16>, grid, block, 0, st, p, pp);
+    return a32 ? launch_pdl(bwd_prep_kernel<64, 32>, grid, block, 0, st, p, pp, nplan)
+               : launch_pdl(bwd_prep_kernel<64, 16>, grid, block, 0, st, p, pp, nplan);
+  return a32 ? launch_pdl(bwd_prep_kernel<128, 32>, grid, block, 0, st, p, pp, nplan)
+             : launch_pdl(bwd_prep_kernel<128, 16>, grid, block, 0, st, p, pp, nplan);
 }
 
 

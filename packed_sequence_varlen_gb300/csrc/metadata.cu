@@ -11,6 +11,26 @@ namespace va {
 
 constexpr int kScanThreads = 1024;
 
+// A stream of at most kInlineTokens tokens cut into at most kInlineSegs lengths gets its
+// positions and segment ids from the scan's own block, from a shared-memory copy of the
+// boundaries: one launch instead of two, and no binary search through global memory.
+constexpr int kInlineTokens = 16384;
+constexpr int kInlineSegs = 2046;
+
+bool metadata_inline_fill(int n, int T_capacity) {
+  return T_capacity > 0 && T_capacity <= kInlineTokens && n <= kInlineSegs;
+}
+
+// Segment of token t: b with cu[b] <= t < cu[b + 1], over cu[0..nseg].
+__device__ __forceinline__ int find_segment(const int32_t* cu, int nseg, int t) {
+  int lo = 0, hi = nseg;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 // Block-wide inclusive scan of one int per thread (1024 threads).
 __device__ __forceinline__ int block_inclusive_scan(int x, int* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -36,19 +56,24 @@ __device__ __forceinline__ int block_inclusive_scan(int x, int* warp_sums) {
   return x;
 }
 
-// One block: exclusive scan of the lengths into cu[0..n], tail pad into cu[n+1].
+// One block: exclusive scan of the lengths into cu[0..n], tail pad into cu[n+1]; with
+// inline_fill (metadata_inline_fill) also position_ids and segment_ids, as the fill kernel
+// would write them.
 __global__ void __launch_bounds__(kScanThreads)
     metadata_scan_kernel(const int32_t* __restrict__ lengths, int n, int pad_to,
                          int T_capacity, int32_t* __restrict__ cu, int32_t* __restrict__ max_out,
-                         int32_t* __restrict__ status) {
+                         int32_t* __restrict__ status, int inline_fill, int32_t* __restrict__ pos,
+                         int32_t* __restrict__ seg) {
   __shared__ int warp_sums[32];
   __shared__ int carry, mx, bad;
+  __shared__ int s_cu[kInlineSegs + 2];
   griddep_begin();  // the lengths may come from the kernel just before
   if (threadIdx.x == 0) {
     carry = 0;
     mx = 0;
     bad = 0;
     cu[0] = 0;
+    s_cu[0] = 0;
   }
   __syncthreads();
   for (int base = 0; base < n; base += kScanThreads) {
@@ -57,7 +82,10 @@ __global__ void __launch_bounds__(kScanThreads)
     if (i < n && L <= 0) atomicOr(&bad, 1);
     if (i < n) atomicMax(&mx, L);
     const int incl = block_inclusive_scan(L, warp_sums);
-    if (i < n) cu[i + 1] = carry + incl;
+    if (i < n) {
+      cu[i + 1] = carry + incl;
+      if (inline_fill) s_cu[i + 1] = carry + incl;
+    }
     __syncthreads();
     if (threadIdx.x == kScanThreads - 1) carry += incl;
     __syncthreads();
@@ -73,8 +101,19 @@ __global__ void __launch_bounds__(kScanThreads)
     }
     if (last > T_capacity) bad = 1;
     cu[n + 1] = last;
+    if (inline_fill) s_cu[n + 1] = last;
     *max_out = mx;
     *status = bad ? VA_ERR_BAD_SEQLENS : VA_OK;
+  }
+  if (!inline_fill) return;
+  __syncthreads();
+  if (bad) return;
+  const int T = s_cu[n + 1];
+  const int nseg = (s_cu[n + 1] > s_cu[n]) ? n + 1 : n;
+  for (int t = threadIdx.x; t < T && t < T_capacity; t += kScanThreads) {
+    const int b = find_segment(s_cu, nseg, t);
+    seg[t] = b;
+    pos[t] = t - s_cu[b];
   }
 }
 
@@ -88,13 +127,9 @@ __global__ void metadata_fill_kernel(const int32_t* __restrict__ cu, int n, int 
   const int nseg = (cu[n + 1] > cu[n]) ? n + 1 : n;
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T && t < T_capacity;
        t += gridDim.x * blockDim.x) {
-    int lo = 0, hi = nseg;  // find b with cu[b] <= t < cu[b+1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (cu[mid] <= t) lo = mid; else hi = mid;
-    }
-    seg[t] = lo;
-    pos[t] = t - cu[lo];
+    const int b = find_segment(cu, nseg, t);
+    seg[t] = b;
+    pos[t] = t - cu[b];
   }
 }
 
@@ -117,9 +152,11 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 cudaError_t launch_metadata_scan(const int32_t* lengths, int n, int pad_to, int T_capacity,
-                                 int32_t* cu, int32_t* max_out, int32_t* status, cudaStream_t st) {
+                                 int32_t* cu, int32_t* max_out, int32_t* status, int32_t* pos, int32_t* seg,
+                                 cudaStream_t st) {
+  const int inl = metadata_inline_fill(n, T_capacity) ? 1 : 0;
   return launch_pdl(metadata_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, lengths, n, pad_to, T_capacity, cu,
-                    max_out, status);
+                    max_out, status, inl, pos, seg);
 }
 
 cudaError_t launch_metadata_fill(const int32_t* cu, int n, int T_capacity, int32_t* pos,

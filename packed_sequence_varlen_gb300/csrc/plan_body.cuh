@@ -515,8 +515,12 @@ __device__ __forceinline__ const int* stage_cu(const int32_t* cu, int B, PlanSme
   return sh.cu;
 }
 
-// Validates cu_seqlens (writing the status word) and builds every map of pp.
-__device__ __forceinline__ void validate_plan_body(const PlanPair& pp, PlanSmem& sh) {
+// Validates cu_seqlens and builds the maps of pp: every map (only < 0), writing the status
+// word, or map `only` alone (the CTA that builds map 0 writes the status word).  Two CTAs
+// that each build one map share nothing but the boundaries they read.  Neither can overflow:
+// the library sizes a map at (rows / tile + B) * heads records, which bounds the records of
+// any boundaries that pass the check, so the second CTA's map never writes the status word.
+__device__ __forceinline__ void validate_plan_body(const PlanPair& pp, PlanSmem& sh, int only = -1) {
   const PlanArgs& a0 = pp.map[0];
   const int* cu = stage_cu(a0.cu, a0.B, sh);  // every map is built from the same boundaries
   int bad = 0;
@@ -534,18 +538,19 @@ __device__ __forceinline__ void validate_plan_body(const PlanPair& pp, PlanSmem&
     if (threadIdx.x == 0 && (ck[0] != 0 || ck[a0.B] != pp.Tk)) bad = 1;
   }
   bad = __syncthreads_or(bad);
+  const int i0 = only < 0 ? 0 : only, i1 = only < 0 ? pp.nmaps : only + 1;
   if (bad) {
     if (threadIdx.x == 0) {
-      *a0.status = VA_ERR_BAD_SEQLENS;
-      for (int i = 0; i < pp.nmaps; ++i) {
+      if (i0 == 0) *a0.status = VA_ERR_BAD_SEQLENS;
+      for (int i = i0; i < i1; ++i) {
         *pp.map[i].n_items = 0;
         if (pp.map[i].n_tok) *pp.map[i].n_tok = 0;
       }
     }
     return;
   }
-  if (threadIdx.x == 0) *a0.status = VA_OK;
-  for (int i = 0; i < pp.nmaps; ++i)
+  if (threadIdx.x == 0 && i0 == 0) *a0.status = VA_OK;
+  for (int i = i0; i < i1; ++i)
     plan_body(pp.map[i], sh, cu, a0.B + 1 > kSmemSegs ? pp.map[i].seg_off : sh.off);
 }
 

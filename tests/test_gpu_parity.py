@@ -283,6 +283,32 @@ def test_short_segments_among_long_ones(va):
     wl.assert_close_grads(tuple(x[short] for x in gr), tuple(x[short] for x in rg))
 
 
+def test_more_segments_than_shared_offsets(va):
+    """4400 segments: more than the planner keeps in shared memory (4095 boundaries), so the
+    per-segment record offsets go to the workspace and one planning block builds both backward
+    maps in turn.  Every tenth segment is 65..200 tokens (segment records), the rest 1..40
+    (token tiles under causality); maps bit-exact, causal results as the oracle gives them."""
+    rng = np.random.default_rng(11)
+    lengths = [int(x) for x in rng.integers(1, 41, 4400)]
+    for i in range(0, 4400, 10):
+        lengths[i] = int(rng.integers(65, 201))
+    cu, _, _, mx = op.build_metadata(lengths)
+    T = int(cu[-1])
+    cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    for causal in (True, False):
+        for kind in (0, 1, 2):
+            tm, n = va.plan(cud, T, 2, 1, 64, mx, kind, causal)
+            ref = oracle_map(va, kind, cu, 2, 1, 64, causal)
+            assert n == len(ref)
+            assert np.array_equal(tm.cpu().numpy(), ref)
+    q, k, v, do = si.tensors(T, 2, 1, 64, seed_offset=41)
+    o, lse, gr = run_gpu(va, q, k, v, do, cud, mx)
+    ro, rl, rg = run_oracle(q, k, v, do, cu)
+    wl.assert_close_outputs(o, lse, ro, rl)
+    wl.assert_close_grads(gr, rg)
+    wl.assert_close_grads_chunked(gr, rg)
+
+
 # ------------------------------------------------------------------ properties
 
 def test_first_query_sees_only_itself(va):
