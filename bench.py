@@ -96,6 +96,8 @@ def batch_packs(rank: int, planners):
     raw = si.raw_lengths(WORKLOAD).tolist()
     planner = host_planner(w, planners)
     packs = [raw] if planner is None else [[raw[i] for i in p] for p in planner(raw, w.capacity)]
+    if w.packs_used:  # e.g. tiny4k is the first row only: the rest of its draws are a partial row
+        packs = packs[:w.packs_used]
     idx = rank_pack_indices(rank, PACKS_PER_STEP, len(packs))
     return [packs[i] for i in idx], idx, w
 
@@ -342,6 +344,13 @@ def run_ours(args, rank, world, local_rank):
                     for k, (t, c) in sorted(per_kernel.items(), key=lambda kv: -kv[1][0])}
     fwd_t = per_kernel.get("fwd", (0.0, 1))[0] + per_kernel.get("fwd_tok", (0.0, 1))[0]
     fwd_tflops = 4 * d * Hq * sum(f["e_doc"] for f in fl) * args.steps / (fwd_t * 1e-3) / 1e12 if fwd_t else None
+    # backward: D and the backward's maps, dK/dV and dQ (10 d Hq FLOPs per in-segment edge)
+    bwd_t = sum(per_kernel.get(k, (0.0, 0))[0] for k in ("bwd_prep", "bwd_dkdv", "bwd_dq"))
+    bwd_tflops = 10 * d * Hq * sum(f["e_doc"] for f in fl) * args.steps / (bwd_t * 1e-3) / 1e12 if bwd_t else None
+    # boundary metadata and the forward's check + map, per pack
+    n_calls = len(fl) * args.steps
+    plan_us = sum(t for k, (t, _) in per_kernel.items() if k.startswith("metadata") or k == "validate_plan")
+    plan_us = plan_us * 1e3 / n_calls if n_calls else None
 
     e2e = run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host) if not args.no_e2e else None
 
@@ -357,7 +366,9 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2 ({T * (2 * Hq + 2 * Hkv) * d * 2 // 2**20} MB per pack)",
                    "parallelism": f"replicas x{world}",
                    "pct_of_bf16_peak_burst": round(100 * value / world / peaks["bf16_tflops"], 2),
-                   "fwd_kernel_tflops": round(fwd_tflops, 2) if fwd_tflops else None},
+                   "fwd_kernel_tflops": round(fwd_tflops, 2) if fwd_tflops else None,
+                   "bwd_kernels_tflops": round(bwd_tflops, 2) if bwd_tflops else None,
+                   "metadata_and_fwd_plan_us_per_pack": round(plan_us, 2) if plan_us else None},
         "e2e": e2e,
         "gpu_launches": int(launches),
         "kernels": kernel_table,

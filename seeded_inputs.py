@@ -46,6 +46,7 @@ class Workload:
     causal: bool = True
     description: str = ""
     fixed_lengths: tuple = field(default_factory=tuple)
+    packs_used: int = 0    # the workload is its first this many packs (0: all of them)
 
 
 WORKLOADS = {
@@ -66,7 +67,8 @@ WORKLOADS = {
     "tiny4k": Workload("tiny4k", 8, 8, 64, 131072, "next_fit", 131072,
                        description="lengths U[1,64], next-fit into 131072, first "
                                    "row (~4000 segments), tail padded, Hq=Hkv=8, "
-                                   "d=64, bf16"),
+                                   "d=64, bf16",
+                       packs_used=1),
 }
 
 

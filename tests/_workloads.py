@@ -26,8 +26,8 @@ def real_packs(name: str):
         groups = op.next_fit(lengths, w.capacity)
     else:
         groups = op.best_fit_decreasing(lengths, w.capacity)
-    if name == "tiny4k":
-        groups = groups[:1]          # the workload is the first 131072-token row
+    if w.packs_used:
+        groups = groups[:w.packs_used]   # e.g. tiny4k: the first 131072-token row
     return [([lengths[i] for i in g], w.pad_to) for g in groups]
 
 
