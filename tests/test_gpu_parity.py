@@ -72,6 +72,24 @@ def test_metadata_bit_exact(va, name):
         assert mx == rmx
 
 
+# Streams of at most 16384 tokens cut into at most 2046 lengths get positions and segment ids
+# from the scan's own block; longer ones from a separate fill launch.  Both sides of each limit.
+@pytest.mark.parametrize("n,length,pad_to", [(2046, 8, 16384), (2047, 8, 16384), (2046, 8, 0),
+                                             (100, 163, 16385), (100, 163, 16384), (1, 16384, 0),
+                                             (0, 1, 16384), (0, 1, 16385)])
+def test_metadata_fill_limits_bit_exact(va, n, length, pad_to):
+    rng = np.random.default_rng(n + length + pad_to)
+    lengths = [int(x) for x in rng.integers(1, 2 * length, n)] if length > 1 else [1] * n
+    if pad_to and sum(lengths) > pad_to:
+        lengths = [max(1, x // 2) for x in lengths]
+    cu, pos, seg, mx = gpu_metadata(va, lengths, pad_to)
+    rcu, rpos, rseg, rmx = op.build_metadata(lengths, pad_to)
+    assert np.array_equal(cu.cpu().numpy(), rcu)
+    assert np.array_equal(pos.cpu().numpy(), rpos)
+    assert np.array_equal(seg.cpu().numpy(), rseg)
+    assert mx == rmx
+
+
 def test_metadata_page_layout_and_errors(va):
     cu, pos, seg, mx = gpu_metadata(va, [5, 3, 4])
     assert cu.cpu().tolist() == [0, 5, 8, 12]
