@@ -52,3 +52,25 @@ def test_single_process_aggregate_and_wraparound():
     import bench
     assert bench.aggregate(5.0, 7.0, 4) == (5.0, 28.0)
     assert bench.rank_pack_indices(2, 16, 40) == [(32 + i) % 40 for i in range(16)]
+
+
+@pytest.mark.parametrize("name", ["sft8k", "gqa16k", "long64k", "tiny4k"])
+def test_bench_packs_are_the_workload_packs(name):
+    """Every pack a rank times is one of the workload's own packs (the ones the parity tests
+    check): tiny4k, for one, is its first next-fit row, not the partial row its leftover
+    draws would form."""
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import bench
+    import _workloads as wl
+    from oracle import packing as op
+    old = bench.WORKLOAD, bench.PACKS_PER_STEP
+    try:
+        bench.WORKLOAD, bench.PACKS_PER_STEP = name, 16
+        own = [list(p) for p, _ in wl.real_packs(name)]
+        for rank in (0, 1):
+            packs, idx, w = bench.batch_packs(rank, (op.next_fit, op.best_fit_decreasing))
+            assert len(packs) == 16 and all(0 <= i < len(own) for i in idx)
+            assert all(list(p) == own[i] for p, i in zip(packs, idx))
+    finally:
+        bench.WORKLOAD, bench.PACKS_PER_STEP = old
