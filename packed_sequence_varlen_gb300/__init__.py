@@ -13,6 +13,7 @@ from __future__ import annotations
 import ctypes
 import math
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -43,13 +44,23 @@ def _ptr(t: torch.Tensor | None):
 
 def _pack(fn, lengths, capacity: int):
     lib = _lib.load()
-    n = len(lengths)
-    arr = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in lengths])
-    order = (ctypes.c_int32 * max(n, 1))()
-    offs = (ctypes.c_int32 * (n + 1))()
+    src = np.asarray(lengths)
+    if src.ndim != 1 or (src.size and src.dtype.kind not in "iu"):
+        raise TypeError("lengths: a flat sequence of integers")
+    if src.size and (src.min() < np.iinfo(np.int32).min or src.max() > np.iinfo(np.int32).max):
+        raise ValueError("lengths: values must fit in int32")
+    n = int(src.size)
+    arr = np.zeros(max(n, 1), dtype=np.int32)
+    arr[:n] = src
+    order = np.empty(max(n, 1), dtype=np.int32)
+    offs = np.zeros(n + 1, dtype=np.int32)
     npk = ctypes.c_int32(0)
-    check(getattr(lib, fn)(arr, n, int(capacity), order, offs, ctypes.byref(npk)))
-    return [[order[j] for j in range(offs[p], offs[p + 1])] for p in range(npk.value)]
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    check(getattr(lib, fn)(arr.ctypes.data_as(i32p), n, int(capacity), order.ctypes.data_as(i32p),
+                           offs.ctypes.data_as(i32p), ctypes.byref(npk)))
+    bounds = offs[:npk.value + 1].tolist()
+    flat = order[:n].tolist()
+    return [flat[bounds[p]:bounds[p + 1]] for p in range(npk.value)]
 
 
 def pack_next_fit(lengths, capacity: int):

@@ -67,6 +67,13 @@ def test_host_planner_random_and_errors(va):
     with pytest.raises(va.VarlenError) as e:
         va.pack_best_fit_decreasing([0, 3], 6)
     assert e.value.status == 1
+    # any flat integer sequence; nothing is converted silently
+    assert va.pack_next_fit(np.array([3, 2, 4], dtype=np.int64), 6) == [[0, 1], [2]]
+    assert va.pack_best_fit_decreasing((3, 2, 4), 6) == op.best_fit_decreasing([3, 2, 4], 6)
+    assert va.pack_next_fit([], 6) == []
+    for bad, err in (([3.5, 2], TypeError), ([[1, 2]], TypeError), ([2 ** 40], ValueError)):
+        with pytest.raises(err):
+            va.pack_next_fit(bad, 6)
 
 
 def test_tile_sizes_and_workspace(va):
