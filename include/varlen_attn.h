@@ -272,21 +272,41 @@ va_status varlen_attn_bwd_window(const void* q_dev, const void* k_dev, const voi
  * allocations, or a serving loop that must not call cudaMalloc because it can
  * synchronise the device).  The pages have no counterpart: this is a deployment
  * convenience.  Same arguments, layouts and results as varlen_attn_fwd, without
- * ws_dev/ws_bytes: the scratch (status header and tile map) lives in a 1 MiB
- * static device array that every GPU loading this library holds until exit.
- *   - Limit: (T/256 rounded down + B) * Hq <= 65520 tile records; larger shapes
- *     return VA_ERR_WORKSPACE with a message.
- *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on that device.
+ * ws_dev/ws_bytes: the scratch (status header, tile map, segment offsets) lives
+ * in a 1 MiB static device array that every GPU loading this library holds
+ * until exit.
+ *   - Limit: the shape fits when varlen_attn_workspace_size(shape, 0) <= 1 MiB,
+ *     that is 256 + align256(16 * (floor(T/256) + B) * Hq) + align256(4 * B)
+ *     <= 1,048,576 bytes (align256 rounds up to a multiple of 256).  Larger
+ *     shapes return VA_ERR_WORKSPACE with a message and launch nothing.
+ *   - Every call looks the array's device address up (cudaGetSymbolAddress,
+ *     with the caller's device current).  The first call on a device may load
+ *     the library's device code there; make it before any stream capture.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (each call rewrites what it reads).  Calls that overlap on the
  *     GPU race on it: serialise them (one stream, or events between streams).
- *   - Allocates nothing.  Device-detected errors (a cu_seqlens that breaks the
- *     contract) leave out/lse unwritten; the status word is not exposed. */
+ *   - Allocates nothing.  A device-detected error (a cu_seqlens that breaks the
+ *     contract, a bounded wait that gave up) leaves out/lse unwritten and is
+ *     visible only through varlen_noalloc_read_status. */
 va_status varlen_attn_fwd_noalloc(const void* q_dev, const void* k_dev, const void* v_dev,
                                   const int32_t* cu_seqlens_dev, const va_shape* shape, float scale,
                                   int32_t causal, void* out_dev, float* lse_dev, va_stream_t stream);
+
+/* The status word of the last varlen_attn_fwd_noalloc call on the current
+ * device: synchronises the stream, then copies the 4-byte word to *status_host
+ * (VA_OK, VA_ERR_BAD_SEQLENS or VA_ERR_TIMEOUT).  Allocates nothing.
+ * Errors: VA_ERR_INVALID_ARG (null pointer), VA_ERR_CUDA. */
+va_status varlen_noalloc_read_status(int32_t* status_host, va_stream_t stream);
+
+/* Test hook of the device-detected failure path; the pages have no counterpart.  Arms the
+ * next forward call made in this process (varlen_attn_fwd and its variants): in that call
+ * every attention CTA publishes its first work item and then loads nothing, and every
+ * bounded wait gives up after wait_limit_ns instead of 2 s.  No copy or MMA is in flight
+ * when the waits run out; the kernel writes VA_ERR_TIMEOUT into the status word, drains,
+ * frees its tensor memory and returns, leaving out/lse unwritten and the context usable.
+ * The token-tile kernel is not affected (use a call without token tiles).  One-shot: the
+ * call consumes it.  Errors: VA_ERR_INVALID_ARG unless 1 ms <= wait_limit_ns <= 2 s. */
+va_status varlen_test_stall_next_forward(int64_t wait_limit_ns);
 
 /* Copies the workspace status word to *status_host after synchronising the
  * stream.  VA_ERR_CUDA if the copy fails. */

@@ -25,12 +25,12 @@ EXPORTS = (
     "varlen_attn_workspace_size", "varlen_attn_plan", "varlen_attn_fwd", "varlen_attn_bwd",
     "varlen_read_status", "varlen_clear_status", "varlen_last_error", "varlen_version",
     "varlen_profile_enable", "varlen_profile_read", "varlen_kernel_name", "varlen_launch_count",
-    "varlen_attn_fwd_noalloc", "varlen_cu_seqlens_from_positions",
+    "varlen_attn_fwd_noalloc", "varlen_noalloc_read_status", "varlen_cu_seqlens_from_positions",
     "varlen_loss_targets", "varlen_token_ce_workspace_size", "varlen_token_ce",
     "varlen_unpad_index", "varlen_gather_rows",
     "varlen_attn_plan_window", "varlen_attn_fwd_window", "varlen_attn_bwd_window",
     "varlen_attn_workspace_size_cross", "varlen_attn_plan_cross", "varlen_attn_fwd_cross",
-    "varlen_attn_bwd_cross",
+    "varlen_attn_bwd_cross", "varlen_test_stall_next_forward",
 )
 
 
@@ -96,6 +96,7 @@ def _declare(lib):
         "varlen_attn_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p,
                                               POINTER(VaShape), c_float, c_int32, c_void_p,
                                               c_void_p, c_void_p]),
+        "varlen_noalloc_read_status": (c_int32, [i32p, c_void_p]),
         "varlen_unpad_index": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p]),
         "varlen_gather_rows": (c_int32, [c_void_p, c_int64, c_void_p, c_int32, c_int64, c_void_p, c_int64,
@@ -112,6 +113,7 @@ def _declare(lib):
         "varlen_profile_read": (c_int32, [i32p, POINTER(c_float), c_int32, i32p]),
         "varlen_kernel_name": (c_char_p, [c_int32]),
         "varlen_launch_count": (c_int64, []),
+        "varlen_test_stall_next_forward": (c_int32, [c_int64]),
         "varlen_last_error": (c_char_p, []),
         "varlen_version": (c_char_p, []),
     }

@@ -37,6 +37,8 @@ cudaError_t launch_bwd_dq_tc(const BwdParams&, int, int, bool, cudaStream_t);
 void bwd_tc_tiles(int*, int*, int*, int*);
 
 static thread_local std::string g_error;
+// Test hook of the failure path: a wait limit (ns) armed for the next forward call, 0 = none.
+static std::atomic<long long> g_stall_next_fwd{0};
 
 void set_error(const char* msg) { g_error = msg; }
 
@@ -418,6 +420,11 @@ static va_status fwd_impl(const void* q, const void* k, const void* v, const int
   p.window = window;
   p.cu_k = cu_k;
   p.Tk = cu_k ? Tk : 0;
+  const long long stall_ns = g_stall_next_fwd.exchange(0);
+  if (stall_ns > 0) {  // test hook: the producers load nothing and the waits give up after stall_ns
+    p.wait_ns = static_cast<uint64_t>(stall_ns);
+    p.stall = 1;
+  }
   // segment records, then (as its programmatic dependent, filling its tail) token records
   e = launch(K_FWD, cs, [&] { return launch_fwd_tc(p, s->d, static_cast<int>(L.cap), cs); });
   if (e != cudaSuccess) return cuda_fail(e, "fwd kernel");
@@ -672,5 +679,12 @@ const char* varlen_kernel_name(int32_t id) {
 }
 
 int64_t varlen_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+va_status varlen_test_stall_next_forward(int64_t wait_limit_ns) {
+  if (wait_limit_ns < 1000000 || wait_limit_ns > 2000000000)
+    return fail(VA_ERR_INVALID_ARG, "test_stall_next_forward: the limit must be 1 ms .. 2 s");
+  g_stall_next_fwd.store(wait_limit_ns);
+  return VA_OK;
+}
 
 }  // extern "C"

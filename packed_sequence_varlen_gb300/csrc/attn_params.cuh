@@ -25,6 +25,11 @@ struct FwdParams {
   int window = -1;   // causal local window: query i sees keys i-w..i; -1 = none
   const int32_t* cu_k = nullptr;  // cross-attention: K/V boundaries (cu is Q's); null = cu
   int Tk = 0;                     // cross-attention: rows of K and V
+  // Test hook of the failure path (varlen_test_stall_next_forward): a wait limit in ns
+  // (0 = the default) and stall = 1, which makes each CTA's producer publish its first work
+  // item and then load nothing, so the consumers' bounded waits run out.
+  uint64_t wait_ns = 0;
+  int stall = 0;
 };
 
 struct BwdParams {

@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::B_LE + b), 128);
     }
     *abort_flag = 0;
+    *wait_limit_slot(abort_flag) = kTimeoutNs;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -826,6 +827,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::B_IE + b), 32 + 256);  // MMA warp + both softmax warpgroups
     }
     *abort_flag = 0;
+    *wait_limit_slot(abort_flag) = kTimeoutNs;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {

@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(C::B_IE + b), 32 + 256);  // MMA warp + both softmax warpgroups
     }
     *abort_flag = 0;
+    *wait_limit_slot(abort_flag) = p.wait_ns ? p.wait_ns : kTimeoutNs;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       Item nxt;
       bool more = queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items, dec, nxt,
                                 abort_flag, p.hdr, ok);
+      if (p.stall) more = false;  // test hook: the first item is published and nothing is loaded
       for (; ok && more; ++item_cnt) {
         const Item I = nxt;  // publish the next record first: its decode overlaps this one
         more = queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.counter, n_items,

@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(C::B_IE + b), 32 + 256);  // MMA warp + both softmax warpgroups
     }
     *abort_flag = 0;
+    *wait_limit_slot(abort_flag) = kTimeoutNs;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {

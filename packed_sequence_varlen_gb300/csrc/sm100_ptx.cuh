@@ -44,17 +44,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Every kernel keeps its CTA's abort flag (int) in shared memory, followed by 4 bytes of
+// padding and the CTA's wait limit in nanoseconds (uint64, 8-byte aligned): thread 0 writes
+// both before the CTA's first barrier sync.  The limit is kTimeoutNs except in the forward's
+// test hook, which shortens it.
+__device__ __forceinline__ volatile uint64_t* wait_limit_slot(volatile int* abort_flag) {
+  return reinterpret_cast<volatile uint64_t*>(abort_flag + 1);
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // leaves the CTA's abort flag set) if the CTA is aborting or the wait timed out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           WsHeader* hdr, int where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = *wait_limit_slot(abort_flag);
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > limit) {
         *abort_flag = 1;
         if (atomicCAS(&hdr->status, 0, VA_ERR_TIMEOUT) == 0) hdr->where = where;
         return false;

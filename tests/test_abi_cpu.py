@@ -153,3 +153,27 @@ def test_bridge_entry_points_reject_bad_arguments(va):
     assert lib.varlen_gather_rows(p, 16, p, 4, 32, p, 64, None) == 1     # stride below the row
     assert lib.varlen_gather_rows(ctypes.c_void_p(8), 64, p, 4, 32, p, 64, None) == 1  # misaligned
     assert lib.varlen_gather_rows(p, 64, p, -1, 32, p, 64, None) == 1
+
+
+def test_noalloc_size_limit_is_the_forward_workspace(va):
+    """The allocation-free forward takes a shape exactly when the ordinary forward's workspace
+    fits its 1 MiB static array; past that it returns VA_ERR_WORKSPACE before any CUDA call."""
+    lib = va._lib.load()
+    T, H, d = 65536, 8, 64
+
+    def size(B):
+        s = va._lib.VaShape()
+        lib.varlen_shape_contiguous(ctypes.byref(s), T, B, H, H, d, 1)
+        return s, lib.varlen_attn_workspace_size(ctypes.byref(s), 0)
+
+    # the documented formula: 256 + align256(16 (T/256 + B) H) + align256(4 B)
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for B in (1, 100, 7000, 7693, 7694):
+        assert size(B)[1] == 256 + a256(16 * (T // 256 + B) * H) + a256(4 * B)
+    inside = max(B for B in range(7000, 8000) if size(B)[1] <= 1 << 20)
+    s, n = size(inside + 1)
+    assert n > 1 << 20
+    p = ctypes.c_void_p(256)
+    assert lib.varlen_attn_fwd_noalloc(p, p, p, p, ctypes.byref(s), 0.1, 1, p, p, None) == 3
+    assert b"1048576" in lib.varlen_last_error()
+    assert lib.varlen_noalloc_read_status(None, None) == 1

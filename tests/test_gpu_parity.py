@@ -179,8 +179,39 @@ def test_ragged_edge_lengths(va, d, causal, g):
 
 # ------------------------------------------------------------------ workloads
 
+def check_rows_every_head(q, k, v, do, cu, o, lse, grads, seed, rows_per_head=16, keys_per_head=4):
+    """Sampled rows of every q head (O, LSE, dQ) and key rows of every kv head (dK, dV), each
+    computed by the oracle from its own row, so that an indexing error confined to heads the
+    full-slice checks leave out is still caught.  Rows include segment starts and ends; key rows
+    sit near segment ends (cheap in the oracle)."""
+    dq, dk, dv = grads
+    qq, kk, vv, dd = (si.to_f64(x) for x in (q, k, v, do))
+    T, Hq, Hkv = q.shape[0], q.shape[1], k.shape[1]
+    rng = np.random.default_rng(seed)
+    starts, ends = np.asarray(cu[:-1]), np.asarray(cu[1:]) - 1
+    toks, heads = [], []
+    for h in range(Hq):
+        pick = rng.integers(0, T, rows_per_head - 2).tolist()
+        pick += [int(rng.choice(starts)), int(rng.choice(ends))]
+        toks += pick
+        heads += [h] * len(pick)
+    toks, heads = np.asarray(toks), np.asarray(heads)
+    so, sl, sdq = oa.rows_forward_backward(qq, kk, vv, dd, cu, toks, heads)
+    assert np.abs(o[toks, heads] - so).max() <= wl.O_MAX_ABS
+    assert np.abs(lse[heads, toks] - sl).max() <= wl.LSE_MAX_ABS
+    assert wl.rel_l2(dq[toks, heads], sdq) <= wl.GRAD_REL_L2
+    lens = np.diff(cu)
+    for hk in range(Hkv):
+        segs = rng.choice(len(lens), keys_per_head, replace=False)
+        ktoks = np.array([int(cu[b + 1]) - 1 - int(rng.integers(0, min(48, lens[b]))) for b in segs])
+        rk, rv = oa.key_rows_backward(qq, kk, vv, dd, cu, ktoks, hk)
+        assert wl.rel_l2(dk[ktoks, hk], rk) <= wl.GRAD_REL_L2
+        assert wl.rel_l2(dv[ktoks, hk], rv) <= wl.GRAD_REL_L2
+
+
 @pytest.mark.parametrize("index,kv_heads", [(0, [0, 17]), (1, [31]), (5, [8])])
 def test_sft8k_packs(va, index, kv_heads):
+    """Full-slice checks on a few kv heads, plus sampled rows of every head."""
     w = si.WORKLOADS["sft8k"]
     lengths = wl.pack("sft8k", index)
     cu, _, _, mx = op.build_metadata(lengths)
@@ -189,10 +220,12 @@ def test_sft8k_packs(va, index, kv_heads):
     ro, rl, rg = run_oracle(q, k, v, do, cu, kv_heads=kv_heads)
     wl.assert_close_outputs(o, lse, ro, rl)
     wl.assert_close_grads(g, rg)
+    check_rows_every_head(q, k, v, do, cu, o, lse, g, seed=index)
 
 
 @pytest.mark.parametrize("which", ["first", "most_segments"])
 def test_gqa16k_bins(va, which):
+    """Full-slice checks on one kv head (its four q heads), plus sampled rows of every head."""
     w = si.WORKLOADS["gqa16k"]
     index = 0 if which == "first" else wl.most_segments_pack("gqa16k")
     lengths = wl.pack("gqa16k", index)
@@ -202,6 +235,7 @@ def test_gqa16k_bins(va, which):
     ro, rl, rg = run_oracle(q, k, v, do, cu, kv_heads=[index % w.Hkv])
     wl.assert_close_outputs(o, lse, ro, rl)
     wl.assert_close_grads(g, rg)
+    check_rows_every_head(q, k, v, do, cu, o, lse, g, seed=100 + index)
 
 
 def test_long64k(va):
