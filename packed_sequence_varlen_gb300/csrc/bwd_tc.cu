@@ -23,8 +23,10 @@
 //   publishes them (sched.cuh); warp 1 MMA issuer (whole warp, one elected lane issues) +
 //   TMEM owner; warp 2 (dK/dV only) stages
 //   lse and D of each step in shared memory; warps 4-7 and 8-11 two
-//   softmax warpgroups that take alternate steps, each with its own TMEM S/dP
-//   buffer, so the tensor core computes step i+1 while step i is exponentiated.
+//   softmax warpgroups that split every step's 64 columns between them (32
+//   each), which halves the softmax latency on each step's dependency chain;
+//   S/dP are double-buffered by step, so the tensor core computes step i+1
+//   while step i is exponentiated.
 // TMEM: S_0 | S_1 | dP_0 | dP_1 (64 columns each) | accumulators.
 //
 // Token records (runs of segments of at most 64 tokens, at the end of both maps) take the
@@ -67,12 +69,18 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
 template <int D>
 struct KvCfg {
   static constexpr int KB = 128, QB = 64;
-  static constexpr int QST = D == 128 ? 3 : 8;   // Q/dO ring slots (one step each)
+  // K/V buffers (items alternate) and Q/dO ring slots (one step each).  At d = 128 shared
+  // memory holds either two K/V buffers and three ring slots or one K/V buffer and five
+  // slots.  One buffer and five slots measured 3% faster on 16K packs of long documents but
+  // 1.3% slower on 8K packs of short ones (the next item's K/V load is exposed when items
+  // are short), so the two-buffer form is kept.
+  static constexpr int KVB = 2;
+  static constexpr int QST = D == 128 ? 3 : 8;
   static constexpr int TKV = KB * D * 2;         // one K or V tile
   static constexpr int TQ = QB * D * 2;          // one Q or dO tile
   static constexpr int PKV = KB * 128, PQ = QB * 128;  // 64-column panels
   // two K/V buffers (items alternate): buffer b holds K at KV_OFF(b), V right after
-  static constexpr int RING_OFF = 4 * TKV;
+  static constexpr int RING_OFF = 2 * KVB * TKV;
   static constexpr int LDS = 4;                            // lse/D ring slots (one step each)
   static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [LDS][-lse*log2e 64 | -D 64] fp32
   static constexpr int BAR_OFF = LD_OFF + LDS * 2 * 64 * 4;
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::B_SF + x), 1);
-      mbar_init(bar(C::B_PF + x), 128);
+      mbar_init(bar(C::B_PF + x), 256);  // both softmax warpgroups, one half of the step each
     }
     mbar_init(bar(C::B_AF), 1);
     mbar_init(bar(C::B_AE), 256);
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int b = 0; b < C::LDS; ++b) {
       mbar_init(bar(C::B_LF + b), 32);
-      mbar_init(bar(C::B_LE + b), 128);
+      mbar_init(bar(C::B_LE + b), 256);
     }
     *abort_flag = 0;
     *wait_limit_slot(abort_flag) = kTimeoutNs;
@@ -285,11 +293,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         return out.valid != 0;
       };
-      // K/V of this CTA's j-th item into buffer j & 1, once item j-2's S/dP MMAs are done
+      // K/V of this CTA's j-th item into buffer j % KVB, once item j - KVB's S/dP MMAs are done
       // with it
       auto load_kv = [&](const KvItem& J, int j) -> bool {
-        const int kb = j & 1;
-        if (!wwait(bar(C::B_KVE + kb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
+        const int kb = j % C::KVB;
+        if (!wwait(bar(C::B_KVE + kb), ((j / C::KVB) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
         mbar_expect_tx_w(bar(C::B_KVF + kb), 2 * C::TKV);
         for (int pn = 0; pn < D / 64; ++pn) {
           tma_load_3d_w(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, J.hk,
@@ -311,8 +319,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                      nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
         // the next item's K/V goes out right after this item's first two Q/dO steps, a whole
-        // item ahead of its use
-        const int kv_at = I.steps < 2 ? I.steps : 2;
+        // item ahead of its use (two buffers), or after all of them (one buffer: it waits for
+        // this item's last S/dP MMAs, which need those steps)
+        const int kv_at = C::KVB == 1 ? I.steps : (I.steps < 2 ? I.steps : 2);
         for (int i = 0; ok && i <= I.steps; ++i) {
           if (i == kv_at && more) {
             ok = load_kv(nxt, item_cnt + 1);
@@ -334,8 +343,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) {
         // let every copy this thread started land before the CTA exits
-        for (int j = kv_issued - 1; j >= 0 && j >= kv_issued - 2; --j)
-          drain_wait_b(bar(C::B_KVF + (j & 1)), (j >> 1) & 1);
+        for (int j = kv_issued - 1; j >= 0 && j >= kv_issued - C::KVB; --j)
+          drain_wait_b(bar(C::B_KVF + j % C::KVB), (j / C::KVB) & 1);
         for (int i = qit - 1; i >= 0 && i >= qit - C::QST; --i)
           drain_wait_b(bar(C::B_QF + i % C::QST), (i / C::QST) & 1);
       }
@@ -374,8 +383,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool all_ok = __all_sync(0xffffffffu, ok);
         if (!all_ok) ok = false;
         if (!all_ok || !got_) break;
-        kb = item_cnt & 1;
-        ok = wwait(bar(C::B_KVF + kb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 23);
+        kb = item_cnt % C::KVB;
+        ok = wwait(bar(C::B_KVF + kb), (item_cnt / C::KVB) & 1, abort_flag, p.hdr, 23);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.steps; ++j) {
           const int s = (qit + j) % C::QST;
@@ -400,10 +409,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t qm = ringM0 + ((s * 2 * C::TQ) >> 4), dm = qm + (C::TQ >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts_w(tmem + 256, tmem + x * 64 + kk * 8, dm + kk * (2048 >> 4), idG, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tmem + 256, tmem + x * 64 + (kk >> 1) * 32 + (kk & 1) * 8, dm + kk * (2048 >> 4), idG,
+                     (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < C::QB / 16; ++kk)
-            mma_ts_w(tmem + 256 + D, tmem + 128 + x * 64 + kk * 8, qm + kk * (2048 >> 4), idG,
+            mma_ts_w(tmem + 256 + D, tmem + 128 + x * 64 + (kk >> 1) * 32 + (kk & 1) * 8, qm + kk * (2048 >> 4), idG,
                       (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(bar(C::B_QE + s));
           if (i + 2 < I.steps) {
@@ -458,19 +468,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     regs_inc<kRegsSoftmax>();
-    const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: 0 -> dV, 1 -> dK
+    // Both warpgroups take every step, warpgroup x its query columns [32 x, 32 x + 32) of the
+    // step's S^T / dP^T buffer (step i uses buffer i & 1), writing P^T and dS^T (bf16) over the
+    // first 16 columns of that range; epilogue: 0 -> dV, 1 -> dK.
+    const int x = (warp - 4) >> 2;
+    const int cw = 32 * x;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + x * 64;
-    const uint32_t dp_addr = tmem + lane_off + 128 + x * 64;
+    const uint32_t s_addr = tmem + lane_off + cw;
+    const uint32_t dp_addr = tmem + lane_off + 128 + cw;
     const uint32_t acc_addr = tmem + lane_off + 256 + x * D;
     const float* ldring = reinterpret_cast<const float*>(sm + C::LD_OFF);  // [slot][-lse2 64 | -D 64]
     const float sl2 = p.scale_log2;
-    uint32_t sf = 0;
+    uint32_t sf0 = 0, sf1 = 0;  // s_full phases per buffer
     int item_cnt = 0;
     bool ok = true;
     int g0 = 0;  // this CTA's steps before the current item (the lse/D ring index)
+    // Epilogue: the accumulators are released as soon as they are in registers, and the packed
+    // row is held and stored after this warpgroup's first step of the next item, so that the
+    // tensor core starts that item while the previous one is written out.
+    uint4 held[D / 8];
+    bf16* held_out = nullptr;
+    bool held_store = false, holding = false;
+    auto flush = [&]() {
+      store_rows_coalesced(held, held_out, p.k_rs, held_store);
+      holding = false;
+    };
+    auto take_accumulators = [&](int k, bf16* out, bool store) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_AF), k & 1, abort_flag, p.hdr, 29))) return false;
+      fence_after_sync();
+      const float mul = x == 0 ? 1.f : p.scale;
+      uint32_t o[D];  // the whole accumulator row in one TMEM round trip
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(acc_addr + c * 32, o + c * 32);
+      tmem_wait_ld();
+      fence_before_sync();
+      mbar_arrive(bar(C::B_AE));
+#pragma unroll
+      for (int j = 0; j < D / 2; ++j)
+        o[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) held[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+      held_out = out;
+      held_store = store;
+      holding = true;
+      return true;
+    };
     KvItem J;          // the first token item, once the segment loop has met it
     bool tok = false;
     for (;; ++item_cnt) {
@@ -489,37 +533,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       const int kvrow = I.n * 128 + r;
-      for (int i = x; i < I.steps; i += 2) {
-        const int gs = g0 + i, ls = gs % C::LDS;
+      for (int i = 0; i < I.steps; ++i) {
+        const int gs = g0 + i, ls = gs % C::LDS, b = i & 1;
         ok = mbar_wait(bar(C::B_LF + ls), (gs / C::LDS) & 1, abort_flag, p.hdr, 19);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 28);
+        ok = mbar_wait(bar(C::B_SF + b), (b ? sf1 : sf0) & 1, abort_flag, p.hdr, 28);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        ++sf;
+        if (b) ++sf1;
+        else ++sf0;
         fence_after_sync();
-        const int q0 = (I.m_start + i / p.g) * 64;
+        const int q0 = (I.m_start + i / p.g) * 64 + cw;  // this warpgroup's first query column
         const int lim = kvrow - (X ? I.off : 0) - q0;  // query columns c < lim are masked (key after query)
         // (window) query columns c >= hi are masked too: past the key's window
         const int hi = WIN ? kvrow + p.window + 1 - q0 : 0;
         const bool need_mask =
-            p.causal && (I.n * 128 + 127 - (X ? I.off : 0) > q0 || (WIN && q0 + 63 > I.n * 128 + p.window));
-        const float* L = ldring + ls * 128;
+            p.causal && (I.n * 128 + 127 - (X ? I.off : 0) > q0 || (WIN && q0 + 31 > I.n * 128 + p.window));
+        const float* L = ldring + ls * 128 + cw;
         const float* Dd = L + 64;
-        // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(s_addr, sv);
-        tmem_ld32(s_addr + 32, sv + 32);
-        tmem_ld32(dp_addr, dpv);
-        tmem_ld32(dp_addr + 32, dpv + 32);
+        // one TMEM round trip: this warpgroup's 32 scores and 32 dP values of this kv row
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(s_addr + b * 64, sv);
+        tmem_ld32(dp_addr + b * 64, dpv);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < 32; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(L + c);
           const float4 d4 = *reinterpret_cast<const float4*>(Dd + c);
 #pragma unroll
@@ -539,74 +582,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dpv[j >> 1] = pack_bf16(p0 * t0, p1 * t1);
           }
         }
-        tmem_st32(s_addr, sv);
-        tmem_st32(dp_addr, dpv);
+        tmem_st16(s_addr + b * 64, sv);
+        tmem_st16(dp_addr + b * 64, dpv);
         mbar_arrive(bar(C::B_LE + ls));  // this thread has read the slot's lse/D
         tmem_wait_st();
         fence_before_sync();
-        mbar_arrive(bar(C::B_PF + x));
+        mbar_arrive(bar(C::B_PF + b));
+        if (holding) flush();  // the previous item's row, under this item's first MMAs
       }
       if (!ok) break;
       g0 += I.steps;
-      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
-      ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 29);
-      if (!__all_sync(0xffffffffu, ok)) {
+      // epilogue: warpgroup 0 takes dV, warpgroup 1 scale * dK
+      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>((X ? I.s0k : I.s0) + kvrow) * p.k_rs +
+                  static_cast<int64_t>(I.hk) * p.k_hs;
+      if (!take_accumulators(item_cnt, out, kvrow < (X ? I.lk : I.l))) {
         ok = false;
         break;
       }
-      fence_after_sync();
-      const float mul = x == 0 ? 1.f : p.scale;
-      const bool store = kvrow < (X ? I.lk : I.l);
-      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>((X ? I.s0k : I.s0) + kvrow) * p.k_rs +
-                  static_cast<int64_t>(I.hk) * p.k_hs;
-      {
-        uint32_t o[D];  // the whole accumulator row in one TMEM round trip
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(acc_addr + c * 32, o + c * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < D / 2; ++j)
-          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
-        uint4 ov[D / 8];
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        store_rows_coalesced(ov, out, p.k_rs, store);
-      }
-      fence_before_sync();
-      mbar_arrive(bar(C::B_AE));
     }
     // Token items (runs of short segments; all of them follow the segment items): every step
     // masked on both sides per key row, rows past the item's keys not stored.
     for (KvItem I = J; TOK && ok && tok;) {
       const int kend = I.s0 + row_tables[(item_cnt & 3) * C::KB + r];  // end of this key's segment
-      for (int i = x; i < I.steps; i += 2) {
-        const int gs = g0 + i, ls = gs % C::LDS;
+      for (int i = 0; i < I.steps; ++i) {
+        const int gs = g0 + i, ls = gs % C::LDS, b = i & 1;
         ok = mbar_wait(bar(C::B_LF + ls), (gs / C::LDS) & 1, abort_flag, p.hdr, 19);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 28);
+        ok = mbar_wait(bar(C::B_SF + b), (b ? sf1 : sf0) & 1, abort_flag, p.hdr, 28);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        ++sf;
+        if (b) ++sf1;
+        else ++sf0;
         fence_after_sync();
-        const int q0 = I.s0 + (i / p.g) * 64;
+        const int q0 = I.s0 + (i / p.g) * 64 + cw;  // this warpgroup's first query column
         // query columns c < lim (before the key) and c >= hi (past its segment) are masked
         const int lim = I.s0 + r - q0, hi = kend - q0;
-        const float* L = ldring + ls * 128;
+        const float* L = ldring + ls * 128 + cw;
         const float* Dd = L + 64;
-        // one TMEM round trip: the step's 64 scores and 64 dP values of this kv row
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(s_addr, sv);
-        tmem_ld32(s_addr + 32, sv + 32);
-        tmem_ld32(dp_addr, dpv);
-        tmem_ld32(dp_addr + 32, dpv + 32);
+        // one TMEM round trip: this warpgroup's 32 scores and 32 dP values of this kv row
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(s_addr + b * 64, sv);
+        tmem_ld32(dp_addr + b * 64, dpv);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < 32; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(L + c);
           const float4 d4 = *reinterpret_cast<const float4*>(Dd + c);
 #pragma unroll
@@ -624,41 +648,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dpv[j >> 1] = pack_bf16(p0 * t0, p1 * t1);
           }
         }
-        tmem_st32(s_addr, sv);
-        tmem_st32(dp_addr, dpv);
+        tmem_st16(s_addr + b * 64, sv);
+        tmem_st16(dp_addr + b * 64, dpv);
         mbar_arrive(bar(C::B_LE + ls));  // this thread has read the slot's lse/D
         tmem_wait_st();
         fence_before_sync();
-        mbar_arrive(bar(C::B_PF + x));
+        mbar_arrive(bar(C::B_PF + b));
+        if (holding) flush();  // the previous item's row, under this item's first MMAs
       }
       if (!ok) break;
       g0 += I.steps;
-      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
-      ok = mbar_wait(bar(C::B_AF), item_cnt & 1, abort_flag, p.hdr, 29);
-      if (!__all_sync(0xffffffffu, ok)) {
+      // epilogue: warpgroup 0 takes dV, warpgroup 1 scale * dK; rows past the item's keys are not stored
+      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>(I.s0 + r) * p.k_rs +
+                  static_cast<int64_t>(I.hk) * p.k_hs;
+      if (!take_accumulators(item_cnt, out, r < I.kvn)) {
         ok = false;
         break;
       }
-      fence_after_sync();
-      const float mul = x == 0 ? 1.f : p.scale;
-      const bool store = r < I.kvn;
-      bf16* out = (x == 0 ? p.dv : p.dk) + static_cast<int64_t>(I.s0 + r) * p.k_rs +
-                  static_cast<int64_t>(I.hk) * p.k_hs;
-      {
-        uint32_t o[D];  // the whole accumulator row in one TMEM round trip
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(acc_addr + c * 32, o + c * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < D / 2; ++j)
-          o[j] = pack_bf16(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
-        uint4 ov[D / 8];
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) ov[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        store_rows_coalesced(ov, out, p.k_rs, store);
-      }
-      fence_before_sync();
-      mbar_arrive(bar(C::B_AE));
       ++item_cnt;
       const bool got = queue_take(item_cnt, queue, bar(C::B_IF), bar(C::B_IE), I, abort_flag, p.hdr, ok);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -667,6 +673,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!got) break;
     }
+    if (ok && holding) flush();  // the CTA's last item
   }
 
   fence_before_sync();
@@ -815,7 +822,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::B_SF + x), 1);
-      mbar_init(bar(C::B_PF + x), 128);
+      mbar_init(bar(C::B_PF + x), 256);  // both softmax warpgroups, one half of the step each
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::B_AF + b), 1);
@@ -993,7 +1000,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t km = ringM0 + ((s * 2 * C::TKV) >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::KB / 16; ++kk)
-            mma_ts_w(tmem + 256 + (item_cnt & 1) * D, tmem + 128 + x * 64 + kk * 8, km + kk * (2048 >> 4), idG,
+            mma_ts_w(tmem + 256 + (item_cnt & 1) * D, tmem + 128 + x * 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                     km + kk * (2048 >> 4), idG,
                       (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(bar(C::B_KE + s));
           if (n + 2 < I.nb) {
@@ -1017,15 +1025,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     regs_inc<kRegsSoftmax>();
-    const int x = (warp - 4) >> 2;  // steps x, x+2, ...; epilogue: dQ columns [x D/2, (x+1) D/2)
+    // Both warpgroups take every step, warpgroup x its key columns [32 x, 32 x + 32) of the
+    // step's S / dP buffer (step n uses buffer n & 1), writing dS (bf16) over the first 16
+    // columns of that range of dP; epilogue: dQ columns [x D/2, (x+1) D/2).
+    const int x = (warp - 4) >> 2;
+    const int cw = 32 * x;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + x * 64;
-    const uint32_t dp_addr = tmem + lane_off + 128 + x * 64;
+    const uint32_t s_addr = tmem + lane_off + cw;
+    const uint32_t dp_addr = tmem + lane_off + 128 + cw;
     const uint32_t acc_addr = tmem + lane_off + 256;
     const float sl2 = p.scale_log2;
-    uint32_t sf = 0;
+    uint32_t sf0 = 0, sf1 = 0;  // s_full phases per buffer
     int item_cnt = 0;
     bool ok = true;
     // The dQ accumulator is double-buffered (item k uses buffer k & 1), so item k's
@@ -1087,35 +1099,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         lse_raw = __ldg(p.lse + at);
         dsum = __ldg(p.dsum + at);
       }
-      for (int n = x; n < I.nb; n += 2) {
-        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 38);
+      for (int n = 0; n < I.nb; ++n) {
+        const int b = n & 1;
+        ok = mbar_wait(bar(C::B_SF + b), (b ? sf1 : sf0) & 1, abort_flag, p.hdr, 38);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        ++sf;
+        if (b) ++sf1;
+        else ++sf0;
         fence_after_sync();
         const float lse2 = qin ? lse_raw * kLog2e : INFINITY;
         // key columns c > lim are masked: after the query (causal) or past the segment end;
         // (window) key columns c < lo too: before the query's window
-        const int kn = WIN ? I.kb - I.s0 + n * 64 : n * 64;  // the step's first key, segment-local
-        int lim = p.causal ? qrow - kn : I.l - 1 - n * 64;
+        const int kn = (WIN ? I.kb - I.s0 : 0) + n * 64 + cw;  // this warpgroup's first key, segment-local
+        int lim = p.causal ? qrow - kn : I.l - 1 - kn;
         const int lo = WIN ? qrow - p.window - kn : 0;
-        bool need_mask = p.causal ? (kn + 63 > I.m * 128 || (WIN && kn < I.m * 128 + 127 - p.window))
-                                  : (n * 64 + 64 > I.l);
+        bool need_mask = p.causal ? (kn + 31 > I.m * 128 || (WIN && kn < I.m * 128 + 127 - p.window))
+                                  : (kn + 32 > I.l);
         if constexpr (X) {
           lim = p.causal ? qrow + I.off - kn : I.lk - 1 - kn;
-          need_mask = p.causal ? (kn + 63 > I.m * 128 + I.off) : (kn + 64 > I.lk);
+          need_mask = p.causal ? (kn + 31 > I.m * 128 + I.off) : (kn + 32 > I.lk);
         }
-        // one TMEM round trip: the step's 64 scores and 64 dP values of this q row
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(s_addr, sv);
-        tmem_ld32(s_addr + 32, sv + 32);
-        tmem_ld32(dp_addr, dpv);
-        tmem_ld32(dp_addr + 32, dpv + 32);
+        // one TMEM round trip: this warpgroup's 32 scores and 32 dP values of this q row
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(s_addr + b * 64, sv);
+        tmem_ld32(dp_addr + b * 64, dpv);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < 32; c += 2) {
           float x0, x1;
           ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -1127,10 +1139,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
           dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
         }
-        tmem_st32(dp_addr, dpv);
+        tmem_st16(dp_addr + b * 64, dpv);
         tmem_wait_st();
         fence_before_sync();
-        mbar_arrive(bar(C::B_PF + x));
+        mbar_arrive(bar(C::B_PF + b));
         if (pend >= 0 && !epilogue()) {
           ok = false;
           break;
@@ -1159,27 +1171,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         lse_raw = __ldg(p.lse + at);
         dsum = __ldg(p.dsum + at);
       }
-      for (int n = x; n < I.nb; n += 2) {
-        ok = mbar_wait(bar(C::B_SF + x), sf & 1, abort_flag, p.hdr, 38);
+      for (int n = 0; n < I.nb; ++n) {
+        const int b = n & 1;
+        ok = mbar_wait(bar(C::B_SF + b), (b ? sf1 : sf0) & 1, abort_flag, p.hdr, 38);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        ++sf;
+        if (b) ++sf1;
+        else ++sf0;
         fence_after_sync();
         const float lse2 = qin ? lse_raw * kLog2e : INFINITY;
         // key columns c > lim (after the query) and c < lo (before its segment) are masked
-        const int k0 = I.kb + n * 64;
+        const int k0 = I.kb + n * 64 + cw;
         const int lim = I.s0 + r - k0, lo = klo - k0;
-        // one TMEM round trip: the step's 64 scores and 64 dP values of this q row
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(s_addr, sv);
-        tmem_ld32(s_addr + 32, sv + 32);
-        tmem_ld32(dp_addr, dpv);
-        tmem_ld32(dp_addr + 32, dpv + 32);
+        // one TMEM round trip: this warpgroup's 32 scores and 32 dP values of this q row
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(s_addr + b * 64, sv);
+        tmem_ld32(dp_addr + b * 64, dpv);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < 32; c += 2) {
           float x0, x1;
           ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, -lse2, -lse2);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -1189,10 +1201,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dsum, -dsum);
           dpv[c >> 1] = pack_bf16(p0 * t0, p1 * t1);
         }
-        tmem_st32(dp_addr, dpv);
+        tmem_st16(dp_addr + b * 64, dpv);
         tmem_wait_st();
         fence_before_sync();
-        mbar_arrive(bar(C::B_PF + x));
+        mbar_arrive(bar(C::B_PF + b));
         if (pend >= 0 && !epilogue()) {
           ok = false;
           break;
