@@ -439,11 +439,43 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def link_bandwidth(dev, nbytes: int = 256 << 20, reps: int = 5):
+    """Pinned host <-> device copy bandwidth (GB/s): H2D alone, D2H alone, and each direction
+    while both run at once on their own streams (how the e2e step uses the link)."""
+    import torch
+    h_up = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_dn = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_up = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_dn = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / reps
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_up.copy_(h_up, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_dn.copy_(d_dn, non_blocking=True)
+    return {"h2d": round(nbytes / timed(lambda: d_up.copy_(h_up, non_blocking=True)) / 1e9, 1),
+            "d2h": round(nbytes / timed(lambda: h_dn.copy_(d_dn, non_blocking=True)) / 1e9, 1),
+            "concurrent_each": round(nbytes / timed(both) / 1e9, 1)}
+
+
 def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
     """Same step through the public API from pinned HOST buffers: H2D of every pack's q/k/v/dO
     and lengths, the step, D2H of dq/dk/dv, all inside the timed region.  Copies run on their
-    own streams with two device buffer sets, so pack p+1 uploads and pack p-1 downloads while
-    pack p computes (H2D and D2H use opposite link directions)."""
+    own streams with two device buffer sets used in turn, continuously across steps: pack
+    p+1 uploads and pack p-1 downloads while pack p computes (H2D and D2H use opposite link
+    directions); a set is reused only after its previous pack computed (inputs) and
+    downloaded (gradients).  Two sets measured faster than three (24.5 against 35 ms per
+    sft8k step: with three, the uploads themselves ran at about 150 GB/s instead of 170)."""
     import torch
     d, Hq, Hkv, T = w.d, w.Hq, w.Hkv, w.pad_to or sum(packs[0])
     host_in = []
@@ -451,7 +483,8 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
         q, k, v, do = si.tensors(T, Hq, Hkv, d, seed_offset=1000 * pi)
         host_in.append(tuple(x.pin_memory() for x in (q, k, v, do)))
     host_len = [torch.tensor(p, dtype=torch.int32).pin_memory() for p in packs]
-    host_out = tuple(torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory() for H in (Hq, Hkv, Hkv))
+    host_out = [tuple(torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory() for H in (Hq, Hkv, Hkv))
+                for _ in range(len(packs))]
     nbuf = 2
     dev_in = [[torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv, Hq)]
               for _ in range(nbuf)]
@@ -461,29 +494,29 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
     g = [[torch.empty((T, H, d), dtype=torch.bfloat16, device=dev) for H in (Hq, Hkv, Hkv)] for _ in range(nbuf)]
     all_docs = [L for p in packs for L in p]
     h2d = sum(x.numel() * x.element_size() for t in host_in for x in t) + sum(x.numel() * 4 for x in host_len)
-    d2h = len(packs) * sum(x.numel() * x.element_size() for x in host_out)
+    d2h = sum(x.numel() * x.element_size() for t in host_out for x in t)
     s_up, s_cmp, s_dn = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n = len(packs)
+    done = [None] * nbuf   # the last pack that used buffer set b has computed
+    down = [None] * nbuf   # ... and its gradients are downloaded
 
     def step():
         if plan_host is not None:
             plan_host(all_docs, w.capacity)
-        up = [torch.cuda.Event() for _ in range(n)]
-        done = [torch.cuda.Event() for _ in range(n)]
-        down = [torch.cuda.Event() for _ in range(n)]
         for p in range(n):
             b = p % nbuf
             with torch.cuda.stream(s_up):
-                if p >= nbuf:
-                    s_up.wait_event(done[p - nbuf])  # buffer set b is free once pack p-2 computed
+                if done[b] is not None:
+                    s_up.wait_event(done[b])
                 for dst, src in zip(dev_in[b], host_in[p]):
                     dst.copy_(src, non_blocking=True)
                 lens_dev[b][:len(packs[p])].copy_(host_len[p], non_blocking=True)
-                up[p].record(s_up)
+                up = torch.cuda.Event()
+                up.record(s_up)
             with torch.cuda.stream(s_cmp):
-                s_cmp.wait_event(up[p])
-                if p >= nbuf:
-                    s_cmp.wait_event(down[p - nbuf])  # gradient set b is free once downloaded
+                s_cmp.wait_event(up)
+                if down[b] is not None:
+                    s_cmp.wait_event(down[b])
                 k_ = len(packs[p])
                 cu, _, _, _, _ = va.build_metadata(lens_dev[b][:k_], pad_to=T, T_capacity=T)
                 Bp = k_ + (1 if sum(packs[p]) < T else 0)
@@ -493,26 +526,38 @@ def run_e2e(args, va, dev, packs, idx, w, step_flops, dist, barrier, plan_host):
                 va.varlen_attn_fwd(q, k, v, cu, mxs, None, True, out=o, lse=lse, window=WINDOW)
                 va.varlen_attn_bwd(q, k, v, o, lse, do, cu, mxs, None, True, dq=g[b][0], dk=g[b][1], dv=g[b][2],
                                    window=WINDOW)
-                done[p].record(s_cmp)
+                done[b] = torch.cuda.Event()
+                done[b].record(s_cmp)
             with torch.cuda.stream(s_dn):
-                s_dn.wait_event(done[p])
-                for dst, src in zip(host_out, g[b]):
+                s_dn.wait_event(done[b])
+                for dst, src in zip(host_out[p], g[b]):
                     dst.copy_(src, non_blocking=True)
-                down[p].record(s_dn)
-        torch.cuda.current_stream(dev).wait_stream(s_dn)
+                down[b] = torch.cuda.Event()
+                down[b].record(s_dn)
+
+    def drain():
+        for s_ in (s_up, s_cmp, s_dn):
+            torch.cuda.current_stream(dev).wait_stream(s_)
 
     for _ in range(max(1, args.warmup)):
         step()
+    drain()
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
+    drain()
     barrier()
     dt = time.perf_counter() - t0
     max_ms, total_flops = aggregate(dt * 1e3, step_flops, args.steps, dist, dev)
+    link = link_bandwidth(dev)
+    bound_ms = max(h2d / link["concurrent_each"], d2h / link["concurrent_each"]) / 1e6
     return {"value": round(total_flops / (max_ms * 1e-3) / 1e12, 3), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "overlap": "H2D, compute and D2H on three streams, two device buffer sets"}
+            "ms_per_step": round(max_ms / args.steps, 3),
+            "link_gbs": link, "link_bound_ms_per_step": round(bound_ms, 3),
+            "frac_of_link_bound": round(bound_ms / (max_ms / args.steps), 4),
+            "overlap": "H2D, compute and D2H on three streams, two device buffer sets used in turn across steps"}
 
 
 # ------------------------------------------------------------------ oracle timing
