@@ -69,22 +69,21 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
 template <int D>
 struct KvCfg {
   static constexpr int KB = 128, QB = 64;
-  // K/V buffers (items alternate) and Q/dO ring slots (one step each).  At d = 128 shared
-  // memory holds either two K/V buffers and three ring slots or one K/V buffer and five
-  // slots.  One buffer and five slots measured 3% faster on 16K packs of long documents but
-  // 1.3% slower on 8K packs of short ones (the next item's K/V load is exposed when items
-  // are short), so the two-buffer form is kept.
-  static constexpr int KVB = 2;
-  static constexpr int QST = D == 128 ? 3 : 8;
+  // Two K buffers (items alternate: the next item's K loads a whole item ahead), one V
+  // buffer (the next item's V loads once this item's last dP^T MMA is done, about two steps
+  // before it is needed) and a Q/dO ring of QST slots (one step each).  At d = 128 the
+  // single V buffer is what leaves room for the ring's fourth slot, which lets the producer
+  // load the next item's first Q/dO steps before this item ends.
+  static constexpr int QST = D == 128 ? 4 : 8;
   static constexpr int TKV = KB * D * 2;         // one K or V tile
   static constexpr int TQ = QB * D * 2;          // one Q or dO tile
   static constexpr int PKV = KB * 128, PQ = QB * 128;  // 64-column panels
-  // two K/V buffers (items alternate): buffer b holds K at KV_OFF(b), V right after
-  static constexpr int RING_OFF = 2 * KVB * TKV;
+  static constexpr int V_OFF = 2 * TKV;          // K buffers at 0 and TKV, then V
+  static constexpr int RING_OFF = 3 * TKV;
   static constexpr int LDS = 4;                            // lse/D ring slots (one step each)
   static constexpr int LD_OFF = RING_OFF + QST * 2 * TQ;  // [LDS][-lse*log2e 64 | -D 64] fp32
   static constexpr int BAR_OFF = LD_OFF + LDS * 2 * 64 * 4;
-  static constexpr int B_KVF = 0, B_KVE = 2, B_QF = 4, B_QE = 4 + QST, B_SF = 4 + 2 * QST,
+  static constexpr int B_KF = 0, B_KE = 2, B_VF = 4, B_VE = 5, B_QF = 6, B_QE = 6 + QST, B_SF = 6 + 2 * QST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 1, B_DR = B_AE + 1,
                        B_IF = B_DR + 1, B_IE = B_IF + 2, B_LF = B_IE + 2, B_LE = B_LF + LDS,
                        NBAR = B_LE + LDS;
@@ -92,7 +91,6 @@ struct KvCfg {
   static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 48;   // four 128-byte row tables (item k & 3)
   static constexpr int MISC_OFF = ROWS_OFF + 4 * KB;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
-  __host__ __device__ static constexpr uint32_t kv_off(int b) { return static_cast<uint32_t>(b) * 2 * TKV; }
 };
 static_assert(KvCfg<128>::SMEM <= 232448 && KvCfg<64>::SMEM <= 232448, "dK/dV shared memory");
 
@@ -217,9 +215,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::B_KVF + b), 1);
-      mbar_init(bar(C::B_KVE + b), 1);
+      mbar_init(bar(C::B_KF + b), 1);
+      mbar_init(bar(C::B_KE + b), 1);
     }
+    mbar_init(bar(C::B_VF), 1);
+    mbar_init(bar(C::B_VE), 1);
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(C::B_QF + s), 1);
       mbar_init(bar(C::B_QE + s), 1);
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
     {  // the whole warp runs the loop; elect.sync picks the issuing lane
-      int qit = 0, item_cnt = 0, kv_issued = 0;  // kv_issued: items whose K/V load went out
+      int qit = 0, item_cnt = 0, k_issued = 0, v_issued = 0;  // items whose K / V load went out
       bool ok = true;
       KvItem nxt;
       // Publishes this CTA's k-th item (the next record of the map): lane 0 pulls its index,
@@ -293,38 +293,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         return out.valid != 0;
       };
-      // K/V of this CTA's j-th item into buffer j % KVB, once item j - KVB's S/dP MMAs are done
-      // with it
-      auto load_kv = [&](const KvItem& J, int j) -> bool {
-        const int kb = j % C::KVB;
-        if (!wwait(bar(C::B_KVE + kb), ((j / C::KVB) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
-        mbar_expect_tx_w(bar(C::B_KVF + kb), 2 * C::TKV);
-        for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d_w(base + C::kv_off(kb) + pn * C::PKV, &tk, bar(C::B_KVF + kb), pn * 64, J.hk,
-                      (X ? J.s0k : J.s0) + J.n * 128);
-          tma_load_3d_w(base + C::kv_off(kb) + C::TKV + pn * C::PKV, &tv, bar(C::B_KVF + kb), pn * 64,
-                      J.hk, (X ? J.s0k : J.s0) + J.n * 128);
-        }
-        kv_issued = j + 1;
+      // K of this CTA's j-th item into buffer j & 1, once item j-2's S^T MMAs are done with it
+      auto load_k = [&](const KvItem& J, int j) -> bool {
+        const int kb = j & 1;
+        if (!wwait(bar(C::B_KE + kb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 21)) return false;
+        mbar_expect_tx_w(bar(C::B_KF + kb), C::TKV);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d_w(base + kb * C::TKV + pn * C::PKV, &tk, bar(C::B_KF + kb), pn * 64, J.hk,
+                        (X ? J.s0k : J.s0) + J.n * 128);
+        k_issued = j + 1;
+        return true;
+      };
+      // V of this CTA's j-th item into the V buffer, once item j-1's dP^T MMAs are done with it
+      auto load_v = [&](const KvItem& J, int j) -> bool {
+        if (!wwait(bar(C::B_VE), (j & 1) ^ 1, abort_flag, p.hdr, 20)) return false;
+        mbar_expect_tx_w(bar(C::B_VF), C::TKV);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d_w(base + C::V_OFF + pn * C::PKV, &tv, bar(C::B_VF), pn * 64, J.hk,
+                        (X ? J.s0k : J.s0) + J.n * 128);
+        v_issued = j + 1;
         return true;
       };
       bool more = TOK ? publish(0, nxt, ok)
                       : queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec, nxt,
                                         abort_flag, p.hdr, ok);
-      if (ok && more) ok = load_kv(nxt, 0);
+      if (ok && more) ok = load_k(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const KvItem I = nxt;  // publish the next record first: its decode overlaps this one
         more = TOK ? publish(item_cnt + 1, nxt, ok)
                    : queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.kv_counter, n_items, dec,
                                      nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
-        // the next item's K/V goes out right after this item's first two Q/dO steps, a whole
-        // item ahead of its use (two buffers), or after all of them (one buffer: it waits for
-        // this item's last S/dP MMAs, which need those steps)
-        const int kv_at = C::KVB == 1 ? I.steps : (I.steps < 2 ? I.steps : 2);
+        // This item's first two Q/dO steps, then its V (which waits for the previous item's last
+        // dP^T MMA), then the next item's K (a whole item ahead of its use) and the remaining
+        // steps.
+        const int kv_at = I.steps < 2 ? I.steps : 2;
         for (int i = 0; ok && i <= I.steps; ++i) {
-          if (i == kv_at && more) {
-            ok = load_kv(nxt, item_cnt + 1);
+          if (i == kv_at) {
+            ok = load_v(I, item_cnt) && (!more || load_k(nxt, item_cnt + 1));
             if (!ok) break;
           }
           if (i == I.steps) break;
@@ -343,8 +349,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) {
         // let every copy this thread started land before the CTA exits
-        for (int j = kv_issued - 1; j >= 0 && j >= kv_issued - C::KVB; --j)
-          drain_wait_b(bar(C::B_KVF + j % C::KVB), (j / C::KVB) & 1);
+        for (int j = k_issued - 1; j >= 0 && j >= k_issued - 2; --j)
+          drain_wait_b(bar(C::B_KF + (j & 1)), (j >> 1) & 1);
+        if (v_issued > 0) drain_wait_b(bar(C::B_VF), (v_issued - 1) & 1);
         for (int i = qit - 1; i >= 0 && i >= qit - C::QST; --i)
           drain_wait_b(bar(C::B_QF + i % C::QST), (i / C::QST) & 1);
       }
@@ -362,13 +369,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t kvlo0 = sdesc_lo(base, 16);                 // K/V, K-major A
       const uint32_t ringK0 = sdesc_lo(base + C::RING_OFF, 16);    // Q/dO as K-major B
       const uint32_t ringM0 = sdesc_lo(base + C::RING_OFF, C::PQ); // Q/dO as MN-major B
-      auto issue_SdP = [&](int x, int slot) {
+      // S^T and dP^T of one step into buffer x; the item's first step first waits for its V
+      auto issue_SdP = [&](int x, int slot, bool wait_v) -> bool {
         const uint32_t qd = ringK0 + ((slot * 2 * C::TQ) >> 4), dd = qd + (C::TQ >> 4);
-        const uint32_t kd = kvlo0 + (C::kv_off(kb) >> 4), vd = kd + (C::TKV >> 4);
+        const uint32_t kd = kvlo0 + ((kb * C::TKV) >> 4), vd = kvlo0 + (C::V_OFF >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t okv = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4, oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4;
           mma_ss_w(tmem + x * 64, kd + okv, qd + oq, idS, kk > 0);
+        }
+        if (wait_v) {
+          if (!wwait(bar(C::B_VF), item_cnt & 1, abort_flag, p.hdr, 20)) return false;
+          fence_after_sync();
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -376,6 +388,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss_w(tmem + 128 + x * 64, vd + okv, dd + oq, idS, kk > 0);
         }
         mma_commit_w(bar(C::B_SF + x));
+        return true;
       };
       for (;; ++item_cnt) {
         KvItem I;
@@ -383,18 +396,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool all_ok = __all_sync(0xffffffffu, ok);
         if (!all_ok) ok = false;
         if (!all_ok || !got_) break;
-        kb = item_cnt % C::KVB;
-        ok = wwait(bar(C::B_KVF + kb), (item_cnt / C::KVB) & 1, abort_flag, p.hdr, 23);
+        kb = item_cnt & 1;
+        ok = wwait(bar(C::B_KF + kb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 23);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.steps; ++j) {
           const int s = (qit + j) % C::QST;
           ok = wwait(bar(C::B_QF + s), ((qit + j) / C::QST) & 1, abort_flag, p.hdr, 24);
           if (!ok) break;
           fence_after_sync();
-          issue_SdP(j, s);
+          ok = issue_SdP(j, s, j == 0);
         }
         if (!ok) break;
-        if (I.steps <= 2) mma_commit_w(bar(C::B_KVE + kb));
+        if (I.steps <= 2) {  // the item's last S^T / dP^T MMAs: its K and V buffers may be reloaded
+          mma_commit_w(bar(C::B_KE + kb));
+          mma_commit_w(bar(C::B_VE));
+        }
         for (int i = 0; ok && i < I.steps; ++i) {
           const int x = i & 1, s = (qit + i) % C::QST;
           ok = wwait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 25);
@@ -421,8 +437,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ok = wwait(bar(C::B_QF + s2), ((qit + i + 2) / C::QST) & 1, abort_flag, p.hdr, 27);
             if (!ok) break;
             fence_after_sync();
-            issue_SdP(x, s2);
-            if (i + 2 == I.steps - 1) mma_commit_w(bar(C::B_KVE + kb));
+            issue_SdP(x, s2, false);
+            if (i + 2 == I.steps - 1) {
+              mma_commit_w(bar(C::B_KE + kb));
+              mma_commit_w(bar(C::B_VE));
+            }
           }
         }
         if (!ok) break;
