@@ -709,20 +709,23 @@ namespace {
 template <int D>
 struct QCfg {
   static constexpr int QB = 128, KB = 64;
-  static constexpr int KST = D == 128 ? 3 : 8;   // K/V ring slots (one step each)
+  // Two Q buffers (items alternate: the next item's Q loads a whole item ahead), one dO
+  // buffer (the next item's dO loads once this item's last dP MMA is done, about two steps
+  // before it is needed) and a K/V ring of KST slots (one step each).  At d = 128 the single
+  // dO buffer is what leaves room for the ring's fourth slot.
+  static constexpr int KST = D == 128 ? 4 : 8;
   static constexpr int TQ = QB * D * 2, TKV = KB * D * 2;
   static constexpr int PQ = QB * 128, PKV = KB * 128;
-  // two Q/dO buffers (items alternate): buffer b holds Q at qd_off(b), dO right after
-  static constexpr int RING_OFF = 4 * TQ;
+  static constexpr int DO_OFF = 2 * TQ;          // Q buffers at 0 and TQ, then dO
+  static constexpr int RING_OFF = 3 * TQ;
   static constexpr int BAR_OFF = RING_OFF + KST * 2 * TKV;
-  static constexpr int B_QDF = 0, B_QDE = 2, B_KF = 4, B_KE = 4 + KST, B_SF = 4 + 2 * KST,
+  static constexpr int B_QF = 0, B_QE = 2, B_DF = 4, B_DE = 5, B_KF = 6, B_KE = 6 + KST, B_SF = 6 + 2 * KST,
                        B_PF = B_SF + 2, B_AF = B_PF + 2, B_AE = B_AF + 2, B_DR = B_AE + 2,
                        B_IF = B_DR + 1, B_IE = B_IF + 2, NBAR = B_IE + 2;  // AF/AE: per dQ buffer
   static constexpr int QUEUE_OFF = BAR_OFF + NBAR * 8;  // two item slots
   static constexpr int ROWS_OFF = QUEUE_OFF + 2 * 48;   // four 128-byte row tables (item k & 3)
   static constexpr int MISC_OFF = ROWS_OFF + 4 * QB;
   static constexpr int SMEM = MISC_OFF + 16;     // the dynamic smem base is 1024-aligned
-  __host__ __device__ static constexpr uint32_t qd_off(int b) { return static_cast<uint32_t>(b) * 2 * TQ; }
 };
 static_assert(QCfg<128>::SMEM <= 232448 && QCfg<64>::SMEM <= 232448, "dQ shared memory");
 
@@ -832,9 +835,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::B_QDF + b), 1);
-      mbar_init(bar(C::B_QDE + b), 1);
+      mbar_init(bar(C::B_QF + b), 1);
+      mbar_init(bar(C::B_QE + b), 1);
     }
+    mbar_init(bar(C::B_DF), 1);
+    mbar_init(bar(C::B_DE), 1);
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bar(C::B_KF + s), 1);
       mbar_init(bar(C::B_KE + s), 1);
@@ -875,7 +880,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ TMA producer
     regs_dec<kRegsCtl>();
     {  // the whole warp runs the loop; elect.sync picks the issuing lane
-      int kit = 0, item_cnt = 0, qd_issued = 0;  // qd_issued: items whose Q/dO load went out
+      int kit = 0, item_cnt = 0, q_issued = 0, do_issued = 0;  // items whose Q / dO load went out
       bool ok = true;
       QItem nxt;
       // Publishes this CTA's k-th item (the next record of the map): lane 0 pulls its index,
@@ -906,36 +911,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         return out.valid != 0;
       };
-      // Q/dO of this CTA's j-th item into buffer j & 1, once item j-2's S/dP MMAs are done
-      // with it
-      auto load_qd = [&](const QItem& J, int j) -> bool {
+      // Q of this CTA's j-th item into buffer j & 1, once item j-2's S MMAs are done with it
+      auto load_q = [&](const QItem& J, int j) -> bool {
         const int qb = j & 1;
-        if (!wwait(bar(C::B_QDE + qb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 31)) return false;
-        mbar_expect_tx_w(bar(C::B_QDF + qb), 2 * C::TQ);
-        for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d_w(base + C::qd_off(qb) + pn * C::PQ, &tq, bar(C::B_QDF + qb), pn * 64, J.h,
-                      J.s0 + J.m * 128);
-          tma_load_3d_w(base + C::qd_off(qb) + C::TQ + pn * C::PQ, &tdo, bar(C::B_QDF + qb), pn * 64, J.h,
-                      J.s0 + J.m * 128);
-        }
-        qd_issued = j + 1;
+        if (!wwait(bar(C::B_QE + qb), ((j >> 1) & 1) ^ 1, abort_flag, p.hdr, 31)) return false;
+        mbar_expect_tx_w(bar(C::B_QF + qb), C::TQ);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d_w(base + qb * C::TQ + pn * C::PQ, &tq, bar(C::B_QF + qb), pn * 64, J.h, J.s0 + J.m * 128);
+        q_issued = j + 1;
+        return true;
+      };
+      // dO of this CTA's j-th item into the dO buffer, once item j-1's dP MMAs are done with it
+      auto load_do = [&](const QItem& J, int j) -> bool {
+        if (!wwait(bar(C::B_DE), (j & 1) ^ 1, abort_flag, p.hdr, 30)) return false;
+        mbar_expect_tx_w(bar(C::B_DF), C::TQ);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d_w(base + C::DO_OFF + pn * C::PQ, &tdo, bar(C::B_DF), pn * 64, J.h, J.s0 + J.m * 128);
+        do_issued = j + 1;
         return true;
       };
       bool more = TOK ? publish(0, nxt, ok)
                       : queue_publish_w(0, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec, nxt,
                                         abort_flag, p.hdr, ok);
-      if (ok && more) ok = load_qd(nxt, 0);
+      if (ok && more) ok = load_q(nxt, 0);
       for (; ok && more; ++item_cnt) {
         const QItem I = nxt;  // publish the next record first: its decode overlaps this one
         more = TOK ? publish(item_cnt + 1, nxt, ok)
                    : queue_publish_w(item_cnt + 1, queue, bar(C::B_IF), bar(C::B_IE), p.q_counter, n_items, dec,
                                      nxt, abort_flag, p.hdr, ok);
         if (!ok) break;
-        // the next item's Q/dO goes out right after this item's first two K/V steps
+        // This item's first two K/V steps, then its dO (which waits for the previous item's last
+        // dP MMA), then the next item's Q (a whole item ahead of its use) and the remaining steps.
         const int qd_at = I.nb < 2 ? I.nb : 2;
         for (int n = 0; ok && n <= I.nb; ++n) {
-          if (n == qd_at && more) {
-            ok = load_qd(nxt, item_cnt + 1);
+          if (n == qd_at) {
+            ok = load_do(I, item_cnt) && (!more || load_q(nxt, item_cnt + 1));
             if (!ok) break;
           }
           if (n == I.nb) break;
@@ -953,8 +963,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) {
         // let every copy this thread started land before the CTA exits
-        for (int j = qd_issued - 1; j >= 0 && j >= qd_issued - 2; --j)
-          drain_wait_b(bar(C::B_QDF + (j & 1)), (j >> 1) & 1);
+        for (int j = q_issued - 1; j >= 0 && j >= q_issued - 2; --j)
+          drain_wait_b(bar(C::B_QF + (j & 1)), (j >> 1) & 1);
+        if (do_issued > 0) drain_wait_b(bar(C::B_DF), (do_issued - 1) & 1);
         for (int i = kit - 1; i >= 0 && i >= kit - C::KST; --i)
           drain_wait_b(bar(C::B_KF + i % C::KST), (i / C::KST) & 1);
       }
@@ -972,13 +983,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t qlo0 = sdesc_lo(base, 16);                    // Q/dO, K-major A
       const uint32_t ringK0 = sdesc_lo(base + C::RING_OFF, 16);      // K/V as K-major B
       const uint32_t ringM0 = sdesc_lo(base + C::RING_OFF, C::PKV);  // K as MN-major B
-      auto issue_SdP = [&](int x, int slot) {
+      // S and dP of one step into buffer x; the item's first step first waits for its dO
+      auto issue_SdP = [&](int x, int slot, bool wait_do) -> bool {
         const uint32_t kd = ringK0 + ((slot * 2 * C::TKV) >> 4), vd = kd + (C::TKV >> 4);
-        const uint32_t qd = qlo0 + (C::qd_off(qb) >> 4), dd = qd + (C::TQ >> 4);
+        const uint32_t qd = qlo0 + ((qb * C::TQ) >> 4), dd = qlo0 + (C::DO_OFF >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = ((kk >> 2) * C::PQ + (kk & 3) * 32) >> 4, ok_ = ((kk >> 2) * C::PKV + (kk & 3) * 32) >> 4;
           mma_ss_w(tmem + x * 64, qd + oq, kd + ok_, idS, kk > 0);
+        }
+        if (wait_do) {
+          if (!wwait(bar(C::B_DF), item_cnt & 1, abort_flag, p.hdr, 30)) return false;
+          fence_after_sync();
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -986,6 +1002,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss_w(tmem + 128 + x * 64, dd + oq, vd + ok_, idS, kk > 0);
         }
         mma_commit_w(bar(C::B_SF + x));
+        return true;
       };
       for (;; ++item_cnt) {
         QItem I;
@@ -994,17 +1011,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!all_ok) ok = false;
         if (!all_ok || !got_) break;
         qb = item_cnt & 1;
-        ok = wwait(bar(C::B_QDF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 33);
+        ok = wwait(bar(C::B_QF + qb), (item_cnt >> 1) & 1, abort_flag, p.hdr, 33);
         if (!ok) break;
         for (int j = 0; ok && j < 2 && j < I.nb; ++j) {
           const int s = (kit + j) % C::KST;
           ok = wwait(bar(C::B_KF + s), ((kit + j) / C::KST) & 1, abort_flag, p.hdr, 34);
           if (!ok) break;
           fence_after_sync();
-          issue_SdP(j, s);
+          ok = issue_SdP(j, s, j == 0);
         }
         if (!ok) break;
-        if (I.nb <= 2) mma_commit_w(bar(C::B_QDE + qb));
+        if (I.nb <= 2) {  // the item's last S / dP MMAs: its Q and dO buffers may be reloaded
+          mma_commit_w(bar(C::B_QE + qb));
+          mma_commit_w(bar(C::B_DE));
+        }
         for (int n = 0; ok && n < I.nb; ++n) {
           const int x = n & 1, s = (kit + n) % C::KST;
           ok = wwait(bar(C::B_PF + x), (x ? pf1 : pf0) & 1, abort_flag, p.hdr, 35);
@@ -1028,8 +1048,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ok = wwait(bar(C::B_KF + s2), ((kit + n + 2) / C::KST) & 1, abort_flag, p.hdr, 37);
             if (!ok) break;
             fence_after_sync();
-            issue_SdP(x, s2);
-            if (n + 2 == I.nb - 1) mma_commit_w(bar(C::B_QDE + qb));
+            issue_SdP(x, s2, false);
+            if (n + 2 == I.nb - 1) {
+              mma_commit_w(bar(C::B_QE + qb));
+              mma_commit_w(bar(C::B_DE));
+            }
           }
         }
         if (!ok) break;
