@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       holding = true;
       return true;
     };
-    KvItem J;          // the first token item, once the segment loop has met it
+    KvItem J{};        // the first token item, once the segment loop has met it
     bool tok = false;
     for (;; ++item_cnt) {
       KvItem I;
@@ -812,6 +812,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  const BwdParams p) {
+  // Launched as a programmatic dependent of the dK/dV kernel: it reads none of that kernel's
+  // results (its maps, D and status were final before the dK/dV kernel passed its own wait),
+  // so it starts without waiting, on SMs as dK/dV CTAs finish.  Every thread waits for the
+  // dK/dV grid on its way out, so this grid completes only after that one and the work that
+  // follows in the stream sees both.
+  struct WaitOnExit {
+    __device__ ~WaitOnExit() { griddep_wait(); }
+  } const wait_on_exit;
   using C = QCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);

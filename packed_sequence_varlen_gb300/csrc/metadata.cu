@@ -58,7 +58,8 @@ __device__ __forceinline__ int block_inclusive_scan(int x, int* warp_sums) {
 
 // One block: exclusive scan of the lengths into cu[0..n], tail pad into cu[n+1]; with
 // inline_fill (metadata_inline_fill) also position_ids and segment_ids, as the fill kernel
-// would write them.
+// would write them.  Up to 32 lengths one warp scans them in registers: the launch runs once
+// per call on cold instruction caches, and that path is a small fraction of the block scan's.
 __global__ void __launch_bounds__(kScanThreads)
     metadata_scan_kernel(const int32_t* __restrict__ lengths, int n, int pad_to,
                          int T_capacity, int32_t* __restrict__ cu, int32_t* __restrict__ max_out,
@@ -68,42 +69,66 @@ __global__ void __launch_bounds__(kScanThreads)
   __shared__ int carry, mx, bad;
   __shared__ int s_cu[kInlineSegs + 2];
   griddep_begin();  // the lengths may come from the kernel just before
-  if (threadIdx.x == 0) {
-    carry = 0;
-    mx = 0;
-    bad = 0;
-    cu[0] = 0;
-    s_cu[0] = 0;
-  }
-  __syncthreads();
-  for (int base = 0; base < n; base += kScanThreads) {
-    const int i = base + threadIdx.x;
-    const int L = i < n ? lengths[i] : 0;
-    if (i < n && L <= 0) atomicOr(&bad, 1);
-    if (i < n) atomicMax(&mx, L);
-    const int incl = block_inclusive_scan(L, warp_sums);
-    if (i < n) {
-      cu[i + 1] = carry + incl;
-      if (inline_fill) s_cu[i + 1] = carry + incl;
-    }
-    __syncthreads();
-    if (threadIdx.x == kScanThreads - 1) carry += incl;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const int total = carry;
+  // (one thread) the pad segment, the capacity check and the scalar outputs
+  auto finish = [&](int total, int m, int b) {
     int last = total;
     if (pad_to > total) {
       last = pad_to;
-      mx = max(mx, pad_to - total);
+      m = max(m, pad_to - total);
     } else if (pad_to > 0 && pad_to < total) {
-      bad = 1;
+      b = 1;
     }
-    if (last > T_capacity) bad = 1;
+    if (last > T_capacity) b = 1;
     cu[n + 1] = last;
     if (inline_fill) s_cu[n + 1] = last;
-    *max_out = mx;
-    *status = bad ? VA_ERR_BAD_SEQLENS : VA_OK;
+    *max_out = m;
+    *status = b ? VA_ERR_BAD_SEQLENS : VA_OK;
+    bad = b;
+  };
+  if (n <= 32) {  // one warp scans in registers: no block barriers or shared-memory atomics
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const int L = lane < n ? lengths[lane] : 0;
+      int incl = L;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int m = __reduce_max_sync(0xffffffffu, L);
+      const int b = __any_sync(0xffffffffu, lane < n && L <= 0) ? 1 : 0;
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane < n) cu[lane + 1] = s_cu[lane + 1] = incl;
+      if (lane == 0) {
+        cu[0] = 0;
+        s_cu[0] = 0;
+        finish(total, m, b);
+      }
+    }
+  } else {
+    if (threadIdx.x == 0) {
+      carry = 0;
+      mx = 0;
+      bad = 0;
+      cu[0] = 0;
+      s_cu[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < n; base += kScanThreads) {
+      const int i = base + threadIdx.x;
+      const int L = i < n ? lengths[i] : 0;
+      if (i < n && L <= 0) atomicOr(&bad, 1);
+      if (i < n) atomicMax(&mx, L);
+      const int incl = block_inclusive_scan(L, warp_sums);
+      if (i < n) {
+        cu[i + 1] = carry + incl;
+        if (inline_fill) s_cu[i + 1] = carry + incl;
+      }
+      __syncthreads();
+      if (threadIdx.x == kScanThreads - 1) carry += incl;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) finish(carry, mx, bad);
   }
   if (!inline_fill) return;
   __syncthreads();

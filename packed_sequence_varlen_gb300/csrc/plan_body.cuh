@@ -268,7 +268,13 @@ constexpr int kSmemSegs = 4096;
 
 constexpr int kNoClass = 32;  // class of a segment without records
 
+// The small-map path's table: the segments in map order (class descending, then index).
+struct SmallPlanTable {
+  int seg[32], off[33], nblk[32], len[32];
+};
+
 struct PlanSmem {
+  SmallPlanTable small;
   int scan[33];
   int overflow;
   int seg_total;
@@ -507,6 +513,130 @@ struct PlanPair {
   int Tk = 0, max_seqlen_k = 0;  // cross-attention (map[0].cu_k set): the K/V stream
 };
 
+// Maps of at most 32 segments without token tiles, local window or cross-attention: the
+// same records in the same order as plan_body, from a far shorter instruction path.  A
+// planning launch runs once per call on cold instruction caches, so its time goes mostly to
+// fetching instructions; the general path's ranking (class totals, bases, per-class scans)
+// took about 6 us of it on a 10-segment pack.  Here warp 0 checks the boundaries and ranks
+// the segments in registers (lane b holds segment b; its key is (31 - class, b), its first
+// record the sum of the records of the segments with smaller keys), and the block writes
+// the records, one per thread and pass.
+__device__ __forceinline__ bool small_plan_ok(const PlanPair& pp, int i0, int i1) {
+  if (pp.map[0].B < 1 || pp.map[0].B > 32) return false;
+  for (int i = i0; i < i1; ++i) {
+    const PlanArgs& a = pp.map[i];
+    if (a.cu_k || (a.causal && a.window >= 0) || token_mode(a)) return false;
+  }
+  return true;
+}
+
+template <class M>
+__device__ __forceinline__ void small_rank(const PlanArgs& a, int lane, int l, SmallPlanTable& t, int& total) {
+  int nblk = 0, cost = 0;
+  if (lane < a.B) seg_cost<M>(a, l, l, nblk, cost);
+  const int n = nblk * a.heads;
+  const unsigned key = lane < a.B ? (static_cast<unsigned>(31 - cost_class(cost)) << 5) | lane : 0xffffffffu;
+  int rank = 0, off = 0;
+#pragma unroll 4
+  for (int j = 0; j < 32; ++j) {
+    const unsigned kj = __shfl_sync(0xffffffffu, key, j);
+    const int nj = __shfl_sync(0xffffffffu, n, j);
+    if (kj < key) {
+      ++rank;
+      off += nj;
+    }
+  }
+  total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n)));
+  if (lane < a.B) {
+    t.seg[rank] = lane;
+    t.off[rank] = off;
+    t.nblk[rank] = nblk;
+    t.len[rank] = l;
+  }
+  if (lane == 0) t.off[a.B] = total;
+}
+
+template <class M>
+__device__ __forceinline__ void small_write(const PlanArgs& a, const SmallPlanTable& t, int total) {
+  for (int r = threadIdx.x; r < total; r += blockDim.x) {
+    int k = 0;  // the segment (in map order) that holds record r
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+      if (k + step < a.B && t.off[k + step] <= r) k += step;
+    const int rr = r - t.off[k], nb = t.nblk[k], h = rr / nb, j = rr - h * nb;
+    TileItem it;
+    seg_record<M>(a, t.len[k], t.len[k], nb, j, it.blk, it.count);
+    it.seg = t.seg[k];
+    it.head = h;
+    a.out[r] = it;
+  }
+}
+
+// Every thread of the block calls it; the block's shared state is sh.small and the two ints
+// after it.
+__device__ __forceinline__ void small_plan(const PlanPair& pp, PlanSmem& sh, int i0, int i1) {
+  const PlanArgs& a0 = pp.map[0];
+  const int lane = threadIdx.x & 31;
+  int l = 0, bad = 0;
+  if (threadIdx.x < 32) {
+    int x = 0, y = 0;
+    if (lane < a0.B) {
+      x = a0.cu[lane];
+      y = a0.cu[lane + 1];
+      l = y - x;
+      if (y <= x || l > pp.max_seqlen) bad = 1;
+      if (lane == 0 && x != 0) bad = 1;
+      if (lane == a0.B - 1 && y != pp.T) bad = 1;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) sh.overflow = bad;
+  }
+  __syncthreads();
+  if (sh.overflow) {  // the boundaries break the contract
+    if (threadIdx.x == 0) {
+      if (i0 == 0) *a0.status = VA_ERR_BAD_SEQLENS;
+      for (int i = i0; i < i1; ++i) {
+        *pp.map[i].n_items = 0;
+        if (pp.map[i].n_tok) *pp.map[i].n_tok = 0;
+      }
+    }
+    return;
+  }
+  if (threadIdx.x == 0 && i0 == 0) *a0.status = VA_OK;
+  for (int i = i0; i < i1; ++i) {
+    const PlanArgs& a = pp.map[i];
+    __syncthreads();  // the table of the previous map has been read
+    if (threadIdx.x < 32) {
+      int total = 0;
+      if (a.kind == 1) {
+        if (a.causal) small_rank<MapKind<true, true, false>>(a, lane, l, sh.small, total);
+        else small_rank<MapKind<true, false, false>>(a, lane, l, sh.small, total);
+      } else {
+        if (a.causal) small_rank<MapKind<false, true, false>>(a, lane, l, sh.small, total);
+        else small_rank<MapKind<false, false, false>>(a, lane, l, sh.small, total);
+      }
+      if (lane == 0) {
+        const bool overflow = total > a.capacity;
+        *a.n_items = overflow ? 0 : total;
+        *a.counter = 0;
+        if (a.n_tok) *a.n_tok = 0;
+        if (a.tok_counter) *a.tok_counter = 0;
+        if (overflow && a.status) atomicCAS(a.status, VA_OK, VA_ERR_WORKSPACE);
+        sh.seg_total = overflow ? 0 : total;
+      }
+    }
+    __syncthreads();
+    const int total = sh.seg_total;
+    if (a.kind == 1) {
+      if (a.causal) small_write<MapKind<true, true, false>>(a, sh.small, total);
+      else small_write<MapKind<true, false, false>>(a, sh.small, total);
+    } else {
+      if (a.causal) small_write<MapKind<false, true, false>>(a, sh.small, total);
+      else small_write<MapKind<false, false, false>>(a, sh.small, total);
+    }
+  }
+}
+
 // Copies cu[0..B] into shared memory when it fits; returns the array to read.
 __device__ __forceinline__ const int* stage_cu(const int32_t* cu, int B, PlanSmem& sh) {
   if (B + 1 > kSmemSegs) return cu;
@@ -521,6 +651,10 @@ __device__ __forceinline__ const int* stage_cu(const int32_t* cu, int B, PlanSme
 // the library sizes a map at (rows / tile + B) * heads records, which bounds the records of
 // any boundaries that pass the check, so the second CTA's map never writes the status word.
 __device__ __forceinline__ void validate_plan_body(const PlanPair& pp, PlanSmem& sh, int only = -1) {
+  if (small_plan_ok(pp, only < 0 ? 0 : only, only < 0 ? pp.nmaps : only + 1)) {
+    small_plan(pp, sh, only < 0 ? 0 : only, only < 0 ? pp.nmaps : only + 1);
+    return;
+  }
   const PlanArgs& a0 = pp.map[0];
   const int* cu = stage_cu(a0.cu, a0.B, sh);  // every map is built from the same boundaries
   int bad = 0;

@@ -132,6 +132,60 @@ def test_tile_maps_bit_exact(va, name, causal):
             assert np.array_equal(tm.cpu().numpy(), ref)
 
 
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+def call_maps(va, cu, Hq, Hkv, d, mx, causal):
+    """The maps the attention calls build for themselves (the forward's check + map launch,
+    the backward preparation's planning CTAs), read back from the calls' workspaces.  Layout:
+    a 256-byte header (int32 status, n_items[4], ...); a forward workspace then holds the
+    map; a backward one D [Hq, T] fp32, then the kv-block and the q-block maps, each at a
+    256-byte boundary and (rows / tile + B) * heads records long."""
+    T, B = int(cu[-1]), len(cu) - 1
+    cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    q = torch.zeros((T, Hq, d), dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros((T, Hkv, d), dtype=torch.bfloat16, device=DEV)
+    ws_f = torch.empty(va.workspace_size(T, B, Hq, Hkv, d, mx, False), dtype=torch.uint8, device=DEV)
+    ws_b = torch.empty(va.workspace_size(T, B, Hq, Hkv, d, mx, True), dtype=torch.uint8, device=DEV)
+    o, lse = va.varlen_attn_fwd(q, k, k, cud, mx, causal=causal, workspace=ws_f, check_status=True)
+    va.varlen_attn_bwd(q, k, k, o, lse, q, cud, mx, causal=causal, workspace=ws_b, check_status=True)
+    torch.cuda.synchronize()
+
+    def records(ws, n_slot, at):
+        n = int(ws[4 * (1 + n_slot):4 * (2 + n_slot)].view(torch.int32).item())
+        return ws[at:at + 16 * n].view(torch.int32).reshape(n, 4).cpu().numpy()
+
+    _, BN_kv = va.tile_sizes(1, d)
+    kvmap = _align256(256 + Hq * T * 4)
+    qmap = _align256(kvmap + (T // BN_kv + B) * Hkv * 16)
+    return {0: records(ws_f, 0, 256), 1: records(ws_b, 1, kvmap), 2: records(ws_b, 2, qmap)}
+
+
+@pytest.mark.parametrize("name", ["tiny", "sft8k", "gqa16k", "long64k", "tiny4k"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_call_maps_bit_exact(va, name, causal):
+    """Packs of at most 32 segments take the planner's short path, the rest the general one;
+    both must build the maps the oracle lists, record for record."""
+    w = si.WORKLOADS[name]
+    for lengths in wl.packs(name)[:2]:
+        cu, _, _, mx = op.build_metadata(lengths)
+        got = call_maps(va, cu, w.Hq, w.Hkv, w.d, mx, causal)
+        for kind in (0, 1, 2):
+            assert np.array_equal(got[kind], oracle_map(va, kind, cu, w.Hq, w.Hkv, w.d, causal)), kind
+
+
+@pytest.mark.parametrize("B", [1, 2, 31, 32, 33])
+def test_call_maps_around_the_short_path_limit(va, B):
+    rng = np.random.default_rng(100 + B)
+    lengths = rng.integers(1, 700, size=B).tolist()
+    cu, _, _, mx = op.build_metadata(lengths)
+    for causal in (True, False):
+        got = call_maps(va, cu, 4, 2, 64, mx, causal)
+        for kind in (0, 1, 2):
+            assert np.array_equal(got[kind], oracle_map(va, kind, cu, 4, 2, 64, causal)), (kind, causal)
+
+
 # ------------------------------------------------------------------ small cases
 
 def test_tiny_page_layout_and_merge(va):
