@@ -18,12 +18,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 // One launch per attention call: checks the cu_seqlens contract (cu[0] == 0,
 // cu[B] == T, strictly increasing, every length <= max_seqlen), writes the status
 // word (OK or VA_ERR_BAD_SEQLENS), and only if it holds builds the call's maps.
-// 512 threads: on a pack of ~10 segments (one warp ranks them) the launch took 0.7 us less
-// than with 1024 (fewer warps at each block barrier) and as little as with 256, which writes
-// the records of larger maps in more passes.
-constexpr int kValidatePlanThreads = 512;
+// Packs of at most 32 segments (the planner's short path) get 512 threads: on ~10 segments
+// the launch took 0.7 us less than with 1024 (fewer warps at each block barrier) and as
+// little as with 256, which writes larger maps in more passes.  Larger packs keep 1024, so
+// the general path ranks them in as few rounds as it can.
+constexpr int kSmallPlanThreads = 512;
 
-__global__ void __launch_bounds__(kValidatePlanThreads) validate_plan_kernel(PlanPair pp) {
+__global__ void __launch_bounds__(kPlanThreads) validate_plan_kernel(PlanPair pp) {
   __shared__ PlanSmem sh;
   griddep_begin();  // cu_seqlens may come from the metadata kernels just before
   validate_plan_body(pp, sh);
@@ -43,7 +44,8 @@ cudaError_t launch_validate_plan(const PlanArgs* maps, int nmaps, int T, int max
   pp.max_seqlen = max_seqlen;
   pp.Tk = Tk;
   pp.max_seqlen_k = max_seqlen_k;
-  return launch_pdl(validate_plan_kernel, dim3(1), dim3(kValidatePlanThreads), 0, st, pp);
+  const int threads = nmaps >= 1 && maps[0].B <= 32 ? kSmallPlanThreads : kPlanThreads;
+  return launch_pdl(validate_plan_kernel, dim3(1), dim3(threads), 0, st, pp);
 }
 
 }  // namespace va
