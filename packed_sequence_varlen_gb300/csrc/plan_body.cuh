@@ -572,8 +572,8 @@ __device__ __forceinline__ void small_write(const PlanArgs& a, const SmallPlanTa
   }
 }
 
-// Every thread of the block calls it; the block's shared state is sh.small and the two ints
-// after it.
+// Every thread of the block calls it.  Shared state: sh.small (the table), sh.overflow (the
+// boundary check's verdict) and sh.seg_total (the current map's record count).
 __device__ __forceinline__ void small_plan(const PlanPair& pp, PlanSmem& sh, int i0, int i1) {
   const PlanArgs& a0 = pp.map[0];
   const int lane = threadIdx.x & 31;
