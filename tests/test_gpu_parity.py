@@ -175,10 +175,12 @@ def test_call_maps_bit_exact(va, name, causal):
             assert np.array_equal(got[kind], oracle_map(va, kind, cu, w.Hq, w.Hkv, w.d, causal)), kind
 
 
-@pytest.mark.parametrize("B", [1, 2, 31, 32, 33])
+@pytest.mark.parametrize("B", [1, 2, 31, 32, 33, -20])
 def test_call_maps_around_the_short_path_limit(va, B):
-    rng = np.random.default_rng(100 + B)
-    lengths = rng.integers(1, 700, size=B).tolist()
+    """B < 0: -B segments of at most 64 tokens (token tiles, so the general path even for
+    few segments)."""
+    rng = np.random.default_rng(100 + abs(B))
+    lengths = (rng.integers(1, 700, size=B) if B > 0 else rng.integers(1, 65, size=-B)).tolist()
     cu, _, _, mx = op.build_metadata(lengths)
     for causal in (True, False):
         got = call_maps(va, cu, 4, 2, 64, mx, causal)
